@@ -1,0 +1,272 @@
+"""Python binding of the Occult GB300 C ABI (``include/occult.h``).
+
+Argument marshalling only: every function below has the name of a C entry
+point, checks that the tensors it is handed are CUDA tensors of the expected
+dtype and size, and passes their device pointers and the current CUDA stream to
+``liboccult.so``.  Every step of the layer runs in the library's kernels; there
+is no CPU or PyTorch fallback, and importing a function raises if the library
+has not been built (``python -m combine_top_route_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "liboccult.so")
+
+OCCULT_F32 = 0
+OCCULT_BF16 = 1
+ROUTE_EXACT = 0
+ROUTE_DEVICE_LIMITED = 1
+MAX_EXPERTS = 256
+MAX_VDEV = 32
+MAX_TOPK = 16
+
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_DEVICE_TIMEOUT = -5
+
+
+class occult_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "T", "d", "n_experts", "top_k", "inter", "n_vdev", "dtype", "route_mode",
+        "limit_devices", "renorm", "n_shared", "shared_inter", "shared_gate")]
+
+    @property
+    def n_loc(self) -> int:
+        return self.n_experts // self.n_vdev
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == OCCULT_BF16 else torch.float32
+
+    def replace(self, **kw) -> "occult_desc_t":
+        out = occult_desc_t()
+        for n, _ in self._fields_:
+            setattr(out, n, kw.get(n, getattr(self, n)))
+        return out
+
+
+class OccultError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.code = code
+
+
+_VP = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_D = ctypes.POINTER(occult_desc_t)
+_SIGNATURES = {
+    "occult_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "occult_check_desc": (ctypes.c_int, [_D]),
+    "occult_workspace_size": (ctypes.c_int, [_D, _I32, ctypes.POINTER(ctypes.c_size_t)]),
+    "occult_device_error": (ctypes.c_int, [ctypes.POINTER(_I32)]),
+    "occult_place": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP]),
+    "occult_route": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_build_brim": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                         _VP, _VP]),
+    "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                         _VP]),
+    "occult_shared_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_combine": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
+                                            ctypes.c_size_t, _VP]),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m combine_top_route_gb300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(h, name)
+            f.restype = res
+            f.argtypes = args
+        _lib_handle = h
+    return _lib_handle
+
+
+def strerror(code: int) -> str:
+    return lib().occult_strerror(code).decode()
+
+
+def _call(name: str, *args) -> None:
+    rc = getattr(lib(), name)(*args)
+    if rc != 0:
+        raise OccultError(name, rc)
+
+
+def _dev(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, numel: Optional[int] = None,
+         name: str = "tensor", nullable: bool = False):
+    """Device pointer of a contiguous CUDA tensor (checked), or None."""
+    if t is None:
+        if nullable:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def check_desc(desc: occult_desc_t) -> int:
+    return lib().occult_check_desc(ctypes.byref(desc))
+
+
+def device_error() -> int:
+    code = _I32(0)
+    _call("occult_device_error", ctypes.byref(code))
+    return code.value
+
+
+def workspace_size(desc: occult_desc_t, n_tok: int) -> int:
+    n = ctypes.c_size_t(0)
+    _call("occult_workspace_size", ctypes.byref(desc), n_tok, ctypes.byref(n))
+    return n.value
+
+
+def occult_place(C, n_vdev: int):
+    """Algorithm 1 on host counts C [Ne, Ne] (int64, CPU).  Returns (placement, expert_to_vdev)."""
+    C = torch.as_tensor(C, dtype=torch.int64).contiguous()
+    Ne = C.shape[0]
+    placement = torch.empty(n_vdev, Ne // n_vdev, dtype=torch.int32)
+    e2v = torch.empty(Ne, dtype=torch.int32)
+    _call("occult_place", ctypes.c_void_p(C.data_ptr()), Ne, n_vdev,
+          ctypes.c_void_p(placement.data_ptr()), ctypes.c_void_p(e2v.data_ptr()))
+    return placement, e2v
+
+
+def occult_route(desc, logits, expert_to_vdev, ids, gates, vmask, stream=None):
+    T, Ne, k = desc.T, desc.n_experts, desc.top_k
+    _call("occult_route", ctypes.byref(desc), _dev(logits, torch.float32, T * Ne, "logits"),
+          _dev(expert_to_vdev, torch.int32, Ne, "expert_to_vdev"),
+          _dev(ids, torch.int32, T * k, "ids"), _dev(gates, torch.float32, T * k, "gates"),
+          _dev(vmask, torch.int32, T, "vmask"), _stream(stream))
+
+
+def occult_build_brim(desc, ids, gates, vmask, placement, brim0, seg_off, brim1, exp_off,
+                      epd_src, epd_gate, counts, stream=None):
+    T, Ne, k, Nd = desc.T, desc.n_experts, desc.top_k, desc.n_vdev
+    i32, f32 = torch.int32, torch.float32
+    _call("occult_build_brim", ctypes.byref(desc), _dev(ids, i32, T * k, "ids"),
+          _dev(gates, f32, T * k, "gates"), _dev(vmask, i32, T, "vmask"),
+          _dev(placement, i32, Ne, "placement"), _dev(brim0, i32, Nd * T, "brim0"),
+          _dev(seg_off, i32, Nd + 1, "seg_off"), _dev(brim1, i32, Ne * T, "brim1"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(epd_gate, f32, T * k, "epd_gate"), _dev(counts, i32, 4, "counts"),
+          _stream(stream))
+
+
+def occult_dispatch(desc, x, brim0, vmask, x_sfd, sfd_tok=None, stream=None):
+    T, d, Nd = desc.T, desc.d, desc.n_vdev
+    dt = desc.torch_dtype
+    n_sfd_max = T * min(desc.top_k, Nd)
+    _call("occult_dispatch", ctypes.byref(desc), _dev(x, dt, T * d, "x"),
+          _dev(brim0, torch.int32, Nd * T, "brim0"), _dev(vmask, torch.int32, T, "vmask"),
+          _dev(x_sfd, dt, n_sfd_max * d, "x_sfd"),
+          _dev(sfd_tok, torch.int32, n_sfd_max, "sfd_tok", nullable=True), _stream(stream))
+
+
+def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt = desc.torch_dtype
+    _call("occult_expert_up", ctypes.byref(desc),
+          _dev(x_sfd, dt, T * min(k, desc.n_vdev) * d, "x_sfd"),
+          _dev(epd_src, torch.int32, T * k, "epd_src"),
+          _dev(epd_gate, torch.float32, T * k, "epd_gate"),
+          _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
+          _dev(placement, torch.int32, Ne, "placement"),
+          _dev(w1, dt, Ne * 2 * I * d, "w1"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _stream(stream))
+
+
+def occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt = desc.torch_dtype
+    _call("occult_expert_down", ctypes.byref(desc), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
+          _dev(placement, torch.int32, Ne, "placement"), _dev(w2, dt, Ne * d * I, "w2"),
+          _dev(y_epd, dt, T * k * d, "y_epd"), _stream(stream))
+
+
+def occult_expert_ffn(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd, y_epd,
+                      stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt = desc.torch_dtype
+    _call("occult_expert_ffn", ctypes.byref(desc),
+          _dev(x_sfd, dt, T * min(k, desc.n_vdev) * d, "x_sfd"),
+          _dev(epd_src, torch.int32, T * k, "epd_src"),
+          _dev(epd_gate, torch.float32, T * k, "epd_gate"),
+          _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
+          _dev(placement, torch.int32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
+          _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(y_epd, dt, T * k * d, "y_epd"), _stream(stream))
+
+
+def occult_shared_ffn(desc, x, ws1, ws2, w_sg, h_s, s_gate, y_s, stream=None):
+    T, d = desc.T, desc.d
+    S = desc.n_shared * desc.shared_inter
+    dt = desc.torch_dtype
+    _call("occult_shared_ffn", ctypes.byref(desc), _dev(x, dt, T * d, "x"),
+          _dev(ws1, dt, 2 * S * d, "ws1"), _dev(ws2, dt, d * S, "ws2"),
+          _dev(w_sg, dt, d, "w_sg", nullable=not desc.shared_gate),
+          _dev(h_s, dt, T * S, "h_s"),
+          _dev(s_gate, torch.float32, T, "s_gate", nullable=not desc.shared_gate),
+          _dev(y_s, dt, T * d, "y_s"), _stream(stream))
+
+
+def occult_combine(desc, y_epd, brim0, seg_off, brim1, exp_off, y, y_shared=None, y_sfd=None,
+                   stream=None):
+    T, d, Ne, k, Nd = desc.T, desc.d, desc.n_experts, desc.top_k, desc.n_vdev
+    dt = desc.torch_dtype
+    i32 = torch.int32
+    _call("occult_combine", ctypes.byref(desc), _dev(y_epd, dt, T * k * d, "y_epd"),
+          _dev(brim0, i32, Nd * T, "brim0"), _dev(seg_off, i32, Nd + 1, "seg_off"),
+          _dev(brim1, i32, Ne * T, "brim1"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(y_shared, dt, T * d, "y_shared", nullable=True),
+          _dev(y_sfd, dt, T * min(k, Nd) * d, "y_sfd", nullable=True),
+          _dev(y, dt, T * d, "y"), _stream(stream))
+
+
+def occult_profile_coact(desc, ids, n_tok, C, ws, P=None, vmask=None, ct_hist=None,
+                         stream=None):
+    Ne, k = desc.n_experts, desc.top_k
+    max_ct = min(k, desc.n_vdev)
+    need = workspace_size(desc, n_tok)
+    _call("occult_profile_coact", ctypes.byref(desc), _dev(ids, torch.int32, n_tok * k, "ids",
+                                                            nullable=n_tok == 0),
+          n_tok, _dev(vmask, torch.int32, n_tok, "vmask", nullable=True),
+          _dev(C, torch.int64, Ne * Ne, "C"), _dev(P, torch.float32, Ne * Ne, "P", nullable=True),
+          _dev(ct_hist, torch.int64, max_ct + 1, "ct_hist", nullable=True),
+          _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
+          _stream(stream))
+
+
+from .pipeline import OccultMoE, desc_for  # noqa: E402  (needs the names above)

@@ -1,0 +1,238 @@
+// Row-movement kernels of the Occult pipeline (HBM-bound):
+//  * dispatch -- Appendix A.2 Algorithm 4, stage one of scattering (ORI -> SFD):
+//    each token row is read once and written to the SFD row BRIM0 gives it on
+//    every device it uses.
+//  * combine  -- the two-stage merge: stage one (EPD -> SFD) sums a received
+//    row's local experts (the aggregation of Algorithm 8, done without atomics),
+//    stage two (SFD -> ORI, Algorithm 9) sums the token's devices in order
+//    0..Nd-1.  Accumulation is fp32 in a fixed order, so results are
+//    deterministic.  Fused by default (one warp per token walks BRIM0 then
+//    BRIM1); a materialised mode writes the SFD stage-one result out (the second
+//    all-to-all's send buffer) and reads it back.
+// Rows move as 16-byte vectors (8 bf16 or 4 fp32); one warp per token row.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace occult {
+
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ brim0,
+                const uint32_t* __restrict__ vmask, int ntok, int Nd, int D,
+                T* __restrict__ x_sfd, int32_t* __restrict__ sfd_tok) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = D / Vec16<T>::N;
+  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < ntok; t += gridDim.x * kWarps) {
+    const uint32_t vm = vmask[t];
+    // SFD rows of this token, one per device it uses (at most 32)
+    int my_row = -1;
+    if (lane < Nd && ((vm >> lane) & 1u)) my_row = brim0[static_cast<size_t>(lane) * ntok + t];
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nvec) buf[u] = ld_nc_v4(src + v0 + 32 * u);
+      uint32_t rest = vm;
+      while (rest) {
+        const int d = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const int row = __shfl_sync(0xffffffffu, my_row, d);
+        uint4* dst = reinterpret_cast<uint4*>(x_sfd + static_cast<size_t>(row) * D);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v0 + 32 * u < nvec) st_v4(dst + v0 + 32 * u, buf[u]);
+      }
+    }
+    if (sfd_tok && my_row >= 0) sfd_tok[my_row] = t;
+  }
+}
+
+// Fused stage one + stage two: y[t] = sum_d (sum_j y_epd[...]) (+ y_shared[t]).
+// With y_sfd given, also writes each device's stage-one sum there.
+template <typename T, bool WRITE_SFD>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_fused_kernel(const T* __restrict__ y_epd, const int32_t* __restrict__ brim0,
+                     const int32_t* __restrict__ seg_off, const int32_t* __restrict__ brim1,
+                     const int32_t* __restrict__ exp_off, const T* __restrict__ y_shared, int ntok,
+                     int Nd, int n_loc, int D, T* __restrict__ y_sfd, T* __restrict__ y) {
+  constexpr int VN = Vec16<T>::N;
+  __shared__ int s_rows[kWarps][OCCULT_MAX_TOPK];
+  __shared__ int s_devs[kWarps][OCCULT_MAX_TOPK];
+  __shared__ int s_sfd[kWarps][OCCULT_MAX_VDEV];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nvec = D / VN;
+  for (int t = blockIdx.x * kWarps + warp; t < ntok; t += gridDim.x * kWarps) {
+    // Row list of the token in merge order (device ascending, then local
+    // expert in placement order): lane d walks device d's BRIM1 column, a warp
+    // scan of the per-device counts places every row.
+    int* rows = s_rows[warp];
+    int* devs = s_devs[warp];
+    int* sfd = s_sfd[warp];
+    int v0 = -1, c = 0;
+    if (lane < Nd) {
+      v0 = brim0[static_cast<size_t>(lane) * ntok + t];
+      if (v0 >= 0) {
+        const int r = v0 - seg_off[lane];
+        for (int j = 0; j < n_loc; ++j)
+          c += brim1[static_cast<size_t>(lane * n_loc + j) * ntok + r] >= 0;
+      }
+      sfd[lane] = v0;
+    }
+    int o = c;
+#pragma unroll
+    for (int sh = 1; sh < 32; sh <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, o, sh);
+      if (lane >= sh) o += u;
+    }
+    const int n = min(__shfl_sync(0xffffffffu, o, 31), OCCULT_MAX_TOPK);
+    o -= c;
+    if (c > 0) {
+      const int r = v0 - seg_off[lane];
+      const int base = exp_off[lane * n_loc];
+      for (int j = 0; j < n_loc; ++j) {
+        const int u = brim1[static_cast<size_t>(lane * n_loc + j) * ntok + r];
+        if (u >= 0 && o < OCCULT_MAX_TOPK) {
+          rows[o] = base + u;
+          devs[o] = lane;
+          ++o;
+        }
+      }
+    }
+    __syncwarp();
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[VN], part[VN], f[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f, part[i] = 0.f;
+      uint4 buf[OCCULT_MAX_TOPK];
+#pragma unroll
+      for (int j = 0; j < OCCULT_MAX_TOPK; ++j)
+        if (j < n) buf[j] = ld_nc_v4(reinterpret_cast<const uint4*>(y_epd + static_cast<size_t>(rows[j]) * D) + v);
+#pragma unroll
+      for (int j = 0; j < OCCULT_MAX_TOPK; ++j) {
+        if (j < n) {
+          unpack16(buf[j], f, T());
+#pragma unroll
+          for (int i = 0; i < VN; ++i) part[i] += f[i];
+          // close the device's stage-one sum at its last expert
+          if (j + 1 == n || devs[j + 1] != devs[j]) {
+            if (WRITE_SFD) {
+              st_v4(reinterpret_cast<uint4*>(y_sfd + static_cast<size_t>(sfd[devs[j]]) * D) + v,
+                    pack16(part, T()));
+            }
+#pragma unroll
+            for (int i = 0; i < VN; ++i) acc[i] += part[i], part[i] = 0.f;
+          }
+        }
+      }
+      if (y_shared) {
+        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_shared + static_cast<size_t>(t) * D) + v), f, T());
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += f[i];
+      }
+      st_v4(reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, T()));
+    }
+    __syncwarp();
+  }
+}
+
+// Stage two from a materialised SFD tensor: y[t] = sum_d y_sfd[brim0[d, t]] (+ shared).
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+combine_sfd_kernel(const T* __restrict__ y_sfd, const int32_t* __restrict__ brim0,
+                   const T* __restrict__ y_shared, int ntok, int Nd, int D, T* __restrict__ y) {
+  constexpr int VN = Vec16<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int nvec = D / VN;
+  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < ntok; t += gridDim.x * kWarps) {
+    int my_row = lane < Nd ? brim0[static_cast<size_t>(lane) * ntok + t] : -1;
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[VN], f[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+      for (int d = 0; d < Nd; ++d) {
+        const int row = __shfl_sync(0xffffffffu, my_row, d);
+        if (row < 0) continue;
+        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_sfd + static_cast<size_t>(row) * D) + v), f, T());
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += f[i];
+      }
+      if (y_shared) {
+        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_shared + static_cast<size_t>(t) * D) + v), f, T());
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += f[i];
+      }
+      st_v4(reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, T()));
+    }
+  }
+}
+
+int grid_for(const LaunchCtx& ctx, int ntok) {
+  int blocks = (ntok + kWarps - 1) / kWarps;
+  const int cap = ctx.num_sms * 8;
+  return blocks < cap ? (blocks > 0 ? blocks : 1) : cap;
+}
+
+}  // namespace
+
+int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
+                    const int32_t* brim0, const uint32_t* vmask, void* x_sfd, int32_t* sfd_tok) {
+  if (ds.T == 0) return OCCULT_OK;
+  const int g = grid_for(ctx, ds.T);
+  if (ds.dtype == OCCULT_BF16)
+    dispatch_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, ctx.stream>>>(
+        static_cast<const __nv_bfloat16*>(x), brim0, vmask, ds.T, ds.n_vdev, ds.d,
+        static_cast<__nv_bfloat16*>(x_sfd), sfd_tok);
+  else
+    dispatch_kernel<float><<<g, kWarps * 32, 0, ctx.stream>>>(
+        static_cast<const float*>(x), brim0, vmask, ds.T, ds.n_vdev, ds.d,
+        static_cast<float*>(x_sfd), sfd_tok);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const void* y_epd,
+                   const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
+                   const int32_t* exp_off, const void* y_shared, void* y_sfd, void* y) {
+  if (ds.T == 0) return OCCULT_OK;
+  const int g = grid_for(ctx, ds.T);
+  const int n_loc = ds.n_experts / ds.n_vdev;
+  if (ds.dtype == OCCULT_BF16) {
+    using T = __nv_bfloat16;
+    if (y_sfd) {
+      combine_fused_kernel<T, true><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev,
+          n_loc, ds.d, static_cast<T*>(y_sfd), static_cast<T*>(y));
+      combine_sfd_kernel<T><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_sfd), brim0, static_cast<const T*>(y_shared), ds.T, ds.n_vdev,
+          ds.d, static_cast<T*>(y));
+    } else {
+      combine_fused_kernel<T, false><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off,
+          static_cast<const T*>(y_shared), ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
+          static_cast<T*>(y));
+    }
+  } else {
+    using T = float;
+    if (y_sfd) {
+      combine_fused_kernel<T, true><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev,
+          n_loc, ds.d, static_cast<T*>(y_sfd), static_cast<T*>(y));
+      combine_sfd_kernel<T><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_sfd), brim0, static_cast<const T*>(y_shared), ds.T, ds.n_vdev,
+          ds.d, static_cast<T*>(y));
+    } else {
+      combine_fused_kernel<T, false><<<g, kWarps * 32, 0, ctx.stream>>>(
+          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off,
+          static_cast<const T*>(y_shared), ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
+          static_cast<T*>(y));
+    }
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace occult

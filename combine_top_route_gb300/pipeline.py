@@ -1,0 +1,110 @@
+"""The Occult MoE layer forward, Algorithm 2 of the paper, as a sequence of C-ABI calls.
+
+``OccultMoE`` owns the layer's weights, its expert placement and every buffer
+of the pipeline, sized for the worst case so that no step waits on the host:
+
+    route -> build BRIMs -> dispatch (ORI -> SFD, first all-to-all's send buffer)
+    -> expert_up (SFD -> EPD, SwiGLU, modulation) -> expert_down
+    -> [shared experts] -> combine (EPD -> SFD -> ORI)
+
+PyTorch only allocates the buffers and provides the stream; all work runs in
+the library's kernels.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, occult_build_brim,
+               occult_combine, occult_desc_t, occult_dispatch, occult_expert_down,
+               occult_expert_up, occult_route, occult_shared_ffn)
+
+
+def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
+    """Descriptor from any object with the layer-config attribute names."""
+    ds = occult_desc_t()
+    ds.T = cfg.T if T is None else T
+    ds.d = cfg.d
+    ds.n_experts = cfg.n_experts
+    ds.top_k = cfg.top_k
+    ds.inter = cfg.inter
+    ds.n_vdev = cfg.n_vdev
+    ds.dtype = OCCULT_BF16 if cfg.dtype == "bf16" else OCCULT_F32
+    ds.route_mode = ROUTE_DEVICE_LIMITED if cfg.route_mode == "device_limited" else ROUTE_EXACT
+    ds.limit_devices = cfg.limit_devices
+    ds.renorm = int(bool(cfg.renorm))
+    ds.n_shared = cfg.n_shared
+    ds.shared_inter = cfg.shared_inter
+    ds.shared_gate = int(bool(cfg.shared_gate))
+    return ds
+
+
+class OccultMoE:
+    """One MoE layer resident on a CUDA device."""
+
+    def __init__(self, desc: occult_desc_t, weights: Dict[str, torch.Tensor],
+                 placement: torch.Tensor, device="cuda", materialize_sfd: bool = False):
+        self.desc = desc
+        dev = torch.device(device)
+        dt = desc.torch_dtype
+        self.device = dev
+        self.w = {k: v.to(dev, dt).contiguous() for k, v in weights.items()}
+        placement = torch.as_tensor(placement, dtype=torch.int32)
+        e2v = torch.empty(desc.n_experts, dtype=torch.int32)
+        for d in range(placement.shape[0]):
+            for e in placement[d].tolist():
+                e2v[e] = d
+        self.placement = placement.reshape(-1).to(dev).contiguous()
+        self.expert_to_vdev = e2v.to(dev)
+        T, d, Ne, k, Nd, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.n_vdev, desc.inter
+        n_sfd_max = T * min(k, Nd)
+        i32, f32 = torch.int32, torch.float32
+        e = lambda *s, dtype=i32: torch.empty(*s, dtype=dtype, device=dev)  # noqa: E731
+        self.ids, self.gates, self.vmask = e(T, k), e(T, k, dtype=f32), e(T)
+        self.brim0, self.seg_off, self.brim1 = e(Nd, T), e(Nd + 1), e(Ne, T)
+        self.exp_off, self.epd_src, self.epd_gate = e(Ne + 1), e(T * k), e(T * k, dtype=f32)
+        self.counts = e(4)
+        self.x_sfd, self.sfd_tok = e(n_sfd_max, d, dtype=dt), e(n_sfd_max)
+        self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=dt)
+        self.y = e(T, d, dtype=dt)
+        self.y_sfd = e(n_sfd_max, d, dtype=dt) if materialize_sfd else None
+        if desc.n_shared:
+            S = desc.n_shared * desc.shared_inter
+            self.h_s, self.y_s = e(T, S, dtype=dt), e(T, d, dtype=dt)
+            self.s_gate = e(T, dtype=f32)
+        else:
+            self.h_s = self.y_s = self.s_gate = None
+
+    @property
+    def launches_per_forward(self) -> int:
+        """Kernels this object launches per forward call."""
+        n = 6  # route, brim, dispatch, up, down, combine
+        if self.y_sfd is not None:
+            n += 1
+        if self.desc.n_shared:
+            n += 2 + (1 if self.desc.shared_gate else 0)
+        return n
+
+    def route_and_index(self, logits: torch.Tensor, stream=None) -> None:
+        ds = self.desc
+        occult_route(ds, logits, self.expert_to_vdev, self.ids, self.gates, self.vmask, stream)
+        occult_build_brim(ds, self.ids, self.gates, self.vmask, self.placement, self.brim0,
+                          self.seg_off, self.brim1, self.exp_off, self.epd_src, self.epd_gate,
+                          self.counts, stream)
+
+    def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
+        """y = MoE(x) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""
+        ds = self.desc
+        self.route_and_index(logits, stream)
+        occult_dispatch(ds, x, self.brim0, self.vmask, self.x_sfd, self.sfd_tok, stream)
+        occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
+                         self.placement, self.w["w1"], self.h_epd, stream)
+        occult_expert_down(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
+                           self.y_epd, stream)
+        if ds.n_shared:
+            occult_shared_ffn(ds, x, self.w["ws1"], self.w["ws2"], self.w.get("w_sg"), self.h_s,
+                              self.s_gate, self.y_s, stream)
+        occult_combine(ds, self.y_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, self.y,
+                       y_shared=self.y_s, y_sfd=self.y_sfd, stream=stream)
+        return self.y

@@ -1,0 +1,244 @@
+/*
+ * occult.h -- C ABI of the GB300 (sm_103a) Occult collaboration-aware MoE layer.
+ *
+ * Source of every operation: "Occult: Optimizing Collaborative Communication
+ * across Experts for Accelerated Parallel MoE Training and Inference"
+ * (arXiv 2505.13345), Appendix A.1 Algorithm 2 (the refactored pipeline) and
+ * Appendix A.2 Algorithms 3-9; Sec. 2.1 Eq. 1-4; Sec. 3.2 Algorithm 1.
+ *
+ * The Nd expert-parallel devices of the paper are virtual partitions of one GPU:
+ * virtual device d owns the experts of placement row d and a contiguous range
+ * of the SFD (dispatched) tensor.  The two all-to-all exchanges of Algorithm 2
+ * are therefore identities on the device-major SFD buffers (their byte counts,
+ * N_sfd * d * sizeof(element) per direction, are what crosses devices in the
+ * paper's setting).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory:    every pointer is a DEVICE pointer unless the comment says "host".
+ *            All buffers belong to the caller; the library never allocates,
+ *            frees or synchronises (except occult_device_error, which reads back
+ *            one word).  Row-major, densely packed unless stated.
+ * Execution: calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *            default stream) and capture into CUDA graphs.
+ * Sizing:    data-dependent sizes are bounded by their worst case so that no
+ *            host synchronisation is needed: N_sfd <= T * min(k, Nd) SFD rows,
+ *            N_epd = T * k EPD rows.  Actual counts are written to device memory.
+ * Types:     OCCULT_F32 layers hold x, weights, h, y in fp32; OCCULT_BF16 layers
+ *            hold them in bf16 and accumulate in fp32.  Logits and gates are fp32.
+ * Errors:    0 on success, a negative OCCULT_ERR_* code otherwise.  Arguments
+ *            are checked on the host before anything is launched; a failed check
+ *            launches nothing.  A bounded device-side wait that expires sets a
+ *            device error word (read with occult_device_error) and the kernel
+ *            returns early, leaving its outputs undefined.
+ */
+#ifndef OCCULT_H_
+#define OCCULT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OCCULT_OK                   0
+#define OCCULT_ERR_INVALID_ARG     -1  /* null pointer, bad size or option           */
+#define OCCULT_ERR_UNSUPPORTED     -2  /* valid layer this build does not run         */
+#define OCCULT_ERR_WORKSPACE       -3  /* workspace smaller than occult_workspace_size */
+#define OCCULT_ERR_CUDA            -4  /* a CUDA runtime/driver call failed          */
+#define OCCULT_ERR_DEVICE_TIMEOUT  -5  /* a bounded device wait expired               */
+
+#define OCCULT_F32   0
+#define OCCULT_BF16  1
+
+#define OCCULT_ROUTE_EXACT           0  /* Eq. 2 top-k                                 */
+#define OCCULT_ROUTE_DEVICE_LIMITED  1  /* keep `limit_devices` devices, then top-k   */
+
+/* Largest supported sizes. */
+#define OCCULT_MAX_EXPERTS  256
+#define OCCULT_MAX_VDEV     32
+#define OCCULT_MAX_TOPK     16
+
+typedef void* occult_stream_t;   /* cudaStream_t */
+
+/* One MoE layer.  Shapes: T tokens (N_ori), hidden d, Ne experts, top-k,
+ * SwiGLU intermediate `inter` (I), Nd virtual devices (Ne % Nd == 0),
+ * n_loc = Ne / Nd experts per device. */
+typedef struct occult_desc {
+  int32_t T;
+  int32_t d;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t inter;
+  int32_t n_vdev;
+  int32_t dtype;          /* OCCULT_F32 | OCCULT_BF16                              */
+  int32_t route_mode;     /* OCCULT_ROUTE_EXACT | OCCULT_ROUTE_DEVICE_LIMITED      */
+  int32_t limit_devices;  /* devices kept per token in device-limited mode         */
+  int32_t renorm;         /* 1: renormalise the k gates to sum to one              */
+  int32_t n_shared;       /* always-on shared experts (0 = none)                   */
+  int32_t shared_inter;   /* intermediate size of each shared expert               */
+  int32_t shared_gate;    /* 1: scale the shared output by sigmoid(w_sg . x)       */
+} occult_desc_t;
+
+/* Human-readable name of an OCCULT_* return code (static string). */
+const char* occult_strerror(int code);
+
+/* Checks a descriptor; returns 0 or OCCULT_ERR_INVALID_ARG / _UNSUPPORTED.
+ * bf16 layers need d % 64 == 0, inter % 64 == 0, shared_inter % 64 == 0. */
+int occult_check_desc(const occult_desc_t* desc);
+
+/* Host: bytes of device workspace `ws` that occult_profile_coact needs for
+ * n_tok profiled tokens (the other entry points need none). */
+int occult_workspace_size(const occult_desc_t* desc, int32_t n_tok, size_t* bytes);
+
+/* Host: reads and clears the device error word of the current device (one
+ * 4-byte device-to-host copy, synchronising).  *code receives 0 or a negative
+ * OCCULT_ERR_* value latched by a kernel since the last call. */
+int occult_device_error(int32_t* code);
+
+/*
+ * occult_place -- Algorithm 1 (Sec. 3.2), HOST function, run once offline.
+ *   C               host int64 [Ne, Ne] co-activation counts (Eq. 3).
+ *   placement       host int32 [Nd, Ne/Nd] out: device d's experts in the order
+ *                   Algorithm 1 adds them (this order numbers the local experts).
+ *   expert_to_vdev  host int32 [Ne] out: device of every expert.
+ * Comparisons are made on integer sums of C (P = C / max C only rescales), ties
+ * go to the lowest expert id, each device is filled to exactly Ne/Nd experts.
+ */
+int occult_place(const int64_t* C, int32_t n_experts, int32_t n_vdev,
+                 int32_t* placement, int32_t* expert_to_vdev);
+
+/*
+ * occult_route -- router of Sec. 2.1 Eq. 2 (Algorithm 2 step 1).
+ *   logits          fp32 [T, Ne] router logits g(x).
+ *   expert_to_vdev  int32 [Ne] device of each expert (from the placement).
+ *   ids      out    int32 [T, k] chosen experts, descending logit; equal logits
+ *                   go to the lower id.  The choice is made on the fp32 logits.
+ *   gates    out    fp32 [T, k] softmax probabilities of the chosen experts
+ *                   (renormalised over the k if desc->renorm).
+ *   vmask    out    uint32 [T] bit d set iff the token uses virtual device d.
+ * Device-limited mode keeps the desc->limit_devices devices with the largest
+ * summed softmax mass over all their experts (ties: lower device), takes the
+ * top-k among their experts and renormalises the gates.
+ */
+int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* expert_to_vdev,
+                 int32_t* ids, float* gates, uint32_t* vmask, occult_stream_t stream);
+
+/*
+ * occult_build_brim -- BRIM0 (Algorithm 3) and BRIM1 (Algorithm 5).
+ *   ids, gates, vmask  from occult_route.
+ *   placement   int32 [Nd, n_loc] device-major expert lists; slot s = d*n_loc + j
+ *               holds expert placement[s].
+ *   brim0    out int32 [Nd, T]: running counter over active (d, t) pairs taken
+ *               device by device, token by token; -1 where token t uses no
+ *               expert of device d.  Non-negative values are SFD row indices.
+ *   seg_off  out int32 [Nd + 1]: device d received SFD rows [seg_off[d], seg_off[d+1]).
+ *   brim1    out int32 [Ne, T]: row s = d*n_loc + j; entry [s, r] for
+ *               r < n_d = seg_off[d+1]-seg_off[d] is device d's Algorithm 5
+ *               counter (local EPD index) of (local expert j, received row r),
+ *               or -1 if that row does not activate that expert.  Entries with
+ *               r >= n_d are not written.
+ *   exp_off  out int32 [Ne + 1]: EPD rows of slot s are [exp_off[s], exp_off[s+1]);
+ *               device d's EPD tensor starts at exp_off[d*n_loc], so the global
+ *               EPD row of brim1[s, r] >= 0 is exp_off[d*n_loc] + brim1[s, r].
+ *   epd_src  out int32 [T*k]: SFD row feeding each EPD row (the condensed,
+ *               non-negative BRIM1 entries' column coordinates).
+ *   epd_gate out fp32 [T*k]: routing weight of each EPD row (Algorithm 7's w).
+ *   counts   out int32 [4]: {N_sfd, N_epd, max C_T, reserved}.
+ */
+int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float* gates,
+                      const uint32_t* vmask, const int32_t* placement,
+                      int32_t* brim0, int32_t* seg_off, int32_t* brim1, int32_t* exp_off,
+                      int32_t* epd_src, float* epd_gate, int32_t* counts,
+                      occult_stream_t stream);
+
+/*
+ * occult_dispatch -- Algorithm 4: x_sfd[brim0[d, t]] = x[t] for every
+ * non-negative entry (stage one of scattering, ORI -> SFD).  The result is the
+ * first all-to-all's send buffer, segment d going to virtual device d.
+ *   x        [T, d] layer dtype.
+ *   x_sfd    out [T*min(k,Nd), d] layer dtype; rows >= N_sfd untouched.
+ *   sfd_tok  out int32 [T*min(k,Nd)] ORI token of each SFD row (nullable).
+ */
+int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* brim0,
+                    const uint32_t* vmask, void* x_sfd, int32_t* sfd_tok,
+                    occult_stream_t stream);
+
+/*
+ * occult_expert_up -- scattering sparse matmul (Algorithm 6, stage two of
+ * scattering, SFD -> EPD) fused with the SwiGLU activation and the weight
+ * modulation of Algorithm 7:
+ *   h_epd[r, :] = epd_gate[r] * silu(A_r . W_g[e]^T) * (A_r . W_u[e]^T),
+ *   A_r = x_sfd[epd_src[r]], e = placement[s] for the slot s whose segment holds r.
+ *   w1     [Ne, 2*I, d]: rows [0, I) of expert e are W_g, rows [I, 2I) are W_u.
+ *   h_epd  out [T*k, I] layer dtype.
+ * bf16 layers run on the tcgen05 tensor cores (fp32 accumulate in TMEM).
+ */
+int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
+                     const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
+                     const void* w1, void* h_epd, occult_stream_t stream);
+
+/*
+ * occult_expert_down -- the second linear layer of Algorithm 8 on the EPD rows:
+ *   y_epd[r, :] = h_epd[r, :] . W_d[e]^T,   w2 [Ne, d, I],  y_epd out [T*k, d].
+ * The merge of Algorithm 8 (summing a token's local experts) is done without
+ * atomics by occult_combine.
+ */
+int occult_expert_down(const occult_desc_t* desc, const void* h_epd, const int32_t* exp_off,
+                       const int32_t* placement, const void* w2, void* y_epd,
+                       occult_stream_t stream);
+
+/* occult_expert_ffn -- occult_expert_up followed by occult_expert_down. */
+int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
+                      const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
+                      const void* w1, const void* w2, void* h_epd, void* y_epd,
+                      occult_stream_t stream);
+
+/*
+ * occult_shared_ffn -- always-on shared experts on the token's own device (no
+ * all-to-all):  y_s[t] = s_t * W_d^s (silu(W_g^s x_t) * (W_u^s x_t)), with
+ * s_t = sigmoid(w_sg . x_t) if desc->shared_gate else 1.  Several shared
+ * experts are stacked on the intermediate axis, S = n_shared * shared_inter:
+ *   ws1 [2*S, d] (gate rows then up rows), ws2 [d, S], w_sg [d] (nullable
+ *   without a gate), h_s out [T, S], s_gate out fp32 [T], y_s out [T, d].
+ */
+int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
+                      const void* ws2, const void* w_sg, void* h_s, float* s_gate, void* y_s,
+                      occult_stream_t stream);
+
+/*
+ * occult_combine -- the two-stage merge: stage one (EPD -> SFD, Algorithm 8's
+ * aggregation over a row's local experts) and stage two (SFD -> ORI,
+ * Algorithm 9, devices summed in order 0..Nd-1), in fp32:
+ *   y_sfd[v] = sum_j y_epd[exp_off[d*n_loc] + brim1[d*n_loc + j, v - seg_off[d]]]
+ *   y[t]     = sum_d y_sfd[brim0[d, t]]  (+ y_shared[t])
+ *   y_shared  [T, d] nullable: shared-expert output added to every token.
+ *   y_sfd     out [T*min(k,Nd), d] nullable: when given, stage one is written
+ *             out in the layer dtype (the second all-to-all's send buffer) and
+ *             stage two reads it back; when NULL both stages run fused per token.
+ *   y         out [T, d] layer dtype.
+ */
+int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,
+                   const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
+                   const void* y_shared, void* y_sfd, void* y, occult_stream_t stream);
+
+/*
+ * occult_profile_coact -- co-activation profiling (Sec. 2.1 Eq. 3-4, Sec. 2.2).
+ *   ids      int32 [n_tok, k] routing of the profiling batch.
+ *   vmask    uint32 [n_tok] (nullable) device masks under the current placement.
+ *   C        out int64 [Ne, Ne]: tokens activating both i and j (diagonal = load).
+ *   P        out fp32 [Ne, Ne] (nullable): C / max C.
+ *   ct_hist  out int64 [min(k,Nd) + 1] (nullable, needs vmask): tokens per C_T value.
+ *   ws       device workspace of occult_workspace_size bytes.
+ * Counts are exact integers built from per-expert token bitsets (no atomics).
+ */
+int occult_profile_coact(const occult_desc_t* desc, const int32_t* ids, int32_t n_tok,
+                         const uint32_t* vmask, int64_t* C, float* P, int64_t* ct_hist,
+                         void* ws, size_t ws_bytes, occult_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OCCULT_H_ */

@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+entry point include/occult.h declares; argument checks reject bad calls before
+anything is launched; the host placement (Algorithm 1) equals the oracle's.
+No GPU is needed: nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import coact, placement, routing
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def occ():
+    from combine_top_route_gb300 import build
+    build.build()
+    import combine_top_route_gb300 as occ
+    occ.lib()
+    return occ
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "occult.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(occult_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(occ):
+    names = declared_symbols()
+    assert len(names) >= 14
+    L = ctypes.CDLL(occ.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), f"{n} is declared in occult.h but not exported"
+    assert set(names) == set(occ.EXPORTED)
+
+
+def test_strerror(occ):
+    assert occ.strerror(0) == "success"
+    assert "timeout" in occ.strerror(occ.ERR_DEVICE_TIMEOUT) or "expired" in occ.strerror(occ.ERR_DEVICE_TIMEOUT)
+
+
+def _desc(occ, **kw):
+    ds = occ.desc_for(synth.CONFIGS["olmoe_fwd"])
+    return ds.replace(**kw)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_vdev=7), -1),             # Ne % Nd != 0
+    (dict(top_k=65), -1),             # k > Ne
+    (dict(T=-1), -1),
+    (dict(dtype=5), -1),
+    (dict(route_mode=3), -1),
+    (dict(n_vdev=64), -2),            # more than 32 virtual devices
+    (dict(top_k=17), -2),             # more than 16 experts per token
+    (dict(d=2050), -2),               # bf16 rows must be multiples of 64
+    (dict(inter=1000), -2),
+    (dict(route_mode=1, limit_devices=0), -1),
+    (dict(route_mode=1, limit_devices=1, top_k=9), -1),  # 1 device of 8 experts < k
+    (dict(n_shared=1, shared_inter=0), -1),
+])
+def test_bad_descriptors_are_rejected(occ, kw, code):
+    assert occ.check_desc(_desc(occ, **kw)) == code
+
+
+def test_calls_reject_bad_arguments_before_launching(occ):
+    L = occ.lib()
+    bad = _desc(occ, n_vdev=7)
+    null = ctypes.c_void_p(0)
+    assert L.occult_route(ctypes.byref(bad), null, null, null, null, null, null) == -1
+    good = _desc(occ)
+    # null pointers with a non-empty batch
+    assert L.occult_route(ctypes.byref(good), null, null, null, null, null, null) == -1
+    assert L.occult_build_brim(ctypes.byref(good), *([null] * 12)) == -1
+    assert L.occult_dispatch(ctypes.byref(good), *([null] * 6)) == -1
+    assert L.occult_expert_up(ctypes.byref(good), *([null] * 8)) == -1
+    assert L.occult_expert_down(ctypes.byref(good), *([null] * 6)) == -1
+    assert L.occult_combine(ctypes.byref(good), *([null] * 9)) == -1
+    assert L.occult_shared_ffn(ctypes.byref(good), *([null] * 8)) == -1   # no shared experts
+    # a workspace smaller than the query is refused
+    need = occ.workspace_size(good, 1024)
+    assert need > 0
+    assert L.occult_profile_coact(ctypes.byref(good), ctypes.c_void_p(16), 1024, null,
+                                  ctypes.c_void_p(16), null, null, ctypes.c_void_p(16),
+                                  ctypes.c_size_t(need - 1), null) == occ.ERR_WORKSPACE
+    assert L.occult_place(null, 8, 4, null, null) == -1
+
+
+def test_host_placement_matches_oracle(occ, golden):
+    g = golden("placement_worked_example.json")
+    L, e2v = occ.occult_place(np.array(g["C"]), g["n_vdev"])
+    assert L.tolist() == g["expect"]["placement"]
+    rng = np.random.default_rng(0)
+    for Ne, Nd in [(8, 2), (16, 4), (64, 8), (60, 4), (6, 6), (64, 16)]:
+        C = rng.integers(0, 40, size=(Ne, Ne))
+        C = C + C.T
+        L, e2v = occ.occult_place(C, Nd)
+        want = placement.place(C, Nd)
+        assert (L.numpy() == want).all()
+        assert (e2v.numpy() == placement.expert_to_vdev(want)).all()
+
+
+def test_host_placement_on_profiled_counts(occ):
+    cfg = synth.CONFIGS["qwen_prefill"]
+    ids, _ = routing.route_topk(synth.profiling_logits(cfg).numpy()[:4096], cfg.top_k)
+    C = coact.coactivation(ids, cfg.n_experts)
+    L, _ = occ.occult_place(C, cfg.n_vdev)
+    assert (L.numpy() == placement.place(C, cfg.n_vdev)).all()
