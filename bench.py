@@ -1,0 +1,414 @@
+"""Throughput of the Occult MoE layer (tokens/s) on GB300, with roofline and CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+One step = one forward of the whole layer path (route -> BRIM build -> dispatch
+-> grouped SwiGLU expert GEMMs -> two-stage combine) over one batch of the
+OLMoE-shaped bf16 workload (T=4096, d=2048, Ne=64, k=8, I=1024, Nd=8 virtual
+devices, Algorithm 1 placement from a 16384-token profiling batch).  Inputs are
+resident in HBM when the timed region starts; they are larger than L2 (the
+expert weights alone are 805 MB), so no L2 flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs its own replica of the layer on its own
+batch (the layer's batches are independent problems; no data-path collective),
+so the scaling is weak.  Prints ONE JSON line on rank 0.
+
+``--impl reference`` times the plain CPU oracle (the only reference of this
+method) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "Occult MoE-layer tokens/s on 1 GB300"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="olmoe_fwd")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="CPU time of the oracle sample in the baseline leg")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_desc(cfg) -> str:
+    s = (f"{cfg.name}: T={cfg.T} d={cfg.d} Ne={cfg.n_experts} k={cfg.top_k} I={cfg.inter} "
+         f"Nd={cfg.n_vdev} {cfg.dtype} {cfg.route_mode}")
+    if cfg.n_shared:
+        s += f" shared={cfg.n_shared}x{cfg.shared_inter}"
+    return s + ", Algorithm 1 placement"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], None, set()
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j.get("hbm_gbs", 6800.0), j.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    e = j.get(kernel)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "combine_top_route_gb300", "csrc", e["source"])
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return e["bytes_per_launch"] if h == e["source_sha256_16"] else None
+
+
+class OracleSample:
+    """The oracle as it stands, timed on the host cores on the first tokens of the batch."""
+
+    def __init__(self, cfg):
+        from layer_cases import alg1_placement
+        self.cfg = cfg
+        self.L = alg1_placement(cfg)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        self.logits = synth.measured_logits(cfg).numpy()
+        self.x = synth.hidden_states(cfg, device=dev).float().cpu().numpy()
+        self.w = {k: v.float().cpu().numpy()
+                  for k, v in synth.expert_weights(cfg, device=dev).items()}
+        try:
+            import threadpoolctl
+            self.cores = max(i["num_threads"] for i in threadpoolctl.threadpool_info()) or 1
+        except Exception:
+            self.cores = len(os.sched_getaffinity(0))
+
+    def run(self, n_tok: int) -> float:
+        """Seconds for routing, BRIMs (Alg. 3, 5) and the Eq. 1 output of n_tok tokens."""
+        from oracle import brim as obrim
+        from oracle import expert as oexpert
+        from oracle import routing as orouting
+        n_tok = max(1, min(n_tok, self.cfg.T))
+        t0 = time.perf_counter()
+        ids, gates = orouting.route_topk(self.logits[:n_tok], self.cfg.top_k,
+                                         renorm=self.cfg.renorm)
+        obrim.Brims(ids, gates, self.L)
+        oexpert.layer_output(self.x[:n_tok], ids, gates, self.w)
+        return time.perf_counter() - t0
+
+    def tokens_for(self, seconds: float) -> int:
+        """Sample size that takes about `seconds` (calibrated on a 16-token run)."""
+        self.run(16)
+        rate = 32 / self.run(32)
+        return max(1, min(self.cfg.T, int(rate * seconds)))
+
+    def describe(self, n_tok: int, dt: float) -> dict:
+        return {"value": n_tok / dt, "unit": UNIT, "cores": self.cores, "kind": "oracle",
+                "sample": f"first {n_tok} tokens of the {self.cfg.T}-token batch: routing, "
+                          f"BRIMs (Alg. 3, 5) and the Eq. 1 output in fp64, {dt:.1f} s"}
+
+
+def cpu_baseline(cfg, seconds: float = 15.0):
+    o = OracleSample(cfg)
+    n = o.tokens_for(seconds)
+    return o.describe(n, o.run(n))
+
+
+def run_reference(args, cfg, world, rank):
+    if rank != 0:
+        return
+    o = OracleSample(cfg)
+    # each step is a bounded sample so that warm-up + timed steps take ~2 minutes
+    n = o.tokens_for(120.0 / max(1, args.warmup + args.steps))
+    for _ in range(args.warmup):
+        o.run(n)
+    dt = sum(o.run(n) for _ in range(args.steps))
+    v = n * args.steps / dt
+    cb = o.describe(n, dt / args.steps)
+    cb["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.T / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_desc(cfg)},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, cfg, world, rank, local):
+    import combine_top_route_gb300 as occ
+    from combine_top_route_gb300 import build
+    from layer_cases import alg1_placement
+
+    build.build()
+    occ.lib()
+    dev = torch.device("cuda", local)
+    ds = occ.desc_for(cfg)
+    L = torch.as_tensor(alg1_placement(cfg))
+    logits = synth.measured_logits(cfg).to(dev)
+    x = synth.hidden_states(cfg, device=dev)
+    w = synth.expert_weights(cfg, device=dev)
+    moe = occ.OccultMoE(ds, w, L, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-call events over the timed region, on the launching stream
+    calls = ["route", "build_brim", "dispatch", "expert_up", "expert_down", "combine"]
+    T, k, d, I = cfg.T, cfg.top_k, cfg.d, cfg.inter
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        occ.occult_route(ds, logits, moe.expert_to_vdev, moe.ids, moe.gates, moe.vmask, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        occ.occult_build_brim(ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0,
+                              moe.seg_off, moe.brim1, moe.exp_off, moe.epd_src, moe.epd_gate,
+                              moe.counts, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        occ.occult_dispatch(ds, x, moe.brim0, moe.vmask, moe.x_sfd, moe.sfd_tok, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        occ.occult_expert_up(ds, moe.x_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
+                             moe.placement, moe.w["w1"], moe.h_epd, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        occ.occult_expert_down(ds, moe.h_epd, moe.exp_off, moe.placement, moe.w["w2"],
+                               moe.y_epd, stream)
+        if ev is not None:
+            ev[5].record(stream)
+        if ds.n_shared:
+            occ.occult_shared_ffn(ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s,
+                                  moe.s_gate, moe.y_s, stream)
+        occ.occult_combine(ds, moe.y_epd, moe.brim0, moe.seg_off, moe.brim1, moe.exp_off,
+                           moe.y, y_shared=moe.y_s, stream=stream)
+        if ev is not None:
+            ev[6].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-timed region: K steps, inputs resident in HBM ----------------
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_total = max_over_ranks(start.elapsed_time(stop), world)
+    ms_step = ms_total / args.steps
+
+    # ---- per-call durations (separate pass with events between calls) ------
+    n_prof = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_prof)]
+    torch.cuda.synchronize(dev)
+    for i in range(n_prof):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    per_call = {c: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof))
+                for j, c in enumerate(calls)}
+    n_sfd = int(moe.counts[0].item())
+
+    # ---- end to end through the public API with host buffers ----------------
+    x_h = x.cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    y_h = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(logits)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        y = moe.forward(lg_d, x_d, stream)
+        y_h.copy_(y, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    n_e2e = max(10, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+
+    hbm, tflops, peak_src = peaks()
+    flops_up = 4.0 * d * I * T * k
+    flops_down = 2.0 * d * I * T * k
+    b = 2  # bytes per bf16 element (x, x_sfd); y_epd and y are fp32
+    kernels = {
+        "route": {"ms": per_call["route"]},
+        "build_brim": {"ms": per_call["build_brim"]},
+        "dispatch": {"ms": per_call["dispatch"],
+                     "GB/s": (T * d * b + n_sfd * d * b) / per_call["dispatch"] / 1e6},
+        "expert_up": {"ms": per_call["expert_up"],
+                      "TFLOP/s": flops_up / per_call["expert_up"] / 1e9},
+        "expert_down": {"ms": per_call["expert_down"],
+                        "TFLOP/s": flops_down / per_call["expert_down"] / 1e9},
+        "combine": {"ms": per_call["combine"],
+                    "GB/s": (T * k * d * 4 + T * d * 4) / per_call["combine"] / 1e6},
+    }
+    dom = max(("expert_up", "expert_down"), key=lambda c: per_call[c])
+    achieved = kernels[dom]["TFLOP/s"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops,
+                "unit": "TFLOP/s", "frac": achieved / tflops, "traffic": recorded_traffic(dom),
+                "peak_source": f"{peak_src} bf16 dense burst"}
+    for c in ("dispatch", "combine"):
+        kernels[c]["hbm_frac"] = kernels[c]["GB/s"] / hbm
+
+    result = {
+        "metric": METRIC, "value": world * T / (ms_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(cfg),
+                   "l2": "inputs larger than L2 (805 MB of expert weights read every step)",
+                   "parallelism": f"{world} independent replica(s), Nd={cfg.n_vdev} virtual "
+                                  "expert-parallel devices each"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "E[C_T]": n_sfd / T,
+        "a2a_bytes_per_direction": n_sfd * d * b,
+        "clocks": clk.summary(),
+        "gpu_launches": moe.launches_per_forward * args.steps,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * 4,
+                "d2h_bytes_per_step": T * d * 4},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+    else:
+        run_ours(args, cfg, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -213,7 +213,7 @@ def occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream=None):
     _call("occult_expert_down", ctypes.byref(desc), _dev(h_epd, dt, T * k * I, "h_epd"),
           _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
           _dev(placement, torch.int32, Ne, "placement"), _dev(w2, dt, Ne * d * I, "w2"),
-          _dev(y_epd, dt, T * k * d, "y_epd"), _stream(stream))
+          _dev(y_epd, torch.float32, T * k * d, "y_epd"), _stream(stream))
 
 
 def occult_expert_ffn(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd, y_epd,
@@ -227,7 +227,7 @@ def occult_expert_ffn(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, w2
           _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
           _dev(placement, torch.int32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
           _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
-          _dev(y_epd, dt, T * k * d, "y_epd"), _stream(stream))
+          _dev(y_epd, torch.float32, T * k * d, "y_epd"), _stream(stream))
 
 
 def occult_shared_ffn(desc, x, ws1, ws2, w_sg, h_s, s_gate, y_s, stream=None):
@@ -239,20 +239,20 @@ def occult_shared_ffn(desc, x, ws1, ws2, w_sg, h_s, s_gate, y_s, stream=None):
           _dev(w_sg, dt, d, "w_sg", nullable=not desc.shared_gate),
           _dev(h_s, dt, T * S, "h_s"),
           _dev(s_gate, torch.float32, T, "s_gate", nullable=not desc.shared_gate),
-          _dev(y_s, dt, T * d, "y_s"), _stream(stream))
+          _dev(y_s, torch.float32, T * d, "y_s"), _stream(stream))
 
 
 def occult_combine(desc, y_epd, brim0, seg_off, brim1, exp_off, y, y_shared=None, y_sfd=None,
                    stream=None):
     T, d, Ne, k, Nd = desc.T, desc.d, desc.n_experts, desc.top_k, desc.n_vdev
-    dt = desc.torch_dtype
+    f32 = torch.float32
     i32 = torch.int32
-    _call("occult_combine", ctypes.byref(desc), _dev(y_epd, dt, T * k * d, "y_epd"),
+    _call("occult_combine", ctypes.byref(desc), _dev(y_epd, f32, T * k * d, "y_epd"),
           _dev(brim0, i32, Nd * T, "brim0"), _dev(seg_off, i32, Nd + 1, "seg_off"),
           _dev(brim1, i32, Ne * T, "brim1"), _dev(exp_off, i32, Ne + 1, "exp_off"),
-          _dev(y_shared, dt, T * d, "y_shared", nullable=True),
-          _dev(y_sfd, dt, T * min(k, Nd) * d, "y_sfd", nullable=True),
-          _dev(y, dt, T * d, "y"), _stream(stream))
+          _dev(y_shared, f32, T * d, "y_shared", nullable=True),
+          _dev(y_sfd, f32, T * min(k, Nd) * d, "y_sfd", nullable=True),
+          _dev(y, f32, T * d, "y"), _stream(stream))
 
 
 def occult_profile_coact(desc, ids, n_tok, C, ws, P=None, vmask=None, ct_hist=None,

@@ -302,7 +302,9 @@ int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* 
   if (rc) return rc;
   OCCULT_REQUIRE(desc->T == 0 || (y_epd && brim0 && seg_off && brim1 && exp_off && y));
   OCCULT_CTX(stream);
-  return launch_combine(ctx, *desc, y_epd, brim0, seg_off, brim1, exp_off, y_shared, y_sfd, y);
+  return launch_combine(ctx, *desc, static_cast<const float*>(y_epd), brim0, seg_off, brim1,
+                        exp_off, static_cast<const float*>(y_shared), static_cast<float*>(y_sfd),
+                        static_cast<float*>(y));
 }
 
 int occult_profile_coact(const occult_desc_t* desc, const int32_t* ids, int32_t n_tok,

@@ -5,7 +5,8 @@
 //  * combine  -- the two-stage merge: stage one (EPD -> SFD) sums a received
 //    row's local experts (the aggregation of Algorithm 8, done without atomics),
 //    stage two (SFD -> ORI, Algorithm 9) sums the token's devices in order
-//    0..Nd-1.  Accumulation is fp32 in a fixed order, so results are
+//    0..Nd-1.  Inputs, accumulation and outputs are fp32 (the paper keeps its
+//    merged SFD tensor in fp32 too), in a fixed order, so results are
 //    deterministic.  Fused by default (one warp per token walks BRIM0 then
 //    BRIM1); a materialised mode writes the SFD stage-one result out (the second
 //    all-to-all's send buffer) and reads it back.
@@ -53,14 +54,16 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ brim0,
 }
 
 // Fused stage one + stage two: y[t] = sum_d (sum_j y_epd[...]) (+ y_shared[t]).
-// With y_sfd given, also writes each device's stage-one sum there.
-template <typename T, bool WRITE_SFD>
+// With y_sfd given, also writes each device's stage-one sum there (and does not
+// write y: the stage-two kernel does, from y_sfd).  Everything is fp32.
+template <bool WRITE_SFD>
 __global__ void __launch_bounds__(kWarps * 32)
-combine_fused_kernel(const T* __restrict__ y_epd, const int32_t* __restrict__ brim0,
+combine_fused_kernel(const float* __restrict__ y_epd, const int32_t* __restrict__ brim0,
                      const int32_t* __restrict__ seg_off, const int32_t* __restrict__ brim1,
-                     const int32_t* __restrict__ exp_off, const T* __restrict__ y_shared, int ntok,
-                     int Nd, int n_loc, int D, T* __restrict__ y_sfd, T* __restrict__ y) {
-  constexpr int VN = Vec16<T>::N;
+                     const int32_t* __restrict__ exp_off, const float* __restrict__ y_shared,
+                     int ntok, int Nd, int n_loc, int D, float* __restrict__ y_sfd,
+                     float* __restrict__ y) {
+  constexpr int VN = 4;
   __shared__ int s_rows[kWarps][OCCULT_MAX_TOPK];
   __shared__ int s_devs[kWarps][OCCULT_MAX_TOPK];
   __shared__ int s_sfd[kWarps][OCCULT_MAX_VDEV];
@@ -106,51 +109,55 @@ combine_fused_kernel(const T* __restrict__ y_epd, const int32_t* __restrict__ br
     }
     __syncwarp();
     for (int v = lane; v < nvec; v += 32) {
-      float acc[VN], part[VN], f[VN];
+      float acc[VN], part[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f, part[i] = 0.f;
-      uint4 buf[OCCULT_MAX_TOPK];
+      float4 buf[OCCULT_MAX_TOPK];
 #pragma unroll
       for (int j = 0; j < OCCULT_MAX_TOPK; ++j)
-        if (j < n) buf[j] = ld_nc_v4(reinterpret_cast<const uint4*>(y_epd + static_cast<size_t>(rows[j]) * D) + v);
+        if (j < n) {
+          const uint4 u = ld_nc_v4(reinterpret_cast<const float4*>(y_epd + static_cast<size_t>(rows[j]) * D) + v);
+          buf[j] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                               __uint_as_float(u.w));
+        }
 #pragma unroll
       for (int j = 0; j < OCCULT_MAX_TOPK; ++j) {
         if (j < n) {
-          unpack16(buf[j], f, T());
-#pragma unroll
-          for (int i = 0; i < VN; ++i) part[i] += f[i];
+          part[0] += buf[j].x; part[1] += buf[j].y; part[2] += buf[j].z; part[3] += buf[j].w;
           // close the device's stage-one sum at its last expert
           if (j + 1 == n || devs[j + 1] != devs[j]) {
             if (WRITE_SFD) {
-              st_v4(reinterpret_cast<uint4*>(y_sfd + static_cast<size_t>(sfd[devs[j]]) * D) + v,
-                    pack16(part, T()));
+              st_v4(reinterpret_cast<float4*>(y_sfd + static_cast<size_t>(sfd[devs[j]]) * D) + v,
+                    pack16(part, float()));
             }
 #pragma unroll
             for (int i = 0; i < VN; ++i) acc[i] += part[i], part[i] = 0.f;
           }
         }
       }
-      if (y_shared) {
-        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_shared + static_cast<size_t>(t) * D) + v), f, T());
-#pragma unroll
-        for (int i = 0; i < VN; ++i) acc[i] += f[i];
+      if (!WRITE_SFD) {
+        if (y_shared) {
+          const uint4 u = ld_nc_v4(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * D) + v);
+          acc[0] += __uint_as_float(u.x); acc[1] += __uint_as_float(u.y);
+          acc[2] += __uint_as_float(u.z); acc[3] += __uint_as_float(u.w);
+        }
+        st_v4(reinterpret_cast<float4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, float()));
       }
-      st_v4(reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, T()));
     }
     __syncwarp();
   }
 }
 
 // Stage two from a materialised SFD tensor: y[t] = sum_d y_sfd[brim0[d, t]] (+ shared).
-template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
-combine_sfd_kernel(const T* __restrict__ y_sfd, const int32_t* __restrict__ brim0,
-                   const T* __restrict__ y_shared, int ntok, int Nd, int D, T* __restrict__ y) {
-  constexpr int VN = Vec16<T>::N;
+combine_sfd_kernel(const float* __restrict__ y_sfd, const int32_t* __restrict__ brim0,
+                   const float* __restrict__ y_shared, int ntok, int Nd, int D,
+                   float* __restrict__ y) {
+  constexpr int VN = 4;
   const int lane = threadIdx.x & 31;
   const int nvec = D / VN;
   for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < ntok; t += gridDim.x * kWarps) {
-    int my_row = lane < Nd ? brim0[static_cast<size_t>(lane) * ntok + t] : -1;
+    const int my_row = lane < Nd ? brim0[static_cast<size_t>(lane) * ntok + t] : -1;
     for (int v = lane; v < nvec; v += 32) {
       float acc[VN], f[VN];
 #pragma unroll
@@ -158,16 +165,16 @@ combine_sfd_kernel(const T* __restrict__ y_sfd, const int32_t* __restrict__ brim
       for (int d = 0; d < Nd; ++d) {
         const int row = __shfl_sync(0xffffffffu, my_row, d);
         if (row < 0) continue;
-        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_sfd + static_cast<size_t>(row) * D) + v), f, T());
+        unpack16(ld_nc_v4(reinterpret_cast<const float4*>(y_sfd + static_cast<size_t>(row) * D) + v), f, float());
 #pragma unroll
         for (int i = 0; i < VN; ++i) acc[i] += f[i];
       }
       if (y_shared) {
-        unpack16(ld_nc_v4(reinterpret_cast<const uint4*>(y_shared + static_cast<size_t>(t) * D) + v), f, T());
+        unpack16(ld_nc_v4(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * D) + v), f, float());
 #pragma unroll
         for (int i = 0; i < VN; ++i) acc[i] += f[i];
       }
-      st_v4(reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, T()));
+      st_v4(reinterpret_cast<float4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, float()));
     }
   }
 }
@@ -195,42 +202,22 @@ int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x
   return cuda_status(cudaGetLastError());
 }
 
-int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const void* y_epd,
+int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
-                   const int32_t* exp_off, const void* y_shared, void* y_sfd, void* y) {
+                   const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y) {
   if (ds.T == 0) return OCCULT_OK;
   const int g = grid_for(ctx, ds.T);
   const int n_loc = ds.n_experts / ds.n_vdev;
-  if (ds.dtype == OCCULT_BF16) {
-    using T = __nv_bfloat16;
-    if (y_sfd) {
-      combine_fused_kernel<T, true><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev,
-          n_loc, ds.d, static_cast<T*>(y_sfd), static_cast<T*>(y));
-      combine_sfd_kernel<T><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_sfd), brim0, static_cast<const T*>(y_shared), ds.T, ds.n_vdev,
-          ds.d, static_cast<T*>(y));
-    } else {
-      combine_fused_kernel<T, false><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off,
-          static_cast<const T*>(y_shared), ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
-          static_cast<T*>(y));
-    }
+  if (y_sfd) {
+    combine_fused_kernel<true><<<g, kWarps * 32, 0, ctx.stream>>>(
+        y_epd, brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev, n_loc, ds.d, y_sfd,
+        nullptr);
+    combine_sfd_kernel<<<g, kWarps * 32, 0, ctx.stream>>>(y_sfd, brim0, y_shared, ds.T,
+                                                          ds.n_vdev, ds.d, y);
   } else {
-    using T = float;
-    if (y_sfd) {
-      combine_fused_kernel<T, true><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev,
-          n_loc, ds.d, static_cast<T*>(y_sfd), static_cast<T*>(y));
-      combine_sfd_kernel<T><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_sfd), brim0, static_cast<const T*>(y_shared), ds.T, ds.n_vdev,
-          ds.d, static_cast<T*>(y));
-    } else {
-      combine_fused_kernel<T, false><<<g, kWarps * 32, 0, ctx.stream>>>(
-          static_cast<const T*>(y_epd), brim0, seg_off, brim1, exp_off,
-          static_cast<const T*>(y_shared), ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
-          static_cast<T*>(y));
-    }
+    combine_fused_kernel<false><<<g, kWarps * 32, 0, ctx.stream>>>(
+        y_epd, brim0, seg_off, brim1, exp_off, y_shared, ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
+        y);
   }
   return cuda_status(cudaGetLastError());
 }

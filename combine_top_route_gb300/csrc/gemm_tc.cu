@@ -16,8 +16,10 @@
 //               the row indices being the SFD rows of the condensed BRIM1.
 //   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators); lane 0
 //               issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate).
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread),
-//               SwiGLU + gate or plain, bf16 out.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread);
+//               SwiGLU + gate -> bf16 (the EPD intermediate feeding the second
+//               matmul), or plain -> fp32 (the merge input; every sum after the
+//               second linear layer stays in fp32).
 // Tile 128 x 256 x 64, 4 smem stages of 48 KB, both operands K-major with the
 // 128-byte swizzle.  Accumulators are double-buffered so the epilogue of one
 // tile overlaps the main loop of the next.  Every wait is bounded (2 s).
@@ -60,7 +62,7 @@ struct Params {
   const int32_t* seg_group;
   const int32_t* gather;
   const float* row_gate;
-  __nv_bfloat16* out;
+  void* out;       // bf16 with SwiGLU, fp32 otherwise
   int64_t ldo;
   int64_t b_group_rows;
   int n_seg;
@@ -258,7 +260,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                   g * silu_f(__uint_as_float(v0[2 * i + 1])) * __uint_as_float(v1[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(p.out + grow * p.ldo + col0 + c);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                  grow * p.ldo + col0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -271,14 +274,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
           if (valid && col0 + c < p.N_out) {
-            uint32_t pk[16];
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.out) + grow * p.ldo +
+                                                  col0 + c);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(p.out + grow * p.ldo + col0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
           }
         }
       }
@@ -359,7 +359,7 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.seg_group = g.seg_group;
   p.gather = g.gather;
   p.row_gate = g.row_gate;
-  p.out = static_cast<__nv_bfloat16*>(g.out);
+  p.out = g.out;
   p.ldo = g.ldo;
   p.b_group_rows = g.b_group_rows;
   p.n_seg = g.n_seg;

@@ -20,9 +20,9 @@ int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32
 int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
                     const int32_t* brim0, const uint32_t* vmask, void* x_sfd, int32_t* sfd_tok);
 
-int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const void* y_epd,
+int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
-                   const int32_t* exp_off, const void* y_shared, void* y_sfd, void* y);
+                   const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y);
 
 size_t profile_ws_bytes(const occult_desc_t& ds, int n_tok);
 int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids, int n_tok,
@@ -31,7 +31,8 @@ int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t*
 // Grouped GEMM over row segments: output rows [seg_off[s], seg_off[s+1]) use
 // weight group seg_group[s] (s when NULL).  Output row r reads A row gather[r]
 // (r when NULL).  With swiglu, the group's B holds 2*N_out rows (gate rows then
-// up rows) and out = row_gate * silu(A.Bg^T) * (A.Bu^T); otherwise out = A.B^T.
+// up rows) and out = row_gate * silu(A.Bg^T) * (A.Bu^T) in the layer dtype;
+// otherwise out = A.B^T in fp32.
 struct GroupedGemm {
   const void* A;
   int64_t a_rows;            // rows addressable in A

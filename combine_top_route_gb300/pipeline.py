@@ -66,12 +66,13 @@ class OccultMoE:
         self.exp_off, self.epd_src, self.epd_gate = e(Ne + 1), e(T * k), e(T * k, dtype=f32)
         self.counts = e(4)
         self.x_sfd, self.sfd_tok = e(n_sfd_max, d, dtype=dt), e(n_sfd_max)
-        self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=dt)
-        self.y = e(T, d, dtype=dt)
-        self.y_sfd = e(n_sfd_max, d, dtype=dt) if materialize_sfd else None
+        # after the second linear layer everything is fp32
+        self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=f32)
+        self.y = e(T, d, dtype=f32)
+        self.y_sfd = e(n_sfd_max, d, dtype=f32) if materialize_sfd else None
         if desc.n_shared:
             S = desc.n_shared * desc.shared_inter
-            self.h_s, self.y_s = e(T, S, dtype=dt), e(T, d, dtype=dt)
+            self.h_s, self.y_s = e(T, S, dtype=dt), e(T, d, dtype=f32)
             self.s_gate = e(T, dtype=f32)
         else:
             self.h_s = self.y_s = self.s_gate = None
@@ -94,7 +95,7 @@ class OccultMoE:
                           self.counts, stream)
 
     def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
-        """y = MoE(x) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""
+        """y = MoE(x) (fp32 [T, d]) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""
         ds = self.desc
         self.route_and_index(logits, stream)
         occult_dispatch(ds, x, self.brim0, self.vmask, self.x_sfd, self.sfd_tok, stream)

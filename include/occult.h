@@ -24,8 +24,13 @@
  * Sizing:    data-dependent sizes are bounded by their worst case so that no
  *            host synchronisation is needed: N_sfd <= T * min(k, Nd) SFD rows,
  *            N_epd = T * k EPD rows.  Actual counts are written to device memory.
- * Types:     OCCULT_F32 layers hold x, weights, h, y in fp32; OCCULT_BF16 layers
- *            hold them in bf16 and accumulate in fp32.  Logits and gates are fp32.
+ * Types:     x, the weights and the EPD intermediate h are in the layer dtype
+ *            (OCCULT_F32 or OCCULT_BF16).  Everything after the second linear
+ *            layer -- y_epd, y_sfd, the shared-expert output and the layer output
+ *            y -- is fp32, as is all accumulation: the paper keeps its merged SFD
+ *            tensor in fp32 as well, and rounding these to bf16 would alone use up
+ *            most of the 2e-2 * rms(y) error budget of a bf16 layer.  Logits and
+ *            gates are fp32.
  * Errors:    0 on success, a negative OCCULT_ERR_* code otherwise.  Arguments
  *            are checked on the host before anything is launched; a failed check
  *            launches nothing.  A bounded device-side wait that expires sets a
@@ -181,7 +186,7 @@ int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t
 
 /*
  * occult_expert_down -- the second linear layer of Algorithm 8 on the EPD rows:
- *   y_epd[r, :] = h_epd[r, :] . W_d[e]^T,   w2 [Ne, d, I],  y_epd out [T*k, d].
+ *   y_epd[r, :] = h_epd[r, :] . W_d[e]^T,   w2 [Ne, d, I],  y_epd out fp32 [T*k, d].
  * The merge of Algorithm 8 (summing a token's local experts) is done without
  * atomics by occult_combine.
  */
@@ -201,7 +206,7 @@ int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_
  * s_t = sigmoid(w_sg . x_t) if desc->shared_gate else 1.  Several shared
  * experts are stacked on the intermediate axis, S = n_shared * shared_inter:
  *   ws1 [2*S, d] (gate rows then up rows), ws2 [d, S], w_sg [d] (nullable
- *   without a gate), h_s out [T, S], s_gate out fp32 [T], y_s out [T, d].
+ *   without a gate), h_s out [T, S], s_gate out fp32 [T], y_s out fp32 [T, d].
  */
 int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
                       const void* ws2, const void* w_sg, void* h_s, float* s_gate, void* y_s,
@@ -213,11 +218,12 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
  * Algorithm 9, devices summed in order 0..Nd-1), in fp32:
  *   y_sfd[v] = sum_j y_epd[exp_off[d*n_loc] + brim1[d*n_loc + j, v - seg_off[d]]]
  *   y[t]     = sum_d y_sfd[brim0[d, t]]  (+ y_shared[t])
- *   y_shared  [T, d] nullable: shared-expert output added to every token.
- *   y_sfd     out [T*min(k,Nd), d] nullable: when given, stage one is written
- *             out in the layer dtype (the second all-to-all's send buffer) and
- *             stage two reads it back; when NULL both stages run fused per token.
- *   y         out [T, d] layer dtype.
+ *   y_epd     fp32 [T*k, d] from occult_expert_down.
+ *   y_shared  fp32 [T, d] nullable: shared-expert output added to every token.
+ *   y_sfd     out fp32 [T*min(k,Nd), d] nullable: when given, stage one is
+ *             written out (the second all-to-all's send buffer) and stage two
+ *             reads it back; when NULL both stages run fused per token.
+ *   y         out fp32 [T, d].
  */
 int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,
                    const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,

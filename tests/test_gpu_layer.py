@@ -202,7 +202,8 @@ def test_expert_up(occ, name):
     x_sfd[:b.n_sfd] = obrim.dispatch(x, b.brim0)
     h = torch.full((cfg.T * cfg.top_k, cfg.inter), float("nan"), dtype=cfg.torch_dtype,
                    device="cuda")
-    occ.occult_expert_up(ds, cuda(x_sfd, cfg.torch_dtype), i32(b.epd_src), cuda(g32),
+    occ.occult_expert_up(ds, cuda(x_sfd, cfg.torch_dtype), i32(b.epd_src),
+                         cuda(b.epd_gate.astype(np.float32)),
                          i32(b.exp_off), i32(case.placement.reshape(-1)),
                          case.weights["w1"], h)
     torch.cuda.synchronize()
@@ -228,7 +229,7 @@ def test_expert_down(occ, name):
     ds = occ.desc_for(cfg)
     g = torch.Generator().manual_seed(11)
     h = torch.randn(cfg.T * cfg.top_k, cfg.inter, generator=g).to(cfg.torch_dtype)
-    y = torch.full((cfg.T * cfg.top_k, cfg.d), float("nan"), dtype=cfg.torch_dtype, device="cuda")
+    y = torch.full((cfg.T * cfg.top_k, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
     occ.occult_expert_down(ds, h.cuda(), i32(b.exp_off), i32(case.placement.reshape(-1)),
                            case.weights["w2"], y)
     torch.cuda.synchronize()
@@ -249,7 +250,7 @@ def test_shared_ffn(occ, name):
     ds = occ.desc_for(cfg)
     S = cfg.n_shared * cfg.shared_inter
     h_s = torch.empty(cfg.T, S, dtype=cfg.torch_dtype, device="cuda")
-    y_s = torch.empty(cfg.T, cfg.d, dtype=cfg.torch_dtype, device="cuda")
+    y_s = torch.empty(cfg.T, cfg.d, dtype=torch.float32, device="cuda")
     s_gate = torch.empty(cfg.T, dtype=torch.float32, device="cuda")
     occ.occult_shared_ffn(ds, case.x, case.weights["ws1"], case.weights["ws2"],
                           case.weights.get("w_sg"), h_s, s_gate, y_s)
