@@ -114,3 +114,50 @@ def assert_close_layer(got: np.ndarray, ref: np.ndarray, dtype: str, what: str =
 
 def oracle_brims(case: Case, ids, gates) -> obrim.Brims:
     return obrim.Brims(ids, gates, case.placement)
+
+
+# Per-element error bounds of intermediates, derived from the arithmetic.  The
+# 2e-2 * rms bar is the layer-output bar; the EPD intermediate h is heavy-tailed
+# (a product silu(G) * U; max|h| reaches ~45 rms), so its bf16 rounding alone
+# exceeds 2e-2 * rms(h) although every element is as exact as bf16 allows.
+BF16_HALF_ULP = 2.0 ** -8     # |round_bf16(v) - v| <= 2^-8 |v|
+F32_EPS = 2.0 ** -24
+
+
+def h_bound(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, gate: float, h_ref: np.ndarray,
+            layer_dtype: str) -> np.ndarray:
+    """Bound on |h_gpu - h_ref| for one EPD row.
+
+    G = W_g a and U = W_u a accumulate K = len(a) products in fp32: their error is
+    at most 2 K 2^-24 sum|w||a| (twice the textbook gamma_K, for any internal
+    ordering of the tensor-core sum).  silu has slope <= 1.1, so the fp32 value of
+    h = g silu(G) U is off by at most g (1.1 |U| dG + |silu G| dU + 1.1 dG dU) plus
+    a few fp32 roundings; bf16 layers then round h once more (2^-8 relative).
+    """
+    a = a.astype(np.float64)
+    K = a.size
+    dG = 2 * K * F32_EPS * (np.abs(wg) @ np.abs(a))
+    dU = 2 * K * F32_EPS * (np.abs(wu) @ np.abs(a))
+    G = wg.astype(np.float64) @ a
+    U_abs = np.abs(wu.astype(np.float64) @ a)
+    s_abs = np.abs(G / (1.0 + np.exp(-G)))
+    d32 = abs(gate) * (1.1 * U_abs * dG + s_abs * dU + 1.1 * dG * dU) + 8 * F32_EPS * np.abs(h_ref)
+    if layer_dtype == "f32":
+        return d32
+    return BF16_HALF_ULP * (np.abs(h_ref) + d32) + d32
+
+
+def sfd_bound(w2: np.ndarray, h_abs_rows, layer_dtype: str) -> np.ndarray:
+    """Bound on |y_sfd_gpu - y_sfd_ref| for one SFD row summing the given EPD rows.
+
+    Each EPD row y = W_d h' reads h' rounded to the layer dtype (2^-8 relative for
+    bf16, with the small fp32 error of h' folded in as 1 %), accumulates I products
+    in fp32 (2 I 2^-24 sum|W||h'|), and the row sum adds one fp32 rounding per row.
+    """
+    B = 0.0
+    for e, h_abs in h_abs_rows:
+        B = B + np.abs(w2[e]).astype(np.float64) @ h_abs
+    I = w2.shape[-1]
+    rel = (1.01 * BF16_HALF_ULP if layer_dtype == "bf16" else 8 * F32_EPS)
+    rel += (2 * I + 2 * len(h_abs_rows) + 4) * F32_EPS
+    return rel * B
