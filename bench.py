@@ -270,7 +270,7 @@ def run_ours(args, cfg, world, rank, local):
             ev[1].record(stream)
         occ.occult_build_brim(ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0,
                               moe.seg_off, moe.brim1, moe.exp_off, moe.epd_src, moe.epd_gate,
-                              moe.counts, stream)
+                              moe.counts, moe.brim_ws, stream)
         if ev is not None:
             ev[2].record(stream)
         occ.occult_dispatch(ds, x, moe.brim0, moe.vmask, moe.x_sfd, moe.sfd_tok, stream)

@@ -31,6 +31,8 @@ ERR_UNSUPPORTED = -2
 ERR_WORKSPACE = -3
 ERR_CUDA = -4
 ERR_DEVICE_TIMEOUT = -5
+WS_BUILD_BRIM = 0
+WS_PROFILE_COACT = 1
 
 
 class occult_desc_t(ctypes.Structure):
@@ -65,12 +67,12 @@ _D = ctypes.POINTER(occult_desc_t)
 _SIGNATURES = {
     "occult_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "occult_check_desc": (ctypes.c_int, [_D]),
-    "occult_workspace_size": (ctypes.c_int, [_D, _I32, ctypes.POINTER(ctypes.c_size_t)]),
+    "occult_workspace_size": (ctypes.c_int, [_D, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     "occult_device_error": (ctypes.c_int, [ctypes.POINTER(_I32)]),
     "occult_place": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP]),
     "occult_route": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_build_brim": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
-                                         _VP, _VP]),
+                                         _VP, _VP, ctypes.c_size_t, _VP]),
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -146,9 +148,10 @@ def device_error() -> int:
     return code.value
 
 
-def workspace_size(desc: occult_desc_t, n_tok: int) -> int:
+def workspace_size(desc: occult_desc_t, op: int, n_tok: int = 0) -> int:
+    """Device workspace bytes of the entry point selected by `op` (WS_* constants)."""
     n = ctypes.c_size_t(0)
-    _call("occult_workspace_size", ctypes.byref(desc), n_tok, ctypes.byref(n))
+    _call("occult_workspace_size", ctypes.byref(desc), op, n_tok, ctypes.byref(n))
     return n.value
 
 
@@ -172,15 +175,17 @@ def occult_route(desc, logits, expert_to_vdev, ids, gates, vmask, stream=None):
 
 
 def occult_build_brim(desc, ids, gates, vmask, placement, brim0, seg_off, brim1, exp_off,
-                      epd_src, epd_gate, counts, stream=None):
+                      epd_src, epd_gate, counts, ws, stream=None):
     T, Ne, k, Nd = desc.T, desc.n_experts, desc.top_k, desc.n_vdev
     i32, f32 = torch.int32, torch.float32
+    need = workspace_size(desc, WS_BUILD_BRIM)
     _call("occult_build_brim", ctypes.byref(desc), _dev(ids, i32, T * k, "ids"),
           _dev(gates, f32, T * k, "gates"), _dev(vmask, i32, T, "vmask"),
           _dev(placement, i32, Ne, "placement"), _dev(brim0, i32, Nd * T, "brim0"),
           _dev(seg_off, i32, Nd + 1, "seg_off"), _dev(brim1, i32, Ne * T, "brim1"),
           _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(counts, i32, 4, "counts"),
+          _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
 
 
@@ -259,7 +264,7 @@ def occult_profile_coact(desc, ids, n_tok, C, ws, P=None, vmask=None, ct_hist=No
                          stream=None):
     Ne, k = desc.n_experts, desc.top_k
     max_ct = min(k, desc.n_vdev)
-    need = workspace_size(desc, n_tok)
+    need = workspace_size(desc, WS_PROFILE_COACT, n_tok)
     _call("occult_profile_coact", ctypes.byref(desc), _dev(ids, torch.int32, n_tok * k, "ids",
                                                             nullable=n_tok == 0),
           n_tok, _dev(vmask, torch.int32, n_tok, "vmask", nullable=True),

@@ -114,10 +114,15 @@ const char* occult_strerror(int code) {
 
 int occult_check_desc(const occult_desc_t* desc) { return check(desc); }
 
-int occult_workspace_size(const occult_desc_t* desc, int32_t n_tok, size_t* bytes) {
+int occult_workspace_size(const occult_desc_t* desc, int32_t op, int32_t n_tok, size_t* bytes) {
   int rc = check(desc);
   if (rc) return rc;
-  OCCULT_REQUIRE(bytes && n_tok >= 0);
+  OCCULT_REQUIRE(bytes);
+  if (op == OCCULT_WS_BUILD_BRIM) {
+    *bytes = brim_ws_bytes(*desc);
+    return OCCULT_OK;
+  }
+  OCCULT_REQUIRE(op == OCCULT_WS_PROFILE_COACT && n_tok >= 0);
   *bytes = profile_ws_bytes(*desc, n_tok);
   return OCCULT_OK;
 }
@@ -147,14 +152,17 @@ int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* 
 int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float* gates,
                       const uint32_t* vmask, const int32_t* placement, int32_t* brim0,
                       int32_t* seg_off, int32_t* brim1, int32_t* exp_off, int32_t* epd_src,
-                      float* epd_gate, int32_t* counts, occult_stream_t stream) {
+                      float* epd_gate, int32_t* counts, void* ws, size_t ws_bytes,
+                      occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   OCCULT_REQUIRE(placement && seg_off && exp_off && counts);
   OCCULT_REQUIRE(desc->T == 0 || (ids && gates && vmask && brim0 && brim1 && epd_src && epd_gate));
+  const size_t need = brim_ws_bytes(*desc);
+  if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
   return launch_build_brim(ctx, *desc, ids, gates, vmask, placement, brim0, seg_off, brim1,
-                           exp_off, epd_src, epd_gate, counts);
+                           exp_off, epd_src, epd_gate, counts, ws);
 }
 
 int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* brim0,

@@ -15,7 +15,8 @@ int launch_route(const LaunchCtx& ctx, const occult_desc_t& ds, const float* log
 int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids,
                       const float* gates, const uint32_t* vmask, const int32_t* placement,
                       int32_t* brim0, int32_t* seg_off, int32_t* brim1, int32_t* exp_off,
-                      int32_t* epd_src, float* epd_gate, int32_t* counts);
+                      int32_t* epd_src, float* epd_gate, int32_t* counts, void* ws);
+size_t brim_ws_bytes(const occult_desc_t& ds);
 
 int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
                     const int32_t* brim0, const uint32_t* vmask, void* x_sfd, int32_t* sfd_tok);

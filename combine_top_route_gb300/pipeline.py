@@ -16,9 +16,10 @@ from typing import Dict, Optional
 
 import torch
 
-from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, occult_build_brim,
-               occult_combine, occult_desc_t, occult_dispatch, occult_expert_down,
-               occult_expert_up, occult_route, occult_shared_ffn)
+from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, WS_BUILD_BRIM,
+               occult_build_brim, occult_combine, occult_desc_t, occult_dispatch,
+               occult_expert_down, occult_expert_up, occult_route, occult_shared_ffn,
+               workspace_size)
 
 
 def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
@@ -65,6 +66,7 @@ class OccultMoE:
         self.brim0, self.seg_off, self.brim1 = e(Nd, T), e(Nd + 1), e(Ne, T)
         self.exp_off, self.epd_src, self.epd_gate = e(Ne + 1), e(T * k), e(T * k, dtype=f32)
         self.counts = e(4)
+        self.brim_ws = e(max(1, workspace_size(desc, WS_BUILD_BRIM)), dtype=torch.uint8)
         self.x_sfd, self.sfd_tok = e(n_sfd_max, d, dtype=dt), e(n_sfd_max)
         # after the second linear layer everything is fp32
         self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=f32)
@@ -80,7 +82,7 @@ class OccultMoE:
     @property
     def launches_per_forward(self) -> int:
         """Kernels this object launches per forward call."""
-        n = 6  # route, brim, dispatch, up, down, combine
+        n = 8  # route, 3 BRIM kernels, dispatch, up, down, combine
         if self.y_sfd is not None:
             n += 1
         if self.desc.n_shared:
@@ -92,7 +94,7 @@ class OccultMoE:
         occult_route(ds, logits, self.expert_to_vdev, self.ids, self.gates, self.vmask, stream)
         occult_build_brim(ds, self.ids, self.gates, self.vmask, self.placement, self.brim0,
                           self.seg_off, self.brim1, self.exp_off, self.epd_src, self.epd_gate,
-                          self.counts, stream)
+                          self.counts, self.brim_ws, stream)
 
     def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
         """y = MoE(x) (fp32 [T, d]) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""

@@ -93,9 +93,15 @@ const char* occult_strerror(int code);
  * bf16 layers need d % 64 == 0, inter % 64 == 0, shared_inter % 64 == 0. */
 int occult_check_desc(const occult_desc_t* desc);
 
-/* Host: bytes of device workspace `ws` that occult_profile_coact needs for
- * n_tok profiled tokens (the other entry points need none). */
-int occult_workspace_size(const occult_desc_t* desc, int32_t n_tok, size_t* bytes);
+/* Workspace selectors of occult_workspace_size. */
+#define OCCULT_WS_BUILD_BRIM     0   /* occult_build_brim for desc->T tokens       */
+#define OCCULT_WS_PROFILE_COACT  1   /* occult_profile_coact for n_tok tokens      */
+
+/* Host: bytes of device workspace `ws` the entry point selected by `op` needs
+ * (n_tok: profiled tokens, used by OCCULT_WS_PROFILE_COACT only).  The other
+ * entry points need no workspace.  Workspace contents need no initialisation
+ * and are not meaningful after the call. */
+int occult_workspace_size(const occult_desc_t* desc, int32_t op, int32_t n_tok, size_t* bytes);
 
 /* Host: reads and clears the device error word of the current device (one
  * 4-byte device-to-host copy, synchronising).  *code receives 0 or a negative
@@ -151,12 +157,14 @@ int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* 
  *               non-negative BRIM1 entries' column coordinates).
  *   epd_gate out fp32 [T*k]: routing weight of each EPD row (Algorithm 7's w).
  *   counts   out int32 [4]: {N_sfd, N_epd, max C_T, reserved}.
+ *   ws       device workspace of occult_workspace_size(OCCULT_WS_BUILD_BRIM)
+ *            bytes (per-tile column counts); OCCULT_ERR_WORKSPACE if smaller.
  */
 int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float* gates,
                       const uint32_t* vmask, const int32_t* placement,
                       int32_t* brim0, int32_t* seg_off, int32_t* brim1, int32_t* exp_off,
                       int32_t* epd_src, float* epd_gate, int32_t* counts,
-                      occult_stream_t stream);
+                      void* ws, size_t ws_bytes, occult_stream_t stream);
 
 /*
  * occult_dispatch -- Algorithm 4: x_sfd[brim0[d, t]] = x[t] for every
@@ -236,7 +244,8 @@ int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* 
  *   C        out int64 [Ne, Ne]: tokens activating both i and j (diagonal = load).
  *   P        out fp32 [Ne, Ne] (nullable): C / max C.
  *   ct_hist  out int64 [min(k,Nd) + 1] (nullable, needs vmask): tokens per C_T value.
- *   ws       device workspace of occult_workspace_size bytes.
+ *   ws       device workspace of occult_workspace_size(OCCULT_WS_PROFILE_COACT)
+ *            bytes (per-expert token bitsets); OCCULT_ERR_WORKSPACE if smaller.
  * Counts are exact integers built from per-expert token bitsets (no atomics).
  */
 int occult_profile_coact(const occult_desc_t* desc, const int32_t* ids, int32_t n_tok,

@@ -75,14 +75,15 @@ def test_calls_reject_bad_arguments_before_launching(occ):
     good = _desc(occ)
     # null pointers with a non-empty batch
     assert L.occult_route(ctypes.byref(good), null, null, null, null, null, null) == -1
-    assert L.occult_build_brim(ctypes.byref(good), *([null] * 12)) == -1
+    assert L.occult_build_brim(ctypes.byref(good), *([null] * 12), ctypes.c_size_t(0), null) == -1
     assert L.occult_dispatch(ctypes.byref(good), *([null] * 6)) == -1
     assert L.occult_expert_up(ctypes.byref(good), *([null] * 8)) == -1
     assert L.occult_expert_down(ctypes.byref(good), *([null] * 6)) == -1
     assert L.occult_combine(ctypes.byref(good), *([null] * 9)) == -1
     assert L.occult_shared_ffn(ctypes.byref(good), *([null] * 8)) == -1   # no shared experts
     # a workspace smaller than the query is refused
-    need = occ.workspace_size(good, 1024)
+    assert occ.workspace_size(good, occ.WS_BUILD_BRIM) > 0
+    need = occ.workspace_size(good, occ.WS_PROFILE_COACT, 1024)
     assert need > 0
     assert L.occult_profile_coact(ctypes.byref(good), ctypes.c_void_p(16), 1024, null,
                                   ctypes.c_void_p(16), null, null, ctypes.c_void_p(16),

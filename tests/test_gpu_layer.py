@@ -115,10 +115,13 @@ def run_brim(occ, case, ids_o, gates_o):
                exp_off=torch.empty(Ne + 1, dtype=torch.int32, device="cuda"),
                epd_src=torch.full((T * k,), -7, dtype=torch.int32, device="cuda"),
                epd_gate=torch.empty(T * k, dtype=torch.float32, device="cuda"),
-               counts=torch.empty(4, dtype=torch.int32, device="cuda"))
+               counts=torch.empty(4, dtype=torch.int32, device="cuda"),
+               ws=torch.empty(max(1, occ.workspace_size(ds, occ.WS_BUILD_BRIM)),
+                              dtype=torch.uint8, device="cuda"))
     occ.occult_build_brim(ds, i32(ids_o), cuda(gates_o.astype(np.float32)),
                           cuda(vmask_bits(ids_o, case.e2v)), i32(case.placement), **out)
     torch.cuda.synchronize()
+    out.pop("ws")
     return {n: v.cpu().numpy() for n, v in out.items()}
 
 
@@ -345,7 +348,7 @@ def test_empty_batch(occ):
     eo = torch.full((cfg.n_experts + 1,), -1, dtype=torch.int32, device="cuda")
     L = i32(alg1_placement(cfg).reshape(-1))
     occ.occult_route(ds, z, L, e, z, e)
-    occ.occult_build_brim(ds, e, z, e, L, e, seg, e, eo, e, z, counts)
+    occ.occult_build_brim(ds, e, z, e, L, e, seg, e, eo, e, z, counts, None)
     torch.cuda.synchronize()
     assert counts[:3].tolist() == [0, 0, 0]
     assert (seg == 0).all() and (eo == 0).all()
@@ -364,7 +367,8 @@ def test_profile_coact_bit_exact(occ, name):
     C = torch.empty(cfg.n_experts, cfg.n_experts, dtype=torch.int64, device="cuda")
     P = torch.empty(cfg.n_experts, cfg.n_experts, dtype=torch.float32, device="cuda")
     hist = torch.empty(min(cfg.top_k, cfg.n_vdev) + 1, dtype=torch.int64, device="cuda")
-    ws = torch.empty(occ.workspace_size(ds, n), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(occ.workspace_size(ds, occ.WS_PROFILE_COACT, n), dtype=torch.uint8,
+                     device="cuda")
     occ.occult_profile_coact(ds, i32(ids), n, C, ws, P=P, vmask=cuda(vmask_bits(ids, e2v)),
                              ct_hist=hist)
     torch.cuda.synchronize()
