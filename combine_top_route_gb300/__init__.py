@@ -73,6 +73,8 @@ _SIGNATURES = {
     "occult_route": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_build_brim": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _VP, ctypes.c_size_t, _VP]),
+    "occult_build_brim_noalloc": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                 _VP, _VP, _VP, _VP]),
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -186,6 +188,24 @@ def occult_build_brim(desc, ids, gates, vmask, placement, brim0, seg_off, brim1,
           _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(counts, i32, 4, "counts"),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
+          _stream(stream))
+
+
+def occult_build_brim_noalloc(desc, ids, gates, vmask, placement, brim0, seg_off, brim1,
+                              exp_off, epd_src, epd_gate, counts, stream=None):
+    """occult_build_brim with the library's static scratch instead of a workspace.
+
+    For callers that cannot allocate device memory; see include/occult.h.
+    Calls that overlap on the GPU share the scratch and race.
+    """
+    T, Ne, k, Nd = desc.T, desc.n_experts, desc.top_k, desc.n_vdev
+    i32, f32 = torch.int32, torch.float32
+    _call("occult_build_brim_noalloc", ctypes.byref(desc), _dev(ids, i32, T * k, "ids"),
+          _dev(gates, f32, T * k, "gates"), _dev(vmask, i32, T, "vmask"),
+          _dev(placement, i32, Ne, "placement"), _dev(brim0, i32, Nd * T, "brim0"),
+          _dev(seg_off, i32, Nd + 1, "seg_off"), _dev(brim1, i32, Ne * T, "brim1"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(epd_gate, f32, T * k, "epd_gate"), _dev(counts, i32, 4, "counts"),
           _stream(stream))
 
 

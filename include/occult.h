@@ -167,6 +167,34 @@ int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float
                       void* ws, size_t ws_bytes, occult_stream_t stream);
 
 /*
+ * occult_build_brim_noalloc -- occult_build_brim without a caller workspace.
+ * The paper has no counterpart; this entry point exists for callers that cannot
+ * allocate device memory: code whose device memory belongs to an allocator it
+ * cannot reach from plain C, serving loops that forbid allocation after
+ * start-up (cudaMalloc and cudaFree may synchronise the device), and processes
+ * that must keep a fixed device footprint.  Same arguments and results as
+ * occult_build_brim minus ws / ws_bytes; it allocates nothing.
+ *   Scratch:  a static device array of OCCULT_STATIC_SCRATCH_BYTES inside the
+ *             library, loaded on every GPU that uses the library and kept until
+ *             the process exits.  A layer needing more scratch than that (more
+ *             than 65536 tokens at 256 experts) gets OCCULT_ERR_WORKSPACE and no
+ *             launch.  Nothing in the array has to start at zero, and each call
+ *             leaves its contents behind.
+ *   Sharing:  every call on a device uses the same array, so calls that overlap
+ *             on the GPU (unordered streams) race and give wrong results; order
+ *             them on one stream or with events.
+ *   Set-up:   the first call on a device looks up the array's device address
+ *             with that device current; make that first call before any stream
+ *             capture on the device.
+ */
+#define OCCULT_STATIC_SCRATCH_BYTES 295936
+int occult_build_brim_noalloc(const occult_desc_t* desc, const int32_t* ids, const float* gates,
+                              const uint32_t* vmask, const int32_t* placement,
+                              int32_t* brim0, int32_t* seg_off, int32_t* brim1,
+                              int32_t* exp_off, int32_t* epd_src, float* epd_gate,
+                              int32_t* counts, occult_stream_t stream);
+
+/*
  * occult_dispatch -- Algorithm 4: x_sfd[brim0[d, t]] = x[t] for every
  * non-negative entry (stage one of scattering, ORI -> SFD).  The result is the
  * first all-to-all's send buffer, segment d going to virtual device d.
