@@ -159,6 +159,24 @@ __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* m
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
          "r"(smem_u32(bar)) : "memory");
 }
+// 16-byte asynchronous global -> shared copies (L1 bypassed), tracked per thread
+// in commit groups.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+// Orders this thread's completed shared-memory writes before later accesses of
+// the async proxy (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(map) : "memory");
 }

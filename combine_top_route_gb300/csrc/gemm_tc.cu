@@ -9,11 +9,15 @@
 // coordinate.  Here those sub-vectors are the 128-row M tiles of every expert's
 // contiguous EPD segment, scheduled by a persistent kernel (one CTA per SM).
 //
-// CTA = 6 warps, warp-specialised:
-//   warp 0      TMA producer.  B (weights) as 2-D tiles; A either as 2-D tiles
-//               (contiguous rows) or gathered four rows per instruction with
-//               TMA tile::gather4 (each lane fetches 4 of the tile's 128 rows),
-//               the row indices being the SFD rows of the condensed BRIM1.
+// CTA = 6 warps (contiguous A) or 10 warps (gathered A), warp-specialised:
+//   warp 0      TMA producer: B (weights) as 2-D tiles, and A as 2-D tiles when
+//               its rows are contiguous.
+//   warps 6..9  (gathered A only) copy the tile's 128 A rows -- the SFD rows of
+//               the condensed BRIM1 -- with 16-byte cp.async straight into the
+//               128-byte-swizzled layout the tensor cores read; one warp
+//               instruction moves four whole 128-byte row segments.  (TMA
+//               tile::gather4 does the same in fewer instructions but measured
+//               2.3x slower on this GEMM.)
 //   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators); lane 0
 //               issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate).
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread);
@@ -41,7 +45,8 @@ constexpr int kStages = 4;
 constexpr int kATileBytes = BM * BK * 2;   // 16 KB
 constexpr int kBTileBytes = BN * BK * 2;   // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
-constexpr int kThreads = 192;
+constexpr int kGatherWarp0 = 6;   // first A-gather warp
+__host__ __device__ constexpr int threads_for(bool gather) { return gather ? 320 : 192; }
 constexpr int kMaxSeg = OCCULT_MAX_EXPERTS;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
@@ -58,6 +63,8 @@ struct SmemTail {
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SmemTail);
 
 struct Params {
+  const __nv_bfloat16* a_ptr;  // A rows (gathered A only)
+  int64_t a_ld;                // elements between A rows
   const int32_t* seg_off;
   const int32_t* seg_group;
   const int32_t* gather;
@@ -102,7 +109,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 template <bool GATHER, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(GATHER), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -115,7 +122,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // ---- prologue ------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&tail->full[s], 1);
+      // TMA arrival (+ one per A-gather warp)
+      mbar_init(&tail->full[s], GATHER ? 5 : 1);
       mbar_init(&tail->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -158,26 +166,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const TileInfo ti = decode_tile(tau, p, tail->mt_off);
       const int grp = p.seg_group ? p.seg_group[ti.seg] : ti.seg;
       const int b_row0 = static_cast<int>(grp * p.b_group_rows) + ti.nt * (SWIGLU ? BN / 2 : BN);
-      int r4[4] = {0, 0, 0, 0};
-      if (GATHER) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = min(lane * 4 + i, ti.rows - 1);
-          r4[i] = p.gather[ti.m0 + r];
-        }
-      }
       for (int kb = 0; kb < k_blocks; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
         uint8_t* sb = sa + kATileBytes;
-        if (lane == 0) mbar_arrive_expect_tx(&tail->full[stage], kStageBytes);
+        if (lane == 0)
+          mbar_arrive_expect_tx(&tail->full[stage], GATHER ? kBTileBytes : kStageBytes);
         __syncwarp();
-        if (GATHER) {
-          tma_gather4(sa + lane * 4 * (BK * 2), &tmA, kb * BK, r4[0], r4[1], r4[2], r4[3],
-                      &tail->full[stage]);
-        } else if (lane == 0) {
-          tma_load_2d(sa, &tmA, kb * BK, ti.m0, &tail->full[stage]);
-        }
+        if (!GATHER && lane == 0) tma_load_2d(sa, &tmA, kb * BK, ti.m0, &tail->full[stage]);
         if (lane == 0) {
           if (SWIGLU) {
             tma_load_2d(sb, &tmB, kb * BK, b_row0, &tail->full[stage]);
@@ -227,7 +223,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kGatherWarp0) {
     // ---- epilogue ----------------------------------------------------------
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int row = quarter * 32 + lane;
@@ -292,6 +288,65 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
+  if (GATHER && warp >= kGatherWarp0) {
+    // ---- A gather (cp.async) -------------------------------------------------
+    // Lane l copies 16-byte chunk (l % 8) of rows (l / 8) + 4 i, i < 8, of this
+    // warp's 32 rows; chunk c of row r lands at r*128 + ((c ^ (r % 8)) * 16), the
+    // 128-byte swizzle.  A stage is signalled full kInFlight stages late, once
+    // this thread's copies for it have landed and been fenced for the async proxy.
+    constexpr int kInFlight = kStages - 1;
+    const int gw = warp - kGatherWarp0;
+    const int chunk = lane & 7;
+    const int rsub = lane >> 3;
+    uint32_t dst_off[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = gw * 32 + rsub + 4 * i;
+      dst_off[i] = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
+    }
+    int stage = 0, arr_stage = 0, inflight = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
+      const TileInfo ti = decode_tile(tau, p, tail->mt_off);
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = min(gw * 32 + rsub + 4 * i, ti.rows - 1);
+        src[i] = p.a_ptr + static_cast<int64_t>(p.gather[ti.m0 + r]) * p.a_ld + chunk * 8;
+      }
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        uint8_t* sa = smem + stage * kStageBytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cp_async_16(sa + dst_off[i], src[i] + kb * BK);
+        cp_async_commit();
+        if (++inflight > kInFlight) {
+          cp_async_wait<kInFlight>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tail->full[arr_stage]);
+          if (++arr_stage == kStages) arr_stage = 0;
+          --inflight;
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // every copy lands before the CTA may exit, also after an abort
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (ok) {
+      for (; inflight > 0; --inflight) {
+        if (lane == 0) mbar_arrive(&tail->full[arr_stage]);
+        if (++arr_stage == kStages) arr_stage = 0;
+      }
+    } else {
+      if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -338,7 +393,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return OCCULT_ERR_CUDA;
-  kern<<<ctx.num_sms, kThreads, kSmemBytes, ctx.stream>>>(ma, mb, p);
+  kern<<<ctx.num_sms, threads_for(GATHER), kSmemBytes, ctx.stream>>>(ma, mb, p);
   return cuda_status(cudaGetLastError());
 }
 
@@ -349,8 +404,8 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.max_rows == 0 || g.n_seg == 0) return OCCULT_OK;
   CUtensorMap ma, mb;
   int rc;
-  if (g.gather) rc = make_map(&ma, g.A, g.a_rows, g.K, BK, 1);
-  else rc = make_map(&ma, g.A, g.a_rows, g.K, BK, BM);
+  // (gathered A is copied by cp.async; its map is made but unused)
+  rc = make_map(&ma, g.A, g.a_rows, g.K, BK, BM);
   if (rc) return rc;
   rc = make_map(&mb, g.B, g.b_group_rows * g.n_groups, g.K, BK, g.swiglu ? BN / 2 : BN);
   if (rc) return rc;
@@ -358,6 +413,8 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.seg_off = g.seg_off;
   p.seg_group = g.seg_group;
   p.gather = g.gather;
+  p.a_ptr = static_cast<const __nv_bfloat16*>(g.A);
+  p.a_ld = g.K;
   p.row_gate = g.row_gate;
   p.out = g.out;
   p.ldo = g.ldo;
