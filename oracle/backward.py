@@ -28,8 +28,9 @@ def moe_backward(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, w1: np.ndarr
                  experts: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """dx [T, d], dw1 [Ne, 2I, d], dw2 [Ne, d, I], dgates [T, k] of sum_t <dy_t, y_t>.
 
-    ``experts`` limits the weight gradients to those experts (dx and dgates still
-    cover every token); the other experts' weight gradients are left at zero.
+    ``experts`` restricts the computation to those experts: the other experts'
+    weight gradients stay zero, and dx / dgates hold only the listed experts'
+    contributions (the full gradients are the sums over disjoint expert sets).
     """
     x = np.asarray(x, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
@@ -42,8 +43,8 @@ def moe_backward(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, w1: np.ndarr
     dw1 = np.zeros((Ne, two_i, d))
     dw2 = np.zeros((Ne, d, I))
     dgates = np.zeros((T, k))
-    wanted = set(range(Ne)) if experts is None else set(int(e) for e in experts)
-    for e in np.unique(ids):
+    todo = np.unique(ids) if experts is None else [int(e) for e in experts]
+    for e in todo:
         rows, slots = np.nonzero(ids == e)
         wg = np.asarray(w1[e, :I], dtype=np.float64)
         wu = np.asarray(w1[e, I:], dtype=np.float64)
@@ -62,8 +63,7 @@ def moe_backward(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, w1: np.ndarr
         dG = dh * U * sig * (1.0 + G * (1.0 - sig))
         dU = dh * s
         np.add.at(dx, rows, dG @ wg + dU @ wu)
-        if int(e) in wanted:
-            dw2[e] = dyr.T @ (g * h)
-            dw1[e, :I] = dG.T @ a
-            dw1[e, I:] = dU.T @ a
+        dw2[e] = dyr.T @ (g * h)
+        dw1[e, :I] = dG.T @ a
+        dw1[e, I:] = dU.T @ a
     return {"dx": dx, "dw1": dw1, "dw2": dw2, "dgates": dgates}
