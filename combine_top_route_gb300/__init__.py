@@ -33,6 +33,7 @@ ERR_CUDA = -4
 ERR_DEVICE_TIMEOUT = -5
 WS_BUILD_BRIM = 0
 WS_PROFILE_COACT = 1
+WS_EXPERT_BWD = 2
 
 
 class occult_desc_t(ctypes.Structure):
@@ -76,12 +77,14 @@ _SIGNATURES = {
     "occult_build_brim_noalloc": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                  _VP, _VP, _VP, _VP]),
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP]),
     "occult_shared_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_combine": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 16 + [ctypes.c_size_t, _VP]),
+    "occult_gate_grad": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_size_t, _VP]),
 }
@@ -219,7 +222,8 @@ def occult_dispatch(desc, x, brim0, vmask, x_sfd, sfd_tok=None, stream=None):
           _dev(sfd_tok, torch.int32, n_sfd_max, "sfd_tok", nullable=True), _stream(stream))
 
 
-def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, stream=None):
+def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd=None,
+                     stream=None):
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt = desc.torch_dtype
     _call("occult_expert_up", ctypes.byref(desc),
@@ -229,7 +233,36 @@ def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_e
           _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
           _dev(placement, torch.int32, Ne, "placement"),
           _dev(w1, dt, Ne * 2 * I * d, "w1"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(gu_epd, dt, T * k * 2 * I, "gu_epd", nullable=True), _stream(stream))
+
+
+def occult_expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
+                      gu_epd, dgu_epd, dx_epd, dw1, dw2, dg_epd, ws, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
+    n_sfd_max = T * min(k, desc.n_vdev)
+    need = workspace_size(desc, WS_EXPERT_BWD)
+    _call("occult_expert_bwd", ctypes.byref(desc), _dev(x_sfd, dt, n_sfd_max * d, "x_sfd"),
+          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
+          _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
+          _dev(dx_epd, f32, T * k * d, "dx_epd"), _dev(dw1, f32, Ne * 2 * I * d, "dw1"),
+          _dev(dw2, f32, Ne * d * I, "dw2"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
+
+
+def occult_gate_grad(desc, ids, placement, brim0, seg_off, brim1, exp_off, dg_epd, dgates,
+                     stream=None):
+    T, Ne, k, Nd = desc.T, desc.n_experts, desc.top_k, desc.n_vdev
+    i32, f32 = torch.int32, torch.float32
+    _call("occult_gate_grad", ctypes.byref(desc), _dev(ids, i32, T * k, "ids"),
+          _dev(placement, i32, Ne, "placement"), _dev(brim0, i32, Nd * T, "brim0"),
+          _dev(seg_off, i32, Nd + 1, "seg_off"), _dev(brim1, i32, Ne * T, "brim1"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(dgates, f32, T * k, "dgates"), _stream(stream))
 
 
 def occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream=None):

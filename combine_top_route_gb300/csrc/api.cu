@@ -122,6 +122,10 @@ int occult_workspace_size(const occult_desc_t* desc, int32_t op, int32_t n_tok, 
     *bytes = brim_ws_bytes(*desc);
     return OCCULT_OK;
   }
+  if (op == OCCULT_WS_EXPERT_BWD) {
+    *bytes = expert_bwd_ws_bytes(*desc);
+    return OCCULT_OK;
+  }
   OCCULT_REQUIRE(op == OCCULT_WS_PROFILE_COACT && n_tok >= 0);
   *bytes = profile_ws_bytes(*desc, n_tok);
   return OCCULT_OK;
@@ -176,12 +180,18 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
 
 static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* x_sfd,
                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
-                     const int32_t* placement, const void* w1, void* h_epd) {
+                     const int32_t* placement, const void* w1, void* h_epd, void* gu_epd) {
   GroupedGemm g;
+  g.a_mode = OP_GATHER_K;
+  g.b_mode = OP_TMA_K;
+  g.epi = EPI_SWIGLU;
   g.A = x_sfd;
   g.a_rows = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+  g.a_cols = desc->d;
   g.gather = epd_src;
   g.B = w1;
+  g.b_rows = 2ll * desc->inter * desc->n_experts;
+  g.b_cols = desc->d;
   g.b_group_rows = 2ll * desc->inter;
   g.n_groups = desc->n_experts;
   g.seg_off = exp_off;
@@ -193,7 +203,7 @@ static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void
   g.ldo = desc->inter;
   g.N_out = desc->inter;
   g.K = desc->d;
-  g.swiglu = true;
+  g.gu_out = gu_epd;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g)
                                     : launch_grouped_gemm_f32(ctx, g);
 }
@@ -202,10 +212,16 @@ static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const vo
                        const int32_t* exp_off, const int32_t* placement, const void* w2,
                        void* y_epd) {
   GroupedGemm g;
+  g.a_mode = OP_TMA_K;
+  g.b_mode = OP_TMA_K;
+  g.epi = EPI_F32;
   g.A = h_epd;
   g.a_rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  g.a_cols = desc->inter;
   g.gather = nullptr;
   g.B = w2;
+  g.b_rows = static_cast<int64_t>(desc->d) * desc->n_experts;
+  g.b_cols = desc->inter;
   g.b_group_rows = desc->d;
   g.n_groups = desc->n_experts;
   g.seg_off = exp_off;
@@ -217,21 +233,21 @@ static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const vo
   g.ldo = desc->d;
   g.N_out = desc->d;
   g.K = desc->inter;
-  g.swiglu = false;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g)
                                     : launch_grouped_gemm_f32(ctx, g);
 }
 
 int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
                      const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
-                     const void* w1, void* h_epd, occult_stream_t stream) {
+                     const void* w1, void* h_epd, void* gu_epd, occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   OCCULT_REQUIRE(exp_off && placement && w1);
   OCCULT_REQUIRE(desc->T == 0 || (x_sfd && epd_src && epd_gate && h_epd));
   OCCULT_CTX(stream);
   if (desc->T == 0) return OCCULT_OK;
-  return expert_up(ctx, desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd);
+  if (gu_epd && desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  return expert_up(ctx, desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd);
 }
 
 int occult_expert_down(const occult_desc_t* desc, const void* h_epd, const int32_t* exp_off,
@@ -250,7 +266,8 @@ int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_
                       const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
                       const void* w1, const void* w2, void* h_epd, void* y_epd,
                       occult_stream_t stream) {
-  int rc = occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, stream);
+  int rc = occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd,
+                            nullptr, stream);
   if (rc) return rc;
   return occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream);
 }
@@ -272,10 +289,16 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
   }
   const int S = desc->n_shared * desc->shared_inter;
   GroupedGemm g;
+  g.a_mode = OP_TMA_K;
+  g.b_mode = OP_TMA_K;
+  g.epi = EPI_SWIGLU;
   g.A = x;
   g.a_rows = desc->T;
+  g.a_cols = desc->d;
   g.gather = nullptr;
   g.B = ws1;
+  g.b_rows = 2ll * S;
+  g.b_cols = desc->d;
   g.b_group_rows = 2ll * S;
   g.n_groups = 1;
   g.seg_off = nullptr;
@@ -287,20 +310,127 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
   g.ldo = S;
   g.N_out = S;
   g.K = desc->d;
-  g.swiglu = true;
   rc = desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g) : launch_grouped_gemm_f32(ctx, g);
   if (rc) return rc;
+  g.epi = EPI_F32;
   g.A = h_s;
   g.a_rows = desc->T;
+  g.a_cols = S;
   g.B = ws2;
+  g.b_rows = desc->d;
+  g.b_cols = S;
   g.b_group_rows = desc->d;
   g.row_gate = nullptr;
   g.out = y_s;
   g.ldo = desc->d;
   g.N_out = desc->d;
   g.K = S;
-  g.swiglu = false;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g) : launch_grouped_gemm_f32(ctx, g);
+}
+
+int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                      const int32_t* placement, const void* w1, const void* w2,
+                      const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
+                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
+                      occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(exp_off && placement && w1 && w2 && dw1 && dw2);
+  OCCULT_REQUIRE(desc->T == 0 || (x_sfd && dy_sfd && epd_src && epd_gate && h_epd && gu_epd &&
+                                  dgu_epd && dx_epd && dg_epd));
+  const size_t need = expert_bwd_ws_bytes(*desc);
+  if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
+  OCCULT_CTX(stream);
+  if (desc->T == 0) {
+    // no rows: every weight gradient is zero
+    const size_t n1 = static_cast<size_t>(desc->n_experts) * 2 * desc->inter * desc->d;
+    const size_t n2 = static_cast<size_t>(desc->n_experts) * desc->d * desc->inter;
+    if (cudaMemsetAsync(dw1, 0, n1 * sizeof(float), ctx.stream) != cudaSuccess ||
+        cudaMemsetAsync(dw2, 0, n2 * sizeof(float), ctx.stream) != cudaSuccess)
+      return OCCULT_ERR_CUDA;
+    return OCCULT_OK;
+  }
+  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
+  float* dg_part = static_cast<float*>(ws);
+  {
+    // dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg
+    GroupedGemm g;
+    g.a_mode = OP_GATHER_K;
+    g.b_mode = OP_TMA_MN;
+    g.epi = EPI_SWIGLU_BWD;
+    g.A = dy_sfd; g.a_rows = n_sfd_max; g.a_cols = d;
+    g.gather = epd_src;
+    g.B = w2; g.b_rows = static_cast<int64_t>(Ne) * d; g.b_cols = I;
+    g.b_group_rows = d;
+    g.n_groups = Ne;
+    g.seg_off = exp_off; g.seg_group = placement; g.n_seg = Ne; g.max_rows = rows;
+    g.K = d; g.N_out = I;
+    g.row_gate = epd_gate;
+    g.out = dgu_epd; g.ldo = 2ll * I;
+    g.gu_in = gu_epd; g.dg_part = dg_part;
+    rc = launch_grouped_gemm_bf16(ctx, g);
+    if (rc) return rc;
+    rc = launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), (I + 255) / 256, dg_epd);
+    if (rc) return rc;
+    // dx_epd = [dG|dU] . [W_g; W_u] (W1 read MN-major), fp32
+    GroupedGemm h;
+    h.a_mode = OP_TMA_K;
+    h.b_mode = OP_TMA_MN;
+    h.epi = EPI_F32;
+    h.A = dgu_epd; h.a_rows = rows; h.a_cols = 2ll * I;
+    h.B = w1; h.b_rows = 2ll * I * Ne; h.b_cols = d;
+    h.b_group_rows = 2ll * I;
+    h.n_groups = Ne;
+    h.seg_off = exp_off; h.seg_group = placement; h.n_seg = Ne; h.max_rows = rows;
+    h.K = 2 * I; h.N_out = d;
+    h.out = dx_epd; h.ldo = d;
+    rc = launch_grouped_gemm_bf16(ctx, h);
+    if (rc) return rc;
+  }
+  // dW_d[e] = sum over e's rows of dy_sfd[src] (x) h' : M = d, N = I
+  GroupedGemm w;
+  w.wgrad = true;
+  w.a_mode = OP_GATHER_MN;
+  w.b_mode = OP_TMA_MN;
+  w.epi = EPI_F32;
+  w.A = dy_sfd; w.a_rows = n_sfd_max; w.a_cols = d;
+  w.gather = epd_src;
+  w.B = h_epd; w.b_rows = rows; w.b_cols = I;
+  w.seg_off = exp_off; w.seg_group = placement; w.n_seg = Ne;
+  w.M_total = d; w.N_out = I;
+  w.out = dw2; w.ldo = I; w.out_group_stride = static_cast<int64_t>(d) * I;
+  rc = launch_grouped_gemm_bf16(ctx, w);
+  if (rc) return rc;
+  // [dW_g; dW_u][e] = sum over e's rows of [dG|dU] (x) x_sfd[src] : M = 2I, N = d
+  GroupedGemm v;
+  v.wgrad = true;
+  v.a_mode = OP_TMA_MN;
+  v.b_mode = OP_GATHER_MN;
+  v.epi = EPI_F32;
+  v.A = dgu_epd; v.a_rows = rows; v.a_cols = 2ll * I;
+  v.B = x_sfd; v.b_rows = n_sfd_max; v.b_cols = d;
+  v.gather = epd_src;
+  v.seg_off = exp_off; v.seg_group = placement; v.n_seg = Ne;
+  v.M_total = 2 * I; v.N_out = d;
+  v.out = dw1; v.ldo = d; v.out_group_stride = 2ll * I * d;
+  return launch_grouped_gemm_bf16(ctx, v);
+}
+
+int occult_gate_grad(const occult_desc_t* desc, const int32_t* ids, const int32_t* placement,
+                     const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
+                     const int32_t* exp_off, const float* dg_epd, float* dgates,
+                     occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(desc->T == 0 || (ids && placement && brim0 && seg_off && brim1 && exp_off &&
+                                  dg_epd && dgates));
+  OCCULT_CTX(stream);
+  return launch_gate_grad(ctx, *desc, ids, placement, brim0, seg_off, brim1, exp_off, dg_epd,
+                          dgates);
 }
 
 int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,

@@ -146,7 +146,7 @@ int launch_grouped_gemm_f32(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.K = g.K;
   const int64_t m_tiles = (g.max_rows + TM - 1) / TM + g.n_seg;
   dim3 grid(static_cast<unsigned>(m_tiles), (g.N_out + TN - 1) / TN);
-  if (g.swiglu) grouped_gemm_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(p);
+  if (g.epi == EPI_SWIGLU) grouped_gemm_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(p);
   else grouped_gemm_f32_kernel<false><<<grid, 256, 0, ctx.stream>>>(p);
   return cuda_status(cudaGetLastError());
 }

@@ -1,32 +1,31 @@
-// Grouped expert GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+// Grouped expert GEMMs on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
-// This is the only dense contraction of the Occult layer: the scattering
-// sparse matmul (Appendix A.2 Algorithm 6, SFD -> EPD, fused with the SwiGLU
-// activation and Algorithm 7's weight modulation) and the second linear layer
-// of Algorithm 8 (EPD rows times W_d).  Algorithm 6 tiles each expert's BRIM1
-// row; the paper condenses the non-empty parts of BRIM1 into fixed-length
-// sub-vectors, one thread-block each, the expert given by the sub-vector's
-// coordinate.  Here those sub-vectors are the 128-row M tiles of every expert's
-// contiguous EPD segment, scheduled by a persistent kernel (one CTA per SM).
+// These are the only dense contractions of the Occult layer:
+//  forward  -- the scattering sparse matmul (Appendix A.2 Algorithm 6, SFD -> EPD)
+//              fused with the SwiGLU activation and Algorithm 7's weight
+//              modulation, and the second linear layer of Algorithm 8;
+//  backward -- their transposes (dgrad through W_d and through [W_g; W_u], with
+//              the SwiGLU derivative fused into the first) and the per-expert
+//              weight gradients, whose reduction runs over an expert's EPD rows.
+// Algorithm 6 tiles each expert's BRIM1 row; the paper condenses the non-empty
+// parts of BRIM1 into fixed-length sub-vectors, one thread block each.  Here those
+// sub-vectors are the 128-row M tiles of every expert's contiguous EPD segment
+// (or, for weight gradients, the 64-row K blocks of that segment), scheduled by a
+// persistent kernel with one CTA per SM.
 //
-// CTA = 6 warps (contiguous A) or 10 warps (gathered A), warp-specialised:
-//   warp 0      TMA producer: B (weights) as 2-D tiles, and A as 2-D tiles when
-//               its rows are contiguous.
-//   warps 6..9  (gathered A only) copy the tile's 128 A rows -- the SFD rows of
-//               the condensed BRIM1 -- with 16-byte cp.async straight into the
-//               128-byte-swizzled layout the tensor cores read; one warp
-//               instruction moves four whole 128-byte row segments.  (TMA
-//               tile::gather4 does the same in fewer instructions but measured
-//               2.3x slower on this GEMM.)
+// CTA = 6 warps, plus 4 when an operand is gathered; warp-specialised:
+//   warp 0      TMA producer for every operand held as a plain 2-D matrix.
+//   warps 6..9  cp.async producers for a gathered operand (rows picked by the
+//               condensed BRIM1), written straight into the 128-byte swizzle the
+//               tensor cores read; zero-filled past a segment's end.  (TMA
+//               tile::gather4 measured 2.3x slower on the up-projection.)
 //   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators); lane 0
 //               issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate).
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread);
-//               SwiGLU + gate -> bf16 (the EPD intermediate feeding the second
-//               matmul), or plain -> fp32 (the merge input; every sum after the
-//               second linear layer stays in fp32).
-// Tile 128 x 256 x 64, 4 smem stages of 48 KB, both operands K-major with the
-// 128-byte swizzle.  Accumulators are double-buffered so the epilogue of one
-// tile overlaps the main loop of the next.  Every wait is bounded (2 s).
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread).
+// Tile 128 x 256 x 64, a 4-stage ring of 48 KB, accumulators double-buffered so
+// one tile's epilogue overlaps the next tile's main loop.  Operands are K-major
+// (rows along K) or MN-major (rows along K of a matrix stored K x MN); both use
+// the 128-byte swizzle.  Every wait is bounded (2 s).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -45,11 +44,21 @@ constexpr int kStages = 4;
 constexpr int kATileBytes = BM * BK * 2;   // 16 KB
 constexpr int kBTileBytes = BN * BK * 2;   // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
-constexpr int kGatherWarp0 = 6;   // first A-gather warp
-__host__ __device__ constexpr int threads_for(bool gather) { return gather ? 320 : 192; }
+constexpr int kMnAtomBytes = BK * 128;     // one 64-element MN atom over the 64 K rows
+constexpr int kGatherWarp0 = 6;            // first cp.async producer warp
 constexpr int kMaxSeg = OCCULT_MAX_EXPERTS;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
+
+__host__ __device__ constexpr bool op_gathered(int m) { return m == OP_GATHER_K || m == OP_GATHER_MN; }
+__host__ __device__ constexpr bool op_mn(int m) { return m == OP_TMA_MN || m == OP_GATHER_MN; }
+__host__ __device__ constexpr int threads_for(int am, int bm) {
+  return (op_gathered(am) || op_gathered(bm)) ? 320 : 192;
+}
+// kind::f16 instruction descriptor, bf16 A/B, fp32 D, M = 128, N = 256; bits 15
+// and 16 select MN-major A and B
+__host__ __device__ constexpr uint32_t idesc_for(int am, int bm) {
+  return idesc_bf16_f32(BM, BN) | (op_mn(am) ? (1u << 15) : 0u) | (op_mn(bm) ? (1u << 16) : 0u);
+}
 
 struct SmemTail {
   uint64_t full[kStages];
@@ -63,21 +72,30 @@ struct SmemTail {
 constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SmemTail);
 
 struct Params {
-  const __nv_bfloat16* a_ptr;  // A rows (gathered A only)
-  int64_t a_ld;                // elements between A rows
-  const int32_t* seg_off;
-  const int32_t* seg_group;
-  const int32_t* gather;
-  const float* row_gate;
-  void* out;       // bf16 with SwiGLU, fp32 otherwise
-  int64_t ldo;
-  int64_t b_group_rows;
+  // schedule
+  const int32_t* seg_off;      // rows (forward / dgrad) or K rows (wgrad) of each segment
+  const int32_t* seg_group;    // weight group or output matrix of each segment
   int n_seg;
-  int N_out;
-  int K;
-  int single_rows; // rows of the only segment when seg_off is NULL
-  int half_n;      // swiglu: rows from a group's gate rows to its up rows
+  int single_rows;             // rows of the only segment when seg_off is NULL
+  int K;                       // reduction length (forward / dgrad)
+  int N_out;                   // output columns
+  int M_total;                 // wgrad: output rows of each matrix
+  int n_tiles_m;               // wgrad: M tiles per matrix
   int n_tiles_n;
+  // operands
+  const int32_t* gather;       // source row of every gathered operand row
+  const __nv_bfloat16* g_ptr;  // gathered operand's matrix
+  int64_t g_ld;                // its row length (elements)
+  int64_t b_group_rows;        // B rows per weight group (forward / dgrad)
+  int half_n;                  // SwiGLU: up rows' offset in a B group; SwiGLU bwd: I
+  // epilogue
+  const float* row_gate;
+  void* out;                   // bf16 h (SwiGLU), fp32 (plain), bf16 dG|dU (SwiGLU bwd)
+  int64_t ldo;
+  int64_t out_group_stride;    // wgrad: elements between output matrices
+  __nv_bfloat16* gu_out;       // SwiGLU: optional copy of G|U for the backward
+  const __nv_bfloat16* gu_in;  // SwiGLU bwd: G|U saved by the forward
+  float* dg_part;              // SwiGLU bwd: [rows, n_tiles_n] partial gate gradients
   int* dev_err;
 };
 
@@ -86,32 +104,74 @@ __device__ __forceinline__ int seg_at(const Params& p, int s) {
 }
 
 struct TileInfo {
-  int seg, m0, rows, nt;
+  int seg;      // segment
+  int grp;      // weight group / output matrix
+  int m0;       // first output row (forward/dgrad: EPD row; wgrad: row of the matrix)
+  int rows;     // valid output rows
+  int nt;       // N tile
+  int k0, k1;   // wgrad: EPD rows [k0, k1) reduced over
+  int kb;       // k blocks
 };
 
+template <bool WGRAD>
 __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const int* mt_off) {
   TileInfo ti;
-  const int mt = tau / p.n_tiles_n;
-  ti.nt = tau - mt * p.n_tiles_n;
-  // largest s with mt_off[s] <= mt (segments without tiles are skipped)
-  int lo = 0, hi = p.n_seg;  // invariant: mt_off[lo] <= mt < mt_off[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (mt_off[mid] <= mt) lo = mid; else hi = mid;
+  if (WGRAD) {
+    const int per = p.n_tiles_m * p.n_tiles_n;
+    ti.seg = tau / per;
+    const int rem = tau - ti.seg * per;
+    const int mt = rem / p.n_tiles_n;
+    ti.nt = rem - mt * p.n_tiles_n;
+    ti.m0 = mt * BM;
+    ti.rows = min(BM, p.M_total - ti.m0);
+    ti.k0 = seg_at(p, ti.seg);
+    ti.k1 = seg_at(p, ti.seg + 1);
+    ti.kb = (ti.k1 - ti.k0 + BK - 1) / BK;
+  } else {
+    const int mt = tau / p.n_tiles_n;
+    ti.nt = tau - mt * p.n_tiles_n;
+    // largest s with mt_off[s] <= mt (segments without tiles are skipped)
+    int lo = 0, hi = p.n_seg;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (mt_off[mid] <= mt) lo = mid; else hi = mid;
+    }
+    ti.seg = lo;
+    ti.m0 = seg_at(p, lo) + (mt - mt_off[lo]) * BM;
+    ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
+    ti.k0 = ti.k1 = 0;
+    ti.kb = p.K / BK;
   }
-  ti.seg = lo;
-  const int s0 = seg_at(p, lo);
-  ti.m0 = s0 + (mt - mt_off[lo]) * BM;
-  ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
+  ti.grp = p.seg_group ? p.seg_group[ti.seg] : ti.seg;
   return ti;
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
-template <bool GATHER, bool SWIGLU>
-__global__ void __launch_bounds__(threads_for(GATHER), 1)
+// Shared-memory descriptor of one K=16 slice of an operand tile.
+//  K-major: rows along M/N at 128 B, 8-row groups every 1024 B; slice kk starts
+//           32 bytes further inside the swizzle atom.
+//  MN-major: 64-element MN atoms every kMnAtomBytes (leading byte offset), 8-row
+//           K groups every 1024 B (stride byte offset); slice kk starts 2 groups on.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+  if (MN) return smem_desc_sw128_mn(base + kk * 2048, kMnAtomBytes, 1024);
+  return smem_desc_sw128(base + kk * 32);
+}
+
+}  // namespace
+
+namespace {
+
+template <int AM, int BMODE, int EPI, bool WGRAD>
+__global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr bool kGather = op_gathered(AM) || op_gathered(BMODE);
+  constexpr uint32_t kIdesc = idesc_for(AM, BMODE);
+  constexpr uint32_t kTmaBytes =
+      (op_gathered(AM) ? 0u : uint32_t(kATileBytes)) + (op_gathered(BMODE) ? 0u : uint32_t(kBTileBytes));
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -122,8 +182,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // ---- prologue ------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // TMA arrival (+ one per A-gather warp)
-      mbar_init(&tail->full[s], GATHER ? 5 : 1);
+      // the TMA arrival, plus one per cp.async producer warp
+      mbar_init(&tail->full[s], kGather ? 5 : 1);
       mbar_init(&tail->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -134,14 +194,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     mbar_fence_init();
   }
   if (warp == 0) {
-    // M-tile prefix over segments (one lane walks them; at most 256)
     if (lane == 0) {
-      int acc = 0;
-      for (int s = 0; s < p.n_seg; ++s) {
-        tail->mt_off[s] = acc;
-        acc += (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
+      if (!WGRAD) {
+        // M-tile prefix over segments (at most 256)
+        int acc = 0;
+        for (int s = 0; s < p.n_seg; ++s) {
+          tail->mt_off[s] = acc;
+          acc += (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
+        }
+        tail->mt_off[p.n_seg] = acc;
       }
-      tail->mt_off[p.n_seg] = acc;
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
     }
@@ -152,10 +214,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   tc_fence_after();
 
-  const int total = tail->mt_off[p.n_seg] * p.n_tiles_n;
+  const int total = WGRAD ? p.n_seg * p.n_tiles_m * p.n_tiles_n
+                          : tail->mt_off[p.n_seg] * p.n_tiles_n;
   const uint32_t tbase = tail->tmem_base;
   volatile int* abort_flag = &tail->abort_flag;
-  const int k_blocks = p.K / BK;
 
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
@@ -163,25 +225,35 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-      const TileInfo ti = decode_tile(tau, p, tail->mt_off);
-      const int grp = p.seg_group ? p.seg_group[ti.seg] : ti.seg;
-      const int b_row0 = static_cast<int>(grp * p.b_group_rows) + ti.nt * (SWIGLU ? BN / 2 : BN);
-      for (int kb = 0; kb < k_blocks; ++kb) {
+      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+      const int n0 = ti.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+      for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
         uint8_t* sb = sa + kATileBytes;
-        if (lane == 0)
-          mbar_arrive_expect_tx(&tail->full[stage], GATHER ? kBTileBytes : kStageBytes);
-        __syncwarp();
-        if (!GATHER && lane == 0) tma_load_2d(sa, &tmA, kb * BK, ti.m0, &tail->full[stage]);
+        uint64_t* bar = &tail->full[stage];
         if (lane == 0) {
-          if (SWIGLU) {
-            tma_load_2d(sb, &tmB, kb * BK, b_row0, &tail->full[stage]);
-            tma_load_2d(sb + kBTileBytes / 2, &tmB, kb * BK, b_row0 + p.half_n, &tail->full[stage]);
-          } else {
-            tma_load_2d(sb, &tmB, kb * BK, b_row0, &tail->full[stage]);
+          mbar_arrive_expect_tx(bar, kTmaBytes);
+          // K row of an MN-major operand: weight rows (dgrad) or EPD rows (wgrad)
+          const int krow = WGRAD ? ti.k0 + kb * BK : static_cast<int>(ti.grp * p.b_group_rows) + kb * BK;
+          if (AM == OP_TMA_K) {
+            tma_load_2d(sa, &tmA, kb * BK, ti.m0, bar);
+          } else if (AM == OP_TMA_MN) {
+            for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, bar);
+          }
+          if (BMODE == OP_TMA_K) {
+            const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0;
+            if (EPI == EPI_SWIGLU) {
+              tma_load_2d(sb, &tmB, kb * BK, brow, bar);
+              tma_load_2d(sb + kBTileBytes / 2, &tmB, kb * BK, brow + p.half_n, bar);
+            } else {
+              tma_load_2d(sb, &tmB, kb * BK, brow, bar);
+            }
+          } else if (BMODE == OP_TMA_MN) {
+            for (int a = 0; a < BN / 64; ++a) tma_load_2d(sb + a * kMnAtomBytes, &tmB, n0 + 64 * a, krow, bar);
           }
         }
+        __syncwarp();
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -197,24 +269,26 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       int it = 0;
       bool ok = true;
       for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(&tail->tempty[a], aph ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tbase + a * BN;
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&tail->full[stage], phase, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kATileBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            tc_mma_f16(d_tmem, smem_desc_sw128(sa + kk * 32), smem_desc_sw128(sb + kk * 32),
+            tc_mma_f16(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
                        kIdesc, (kb | kk) != 0);
           }
           tc_commit(&tail->empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        // with no k block the commit arrives at once and the epilogue writes zeros
         if (ok) tc_commit(&tail->tfull[a]);
       }
       if (!ok) {
@@ -230,7 +304,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int it = 0;
     bool ok = true;
     for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile(tau, p, tail->mt_off);
+      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
       const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tail->tfull[a], aph, abort_flag)) { ok = false; break; }
@@ -239,7 +313,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const bool valid = row < ti.rows;
       const int64_t grow = ti.m0 + row;
       uint32_t v0[32], v1[32];
-      if (SWIGLU) {
+      if (EPI == EPI_SWIGLU) {
         const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
         const int col0 = ti.nt * (BN / 2);
 #pragma unroll 1
@@ -261,20 +335,94 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            if (p.gu_out) {
+              // G and U for the backward, rows [G | U] of 2*N_out
+              __nv_bfloat16* gu = p.gu_out + grow * (2 * static_cast<int64_t>(p.N_out)) + col0 + c;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(gu)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(gu + p.N_out)[i] =
+                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
         }
-      } else {
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        // accumulator = dh' (gradient of the modulated intermediate) for the
+        // tile's 256 columns of I; G and U come from the forward
+        const float g = valid ? p.row_gate[grow] : 0.f;
         const int col0 = ti.nt * BN;
+        const int I = p.half_n;
+        float dg = 0.f;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
           if (valid && col0 + c < p.N_out) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.out) + grow * p.ldo +
-                                                  col0 + c);
+            const uint4* gp = reinterpret_cast<const uint4*>(p.gu_in + grow * (2 * static_cast<int64_t>(I)) + col0 + c);
+            const uint4* up = reinterpret_cast<const uint4*>(p.gu_in + grow * (2 * static_cast<int64_t>(I)) + I + col0 + c);
+            uint32_t pg[16], pu[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) {
+              const uint4 x = gp[i], y = up[i];
+              pg[4 * i] = x.x; pg[4 * i + 1] = x.y; pg[4 * i + 2] = x.z; pg[4 * i + 3] = x.w;
+              pu[4 * i] = y.x; pu[4 * i + 1] = y.y; pu[4 * i + 2] = y.z; pu[4 * i + 3] = y.w;
+            }
+            uint32_t og[16], ou[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float dG[2], dU[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float G = __uint_as_float(h ? (pg[i] & 0xffff0000u) : (pg[i] << 16));
+                const float U = __uint_as_float(h ? (pu[i] & 0xffff0000u) : (pu[i] << 16));
+                const float dhp = __uint_as_float(v0[2 * i + h]);
+                const float sg = sigmoid_f(G);
+                const float s = G * sg;
+                dg = fmaf(dhp, s * U, dg);
+                const float dh = g * dhp;
+                dG[h] = dh * U * sg * (1.0f + G * (1.0f - sg));
+                dU[h] = dh * s;
+              }
+              og[i] = pack_bf16x2(dG[0], dG[1]);
+              ou[i] = pack_bf16x2(dU[0], dU[1]);
+            }
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + col0 + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              reinterpret_cast<uint4*>(o)[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
+              reinterpret_cast<uint4*>(o + I)[i] = make_uint4(ou[4 * i], ou[4 * i + 1], ou[4 * i + 2], ou[4 * i + 3]);
+            }
+          }
+        }
+        if (valid) p.dg_part[grow * p.n_tiles_n + ti.nt] = dg;
+      } else {
+        // plain fp32 tile; a weight-gradient tile without rows is zero
+        const int col0 = ti.nt * BN;
+        float* obase = static_cast<float*>(p.out) + (WGRAD ? ti.grp * p.out_group_stride : 0);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tmem_ld32(t_row + c, v0);
+          tmem_ld_wait();
+          if (valid && col0 + c < p.N_out) {
+            uint4* dst = reinterpret_cast<uint4*>(obase + grow * p.ldo + col0 + c);
+            if (WGRAD && ti.kb == 0) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
+            }
           }
         }
       }
@@ -288,38 +436,61 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
-  if (GATHER && warp >= kGatherWarp0) {
-    // ---- A gather (cp.async) -------------------------------------------------
-    // Lane l copies 16-byte chunk (l % 8) of rows (l / 8) + 4 i, i < 8, of this
-    // warp's 32 rows; chunk c of row r lands at r*128 + ((c ^ (r % 8)) * 16), the
-    // 128-byte swizzle.  A stage is signalled full kInFlight stages late, once
-    // this thread's copies for it have landed and been fenced for the async proxy.
+  if (kGather && warp >= kGatherWarp0) {
+    // ---- cp.async producers for the gathered operand ---------------------------
+    // A stage is signalled full kInFlight stages late, once this thread's copies
+    // for it have landed and been fenced for the async proxy.
     constexpr int kInFlight = kStages - 1;
-    const int gw = warp - kGatherWarp0;
-    const int chunk = lane & 7;
-    const int rsub = lane >> 3;
-    uint32_t dst_off[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = gw * 32 + rsub + 4 * i;
-      dst_off[i] = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
-    }
+    const int gt = (warp - kGatherWarp0) * 32 + lane;   // 0..127
     int stage = 0, arr_stage = 0, inflight = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-      const TileInfo ti = decode_tile(tau, p, tail->mt_off);
-      const __nv_bfloat16* src[8];
+      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+      // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
+      // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
+      // at r*128 + ((c ^ (r % 8)) * 16)
+      const __nv_bfloat16* src_k[8];
+      uint32_t dst_k[8];
+      if (AM == OP_GATHER_K) {
+        const int gw = warp - kGatherWarp0, chunk = lane & 7, rsub = lane >> 3;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = min(gw * 32 + rsub + 4 * i, ti.rows - 1);
-        src[i] = p.a_ptr + static_cast<int64_t>(p.gather[ti.m0 + r]) * p.a_ld + chunk * 8;
+        for (int i = 0; i < 8; ++i) {
+          const int r = gw * 32 + rsub + 4 * i;
+          dst_k[i] = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
+          const int rr = min(r, ti.rows - 1);
+          src_k[i] = p.g_ptr + static_cast<int64_t>(p.gather[ti.m0 + rr]) * p.g_ld + chunk * 8;
+        }
       }
-      for (int kb = 0; kb < k_blocks; ++kb) {
+      for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
+        if (AM == OP_GATHER_K) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cp_async_16(sa + dst_off[i], src[i] + kb * BK);
+          for (int i = 0; i < 8; ++i) cp_async_16(sa + dst_k[i], src_k[i] + kb * BK);
+        } else {
+          // MN-major rows (weight gradients): K row k of the stage is EPD row
+          // k0 + kb*64 + k; chunk c covers MN elements 8c..8c+7 of the tile; rows
+          // past the segment's end and columns past the matrix are zero-filled
+          constexpr bool kOnA = (AM == OP_GATHER_MN);
+          constexpr int MNT = kOnA ? BM : BN;
+          constexpr int CPR = MNT / 8;
+          uint8_t* base = kOnA ? sa : sa + kATileBytes;
+          const int mn0 = kOnA ? ti.m0 : ti.nt * BN;
+          const int mn_total = kOnA ? p.M_total : p.N_out;
+#pragma unroll
+          for (int i = 0; i < CPR / 2; ++i) {
+            const int q = gt + 128 * i;
+            const int k = q / CPR, c = q % CPR;
+            const int r = ti.k0 + kb * BK + k;
+            const bool in = r < ti.k1 && mn0 + c * 8 < mn_total;
+            const __nv_bfloat16* src = p.g_ptr;
+            if (in) src = p.g_ptr + static_cast<int64_t>(p.gather[r]) * p.g_ld + mn0 + c * 8;
+            const int off = (c >> 3) * kMnAtomBytes + (k >> 3) * 1024 + (k & 7) * 128 +
+                            (((c & 7) ^ (k & 7)) << 4);
+            cp_async_16_zfill(base + off, src, in ? 16u : 0u);
+          }
+        }
         cp_async_commit();
         if (++inflight > kInFlight) {
           cp_async_wait<kInFlight>();
@@ -384,54 +555,85 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint3
   return r == CUDA_SUCCESS ? OCCULT_OK : OCCULT_ERR_CUDA;
 }
 
-template <bool GATHER, bool SWIGLU>
+// Tensor map of one operand: K-major tiles are 64 K columns x 128 or 256 rows;
+// MN-major tiles are loaded as 64 MN columns x 64 K rows.
+int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t cols,
+                uint32_t k_major_rows) {
+  if (mode == OP_TMA_K) return make_map(m, ptr, rows, cols, BK, k_major_rows);
+  if (mode == OP_TMA_MN) return make_map(m, ptr, rows, cols, 64, BK);
+  // gathered operands are copied by cp.async: a valid placeholder map
+  return make_map(m, ptr, rows, cols, BK, BK);
+}
+
+template <int AM, int BMODE, int EPI, bool WGRAD>
 int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb, const Params& p) {
-  auto kern = grouped_gemm_tc_kernel<GATHER, SWIGLU>;
+  auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return OCCULT_ERR_CUDA;
-  kern<<<ctx.num_sms, threads_for(GATHER), kSmemBytes, ctx.stream>>>(ma, mb, p);
+  kern<<<ctx.num_sms, threads_for(AM, BMODE), kSmemBytes, ctx.stream>>>(ma, mb, p);
   return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
-  if (g.n_seg > kMaxSeg || g.K % BK != 0 || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
-  if (g.max_rows == 0 || g.n_seg == 0) return OCCULT_OK;
+  if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
+  if (!g.wgrad && g.K % BK != 0) return OCCULT_ERR_UNSUPPORTED;
+  if (g.n_seg == 0 || (!g.wgrad && g.max_rows == 0)) return OCCULT_OK;
   CUtensorMap ma, mb;
-  int rc;
-  // (gathered A is copied by cp.async; its map is made but unused)
-  rc = make_map(&ma, g.A, g.a_rows, g.K, BK, BM);
+  int rc = operand_map(&ma, g.a_mode, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
-  rc = make_map(&mb, g.B, g.b_group_rows * g.n_groups, g.K, BK, g.swiglu ? BN / 2 : BN);
+  rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols, g.epi == EPI_SWIGLU ? BN / 2 : BN);
   if (rc) return rc;
-  Params p;
+  Params p{};
   p.seg_off = g.seg_off;
   p.seg_group = g.seg_group;
+  p.n_seg = g.n_seg;
+  p.single_rows = static_cast<int>(g.max_rows);
+  p.K = g.K;
+  p.N_out = g.N_out;
+  p.M_total = g.M_total;
+  p.n_tiles_m = (g.M_total + BM - 1) / BM;
+  const int tile_n = g.epi == EPI_SWIGLU ? BN / 2 : BN;
+  p.n_tiles_n = (g.N_out + tile_n - 1) / tile_n;
   p.gather = g.gather;
-  p.a_ptr = static_cast<const __nv_bfloat16*>(g.A);
-  p.a_ld = g.K;
+  const bool a_gathered = op_gathered(g.a_mode);
+  p.g_ptr = static_cast<const __nv_bfloat16*>(a_gathered ? g.A : g.B);
+  p.g_ld = a_gathered ? g.a_cols : g.b_cols;
+  p.b_group_rows = g.b_group_rows;
+  p.half_n = g.epi == EPI_SWIGLU ? g.N_out : (g.epi == EPI_SWIGLU_BWD ? g.N_out : 0);
   p.row_gate = g.row_gate;
   p.out = g.out;
   p.ldo = g.ldo;
-  p.b_group_rows = g.b_group_rows;
-  p.n_seg = g.n_seg;
-  p.N_out = g.N_out;
-  p.K = g.K;
-  p.single_rows = static_cast<int>(g.max_rows);
-  p.half_n = g.swiglu ? g.N_out : 0;
-  const int tile_n = g.swiglu ? BN / 2 : BN;
-  p.n_tiles_n = (g.N_out + tile_n - 1) / tile_n;
+  p.out_group_stride = g.out_group_stride;
+  p.gu_out = static_cast<__nv_bfloat16*>(g.gu_out);
+  p.gu_in = static_cast<const __nv_bfloat16*>(g.gu_in);
+  p.dg_part = g.dg_part;
   p.dev_err = ctx.dev_err;
-  if (g.gather) {
-    if (!g.swiglu) return OCCULT_ERR_UNSUPPORTED;
-    return launch_tc<true, true>(ctx, ma, mb, p);
+  const int am = g.a_mode, bm = g.b_mode, ep = g.epi;
+  // the instantiations the layer uses
+  if (!g.wgrad) {
+    if (am == OP_GATHER_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
+      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false>(ctx, ma, mb, p);
+    if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_SWIGLU, false>(ctx, ma, mb, p);
+    if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_F32)
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false>(ctx, ma, mb, p);
+    if (am == OP_GATHER_K && bm == OP_TMA_MN && ep == EPI_SWIGLU_BWD)
+      return launch_tc<OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD, false>(ctx, ma, mb, p);
+    if (am == OP_TMA_K && bm == OP_TMA_MN && ep == EPI_F32)
+      return launch_tc<OP_TMA_K, OP_TMA_MN, EPI_F32, false>(ctx, ma, mb, p);
+  } else if (ep == EPI_F32) {
+    if (am == OP_GATHER_MN && bm == OP_TMA_MN)
+      return launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true>(ctx, ma, mb, p);
+    if (am == OP_TMA_MN && bm == OP_GATHER_MN)
+      return launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true>(ctx, ma, mb, p);
   }
-  return g.swiglu ? launch_tc<false, true>(ctx, ma, mb, p) : launch_tc<false, false>(ctx, ma, mb, p);
+  return OCCULT_ERR_UNSUPPORTED;
 }
 
 }  // namespace occult

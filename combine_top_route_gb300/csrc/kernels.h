@@ -29,32 +29,60 @@ size_t profile_ws_bytes(const occult_desc_t& ds, int n_tok);
 int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids, int n_tok,
                    const uint32_t* vmask, int64_t* C, float* P, int64_t* ct_hist, void* ws);
 
-// Grouped GEMM over row segments: output rows [seg_off[s], seg_off[s+1]) use
-// weight group seg_group[s] (s when NULL).  Output row r reads A row gather[r]
-// (r when NULL).  With swiglu, the group's B holds 2*N_out rows (gate rows then
-// up rows) and out = row_gate * silu(A.Bg^T) * (A.Bu^T) in the layer dtype;
-// otherwise out = A.B^T in fp32.
+// Operand modes of the grouped GEMM: the operand is a row-major matrix whose rows
+// run along K (K-major) or whose rows are K indices (MN-major: stored K x MN);
+// loaded by TMA, or gathered row by row (rows picked by `gather`) with cp.async.
+enum : int { OP_TMA_K = 0, OP_GATHER_K = 1, OP_TMA_MN = 2, OP_GATHER_MN = 3 };
+// Epilogues: SwiGLU + gate -> layer dtype (optionally also G|U); plain fp32;
+// SwiGLU backward -> dG|dU in the layer dtype plus partial gate gradients.
+enum : int { EPI_SWIGLU = 0, EPI_F32 = 1, EPI_SWIGLU_BWD = 2 };
+
+// Grouped GEMM over segments.
+//  rows mode (wgrad = false): output rows [seg_off[s], seg_off[s+1]) use weight
+//    group seg_group[s] (s when NULL); out = A . B^T over K, A rows gathered by
+//    `gather` (row r reads gather[r]) for OP_GATHER_K.  B's group g occupies rows
+//    [g*b_group_rows, (g+1)*b_group_rows) of B (K-major), or K rows likewise
+//    (MN-major).  With EPI_SWIGLU the group holds 2*N_out rows (gate then up) and
+//    out = row_gate * silu(A.Bg^T) * (A.Bu^T).
+//  wgrad mode: segment s reduces over EPD rows [seg_off[s], seg_off[s+1]) and
+//    writes matrix seg_group[s] of out (out_group_stride apart, M_total x N_out):
+//    out[m][n] = sum_r A[r][m] * B[r][n], both operands MN-major, the gathered one
+//    read at row gather[r] and zero past the segment's end.
 struct GroupedGemm {
-  const void* A;
-  int64_t a_rows;            // rows addressable in A
-  const int32_t* gather;     // nullable
-  const void* B;             // [n_groups * b_group_rows, K]
-  int64_t b_group_rows;
-  int n_groups;
-  const int32_t* seg_off;    // [n_seg + 1] device; NULL: one segment of max_rows rows
-  const int32_t* seg_group;  // [n_seg] device, nullable
-  int n_seg;
-  int64_t max_rows;          // upper bound of seg_off[n_seg]
-  const float* row_gate;     // nullable, swiglu only
-  void* out;
-  int64_t ldo;
-  int N_out;
-  int K;
-  bool swiglu;
+  int a_mode = OP_TMA_K, b_mode = OP_TMA_K, epi = EPI_F32;
+  bool wgrad = false;
+  const void* A = nullptr;
+  int64_t a_rows = 0, a_cols = 0;  // A as stored
+  const void* B = nullptr;
+  int64_t b_rows = 0, b_cols = 0;  // B as stored
+  const int32_t* gather = nullptr;
+  int64_t b_group_rows = 0;
+  int n_groups = 0;
+  const int32_t* seg_off = nullptr;   // device; NULL: one segment of max_rows rows
+  const int32_t* seg_group = nullptr; // device, nullable
+  int n_seg = 0;
+  int64_t max_rows = 0;               // upper bound of the rows (rows mode)
+  int K = 0;                          // rows mode reduction length
+  int M_total = 0;                    // wgrad: output rows per matrix
+  int N_out = 0;
+  const float* row_gate = nullptr;
+  void* out = nullptr;
+  int64_t ldo = 0;
+  int64_t out_group_stride = 0;
+  void* gu_out = nullptr;             // EPI_SWIGLU: optional G|U [rows, 2*N_out]
+  const void* gu_in = nullptr;        // EPI_SWIGLU_BWD: G|U [rows, 2*N_out]
+  float* dg_part = nullptr;           // EPI_SWIGLU_BWD: [rows, ceil(N_out/256)]
 };
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g);
 int launch_grouped_gemm_f32(const LaunchCtx& ctx, const GroupedGemm& g);
+
+size_t expert_bwd_ws_bytes(const occult_desc_t& ds);
+int launch_dg_reduce(const LaunchCtx& ctx, const float* part, int rows, int n_part, float* dg);
+int launch_gate_grad(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids,
+                     const int32_t* placement, const int32_t* brim0, const int32_t* seg_off,
+                     const int32_t* brim1, const int32_t* exp_off, const float* dg_epd,
+                     float* dgates);
 
 // s[t] = sigmoid(w . x_t) for the shared-expert gate
 int launch_shared_gate(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,

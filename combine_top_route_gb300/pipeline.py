@@ -17,9 +17,9 @@ from typing import Dict, Optional
 import torch
 
 from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, WS_BUILD_BRIM,
-               occult_build_brim, occult_combine, occult_desc_t, occult_dispatch,
-               occult_expert_down, occult_expert_up, occult_route, occult_shared_ffn,
-               workspace_size)
+               WS_EXPERT_BWD, occult_build_brim, occult_combine, occult_desc_t, occult_dispatch,
+               occult_expert_bwd, occult_expert_down, occult_expert_up, occult_gate_grad,
+               occult_route, occult_shared_ffn, workspace_size)
 
 
 def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
@@ -45,7 +45,8 @@ class OccultMoE:
     """One MoE layer resident on a CUDA device."""
 
     def __init__(self, desc: occult_desc_t, weights: Dict[str, torch.Tensor],
-                 placement: torch.Tensor, device="cuda", materialize_sfd: bool = False):
+                 placement: torch.Tensor, device="cuda", materialize_sfd: bool = False,
+                 train: bool = False):
         self.desc = desc
         dev = torch.device(device)
         dt = desc.torch_dtype
@@ -72,6 +73,21 @@ class OccultMoE:
         self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=f32)
         self.y = e(T, d, dtype=f32)
         self.y_sfd = e(n_sfd_max, d, dtype=f32) if materialize_sfd else None
+        self.train = train
+        if train:
+            # forward saves G|U; backward buffers (weight gradients are fp32)
+            self.gu_epd = e(T * k, 2 * I, dtype=dt)
+            self.dy_sfd = e(n_sfd_max, d, dtype=dt)
+            self.dgu_epd = e(T * k, 2 * I, dtype=dt)
+            self.dx_epd = e(T * k, d, dtype=f32)
+            self.dw1 = e(Ne, 2 * I, d, dtype=f32)
+            self.dw2 = e(Ne, d, I, dtype=f32)
+            self.dg_epd = e(T * k, dtype=f32)
+            self.dgates = e(T, k, dtype=f32)
+            self.dx = e(T, d, dtype=f32)
+            self.bwd_ws = e(max(1, workspace_size(desc, WS_EXPERT_BWD)), dtype=torch.uint8)
+        else:
+            self.gu_epd = None
         if desc.n_shared:
             S = desc.n_shared * desc.shared_inter
             self.h_s, self.y_s = e(T, S, dtype=dt), e(T, d, dtype=f32)
@@ -102,7 +118,7 @@ class OccultMoE:
         self.route_and_index(logits, stream)
         occult_dispatch(ds, x, self.brim0, self.vmask, self.x_sfd, self.sfd_tok, stream)
         occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
-                         self.placement, self.w["w1"], self.h_epd, stream)
+                         self.placement, self.w["w1"], self.h_epd, self.gu_epd, stream)
         occult_expert_down(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
                            self.y_epd, stream)
         if ds.n_shared:
@@ -111,3 +127,32 @@ class OccultMoE:
         occult_combine(ds, self.y_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, self.y,
                        y_shared=self.y_s, y_sfd=self.y_sfd, stream=stream)
         return self.y
+
+    @property
+    def launches_per_backward(self) -> int:
+        """Kernels one backward call launches."""
+        return 8  # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad
+
+    def backward(self, dy: torch.Tensor, stream=None):
+        """Gradients of sum(dy * y) after `forward` (train=True): (dx, dw1, dw2, dgates).
+
+        dy [T, d] in the layer dtype.  Stage one of scattering sends dy to the SFD
+        rows (BRIM0), the expert backward runs on the EPD rows (BRIM1), and the
+        two-stage merge brings dx back to the tokens; dgates return through
+        BRIM0 -> BRIM1 as well.  Router logits get no gradient here.
+        """
+        if not self.train:
+            raise RuntimeError("OccultMoE was built without train=True")
+        ds = self.desc
+        if ds.n_shared:
+            raise NotImplementedError("backward of shared experts is not provided")
+        occult_dispatch(ds, dy, self.brim0, self.vmask, self.dy_sfd, None, stream)
+        occult_expert_bwd(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate, self.exp_off,
+                          self.placement, self.w["w1"], self.w["w2"], self.h_epd, self.gu_epd,
+                          self.dgu_epd, self.dx_epd, self.dw1, self.dw2, self.dg_epd, self.bwd_ws,
+                          stream)
+        occult_combine(ds, self.dx_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, self.dx,
+                       stream=stream)
+        occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
+                         self.exp_off, self.dg_epd, self.dgates, stream)
+        return self.dx, self.dw1, self.dw2, self.dgates

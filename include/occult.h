@@ -96,6 +96,7 @@ int occult_check_desc(const occult_desc_t* desc);
 /* Workspace selectors of occult_workspace_size. */
 #define OCCULT_WS_BUILD_BRIM     0   /* occult_build_brim for desc->T tokens       */
 #define OCCULT_WS_PROFILE_COACT  1   /* occult_profile_coact for n_tok tokens      */
+#define OCCULT_WS_EXPERT_BWD     2   /* occult_expert_bwd for desc->T tokens       */
 
 /* Host: bytes of device workspace `ws` the entry point selected by `op` needs
  * (n_tok: profiled tokens, used by OCCULT_WS_PROFILE_COACT only).  The other
@@ -214,11 +215,13 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
  *   A_r = x_sfd[epd_src[r]], e = placement[s] for the slot s whose segment holds r.
  *   w1     [Ne, 2*I, d]: rows [0, I) of expert e are W_g, rows [I, 2I) are W_u.
  *   h_epd  out [T*k, I] layer dtype.
+ *   gu_epd out [T*k, 2*I] bf16, nullable: the pre-activations G | U of every EPD
+ *          row, saved for occult_expert_bwd (bf16 layers only).
  * bf16 layers run on the tcgen05 tensor cores (fp32 accumulate in TMEM).
  */
 int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
                      const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
-                     const void* w1, void* h_epd, occult_stream_t stream);
+                     const void* w1, void* h_epd, void* gu_epd, occult_stream_t stream);
 
 /*
  * occult_expert_down -- the second linear layer of Algorithm 8 on the EPD rows:
@@ -264,6 +267,40 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
 int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,
                    const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
                    const void* y_shared, void* y_sfd, void* y, occult_stream_t stream);
+
+/*
+ * occult_expert_bwd -- backward of the expert computation (bf16 layers).  The
+ * paper states that its sparse kernels serve the backward pass too (Sec. 1) but
+ * gives no backward pseudo-code; these are the derivatives of Eq. 1 run through
+ * the same BRIM-indexed layout.  With dy_sfd = occult_dispatch(dy) (stage one of
+ * scattering applied to the upstream gradient) and the forward's h_epd and gu_epd:
+ *   dh'_r   = W_d[e]^T dy_sfd[src_r]            (dgrad through W_d, gathered rows)
+ *   dg_r    = <dh'_r, silu(G_r) U_r>             -> dg_epd fp32 [T*k]
+ *   dG, dU  = g_r dh'_r * U silu'(G), g_r dh'_r * silu(G) -> dgu_epd bf16 [T*k, 2I]
+ *   dx_epd  = [dG | dU] . [W_g; W_u]           -> fp32 [T*k, d]; occult_combine merges
+ *                                                 it to dx [T, d] (stage one + two)
+ *   dw2[e]  = sum_r dy_sfd[src_r] h'_r^T        -> fp32 [Ne, d, I]
+ *   dw1[e]  = sum_r [dG | dU]_r x_sfd[src_r]^T  -> fp32 [Ne, 2I, d]
+ * Weight gradients are written, not accumulated; experts without rows get zeros.
+ *   ws  occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
+ */
+int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                      const int32_t* placement, const void* w1, const void* w2,
+                      const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
+                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
+                      occult_stream_t stream);
+
+/*
+ * occult_gate_grad -- gate gradients back in token order: dgates[t, j] =
+ * dg_epd[EPD row of (t, ids[t, j])], the row found as in the combine (BRIM0 gives
+ * the token's received row on the expert's device, BRIM1 its EPD row).
+ *   dgates out fp32 [T, k].
+ */
+int occult_gate_grad(const occult_desc_t* desc, const int32_t* ids, const int32_t* placement,
+                     const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
+                     const int32_t* exp_off, const float* dg_epd, float* dgates,
+                     occult_stream_t stream);
 
 /*
  * occult_profile_coact -- co-activation profiling (Sec. 2.1 Eq. 3-4, Sec. 2.2).

@@ -161,3 +161,62 @@ def sfd_bound(w2: np.ndarray, h_abs_rows, layer_dtype: str) -> np.ndarray:
     rel = (1.01 * BF16_HALF_ULP if layer_dtype == "bf16" else 8 * F32_EPS)
     rel += (2 * I + 2 * len(h_abs_rows) + 4) * F32_EPS
     return rel * B
+
+
+def expert_backward_bounds(x, dy, w1e, w2e, gate, layer_dtype="bf16"):
+    """Oracle-side intermediates and per-element error bounds of one expert's rows.
+
+    x, dy [n, d] are the rows' token inputs and upstream gradients (exact bf16
+    values), gate [n] their routing weights, w1e [2I, d], w2e [d, I].  The GPU
+    saves G and U in bf16 in the forward, reads h' = g silu(G) U in bf16, rounds
+    dG and dU to bf16 and accumulates every contraction in fp32.  Returns a dict
+    with fp64 references and bounds:
+      dG, dU, dG_b, dU_b [n, I]; dx_rows, dx_rows_b [n, d] (each row's W1^T dGU);
+      dg, dg_b [n]; h1 (= h'), h1_b [n, I]; dW1_b [2I, d]; dW2_b [d, I].
+    """
+    f64 = np.float64
+    x = np.asarray(x, f64)
+    dy = np.asarray(dy, f64)
+    wg = np.asarray(w1e, f64)[: w1e.shape[0] // 2]
+    wu = np.asarray(w1e, f64)[w1e.shape[0] // 2:]
+    wd = np.asarray(w2e, f64)
+    g = np.asarray(gate, f64)[:, None]
+    n, d = x.shape
+    I = wg.shape[0]
+    u = BF16_HALF_ULP
+    acc = lambda K, m: 2 * K * F32_EPS * m  # noqa: E731  fp32 accumulation of K terms
+    G = x @ wg.T
+    U = x @ wu.T
+    aG = acc(d, np.abs(x) @ np.abs(wg).T)
+    aU = acc(d, np.abs(x) @ np.abs(wu).T)
+    dG_st = aG * (1 + u) + u * np.abs(G)      # |stored bf16 G - G|
+    dU_st = aU * (1 + u) + u * np.abs(U)
+    sig = 1.0 / (1.0 + np.exp(-G))
+    s = G * sig
+    h1 = g * s * U
+    h1_32 = np.abs(g) * (1.1 * np.abs(U) * aG + np.abs(s) * aU + 1.1 * aG * aU) + 8 * F32_EPS * np.abs(h1)
+    h1_b = h1_32 * (1 + u) + u * np.abs(h1)
+    dhp = dy @ wd
+    ddhp = acc(d, np.abs(dy) @ np.abs(wd))
+    ds = 1.1 * dG_st
+    sU = s * U
+    dg = np.sum(dhp * sU, axis=1)
+    dg_b = np.sum(ddhp * np.abs(sU) + np.abs(dhp) * (ds * np.abs(U) + np.abs(s) * dU_st + ds * dU_st),
+                  axis=1) + acc(I, np.sum(np.abs(dhp * sU), axis=1)) + 1e-30
+    silu1 = sig * (1.0 + G * (1.0 - sig))
+    dG = g * dhp * U * silu1
+    dU = g * dhp * s
+    dG_pre = np.abs(g) * (ddhp * np.abs(U * silu1) +
+                          np.abs(dhp) * (1.1 * dU_st + 0.5 * np.abs(U) * dG_st + 0.5 * dG_st * dU_st))
+    dG_pre += 8 * F32_EPS * np.abs(dG)
+    dU_pre = np.abs(g) * (ddhp * np.abs(s) + np.abs(dhp) * ds) + 8 * F32_EPS * np.abs(dU)
+    dG_b = dG_pre * (1 + u) + u * np.abs(dG)
+    dU_b = dU_pre * (1 + u) + u * np.abs(dU)
+    dx_rows = dG @ wg + dU @ wu
+    dGa, dUa = np.abs(dG) + dG_b, np.abs(dU) + dU_b
+    dx_rows_b = dG_b @ np.abs(wg) + dU_b @ np.abs(wu) + acc(2 * I, dGa @ np.abs(wg) + dUa @ np.abs(wu))
+    ax = np.abs(x)
+    dW1_b = np.concatenate([dG_b.T @ ax, dU_b.T @ ax]) + acc(n, np.concatenate([dGa.T @ ax, dUa.T @ ax]))
+    dW2_b = np.abs(dy).T @ h1_b + acc(n, np.abs(dy).T @ (np.abs(h1) + h1_b))
+    return dict(dG=dG, dU=dU, dG_b=dG_b, dU_b=dU_b, dx_rows=dx_rows, dx_rows_b=dx_rows_b,
+                dg=dg, dg_b=dg_b, h1=h1, h1_b=h1_b, dW1_b=dW1_b, dW2_b=dW2_b)
