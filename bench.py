@@ -266,42 +266,58 @@ def run_ours(args, cfg, world, rank, local):
     logits = synth.measured_logits(cfg).to(dev)
     x = synth.hidden_states(cfg, device=dev)
     w = synth.expert_weights(cfg, device=dev)
-    moe = occ.OccultMoE(ds, w, L, device=dev)
+    train = bool(cfg.backward)
+    moe = occ.OccultMoE(ds, w, L, device=dev, train=train)
+    dy = synth.upstream_grad(cfg, device=dev) if train else None
     stream = torch.cuda.current_stream(dev)
-
-    # per-call events over the timed region, on the launching stream
-    calls = ["route", "build_brim", "dispatch", "expert_up", "expert_down", "combine"]
     T, k, d, I = cfg.T, cfg.top_k, cfg.d, cfg.inter
 
+    # one step as named C-ABI calls, in Algorithm 2's order (+ the backward)
+    calls = [
+        ("route", lambda: occ.occult_route(ds, logits, moe.expert_to_vdev, moe.ids, moe.gates,
+                                           moe.vmask, stream)),
+        ("build_brim", lambda: occ.occult_build_brim(
+            ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0, moe.seg_off, moe.brim1,
+            moe.exp_off, moe.epd_src, moe.epd_gate, moe.counts, moe.brim_ws, stream)),
+        ("dispatch", lambda: occ.occult_dispatch(ds, x, moe.brim0, moe.vmask, moe.x_sfd,
+                                                 moe.sfd_tok, stream)),
+        ("expert_up", lambda: occ.occult_expert_up(ds, moe.x_sfd, moe.epd_src, moe.epd_gate,
+                                                   moe.exp_off, moe.placement, moe.w["w1"],
+                                                   moe.h_epd, moe.gu_epd, stream=stream)),
+        ("expert_down", lambda: occ.occult_expert_down(ds, moe.h_epd, moe.exp_off, moe.placement,
+                                                       moe.w["w2"], moe.y_epd, stream)),
+    ]
+    if ds.n_shared:
+        calls.append(("shared_ffn", lambda: occ.occult_shared_ffn(
+            ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s, moe.s_gate, moe.y_s,
+            stream)))
+    calls.append(("combine", lambda: occ.occult_combine(ds, moe.y_epd, moe.brim0, moe.seg_off,
+                                                        moe.brim1, moe.exp_off, moe.y,
+                                                        y_shared=moe.y_s, stream=stream)))
+    if train:
+        calls += [
+            ("dispatch_dy", lambda: occ.occult_dispatch(ds, dy, moe.brim0, moe.vmask, moe.dy_sfd,
+                                                        None, stream)),
+            ("expert_bwd", lambda: occ.occult_expert_bwd(
+                ds, moe.x_sfd, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
+                moe.w["w1"], moe.w["w2"], moe.h_epd, moe.gu_epd, moe.dgu_epd, moe.dx_epd, moe.dw1,
+                moe.dw2, moe.dg_epd, moe.bwd_ws, stream)),
+            ("combine_dx", lambda: occ.occult_combine(ds, moe.dx_epd, moe.brim0, moe.seg_off,
+                                                      moe.brim1, moe.exp_off, moe.dx,
+                                                      stream=stream)),
+            ("gate_grad", lambda: occ.occult_gate_grad(ds, moe.ids, moe.placement, moe.brim0,
+                                                       moe.seg_off, moe.brim1, moe.exp_off,
+                                                       moe.dg_epd, moe.dgates, stream)),
+        ]
+    names = [c[0] for c in calls]
+
     def step(ev=None):
+        for j, (_, fn) in enumerate(calls):
+            if ev is not None:
+                ev[j].record(stream)
+            fn()
         if ev is not None:
-            ev[0].record(stream)
-        occ.occult_route(ds, logits, moe.expert_to_vdev, moe.ids, moe.gates, moe.vmask, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        occ.occult_build_brim(ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0,
-                              moe.seg_off, moe.brim1, moe.exp_off, moe.epd_src, moe.epd_gate,
-                              moe.counts, moe.brim_ws, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        occ.occult_dispatch(ds, x, moe.brim0, moe.vmask, moe.x_sfd, moe.sfd_tok, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        occ.occult_expert_up(ds, moe.x_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
-                             moe.placement, moe.w["w1"], moe.h_epd, stream)
-        if ev is not None:
-            ev[4].record(stream)
-        occ.occult_expert_down(ds, moe.h_epd, moe.exp_off, moe.placement, moe.w["w2"],
-                               moe.y_epd, stream)
-        if ev is not None:
-            ev[5].record(stream)
-        if ds.n_shared:
-            occ.occult_shared_ffn(ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s,
-                                  moe.s_gate, moe.y_s, stream)
-        occ.occult_combine(ds, moe.y_epd, moe.brim0, moe.seg_off, moe.brim1, moe.exp_off,
-                           moe.y, y_shared=moe.y_s, stream=stream)
-        if ev is not None:
-            ev[6].record(stream)
+            ev[len(calls)].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -323,13 +339,14 @@ def run_ours(args, cfg, world, rank, local):
 
     # ---- per-call durations (separate pass with events between calls) ------
     n_prof = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_prof)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+           for _ in range(n_prof)]
     torch.cuda.synchronize(dev)
     for i in range(n_prof):
         step(evs[i])
     torch.cuda.synchronize(dev)
     per_call = {c: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_prof))
-                for j, c in enumerate(calls)}
+                for j, c in enumerate(names)}
     n_sfd = int(moe.counts[0].item())
 
     # ---- end to end through the public API with host buffers ----------------
@@ -339,11 +356,17 @@ def run_ours(args, cfg, world, rank, local):
     x_d = torch.empty_like(x)
     lg_d = torch.empty_like(logits)
 
+    dy_h = dy.cpu().pin_memory() if train else None
+    dy_d = torch.empty_like(dy) if train else None
+
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
         y = moe.forward(lg_d, x_d, stream)
         y_h.copy_(y, non_blocking=True)
+        if train:
+            dy_d.copy_(dy_h, non_blocking=True)
+            moe.backward(dy_d, stream)
 
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()
@@ -363,7 +386,8 @@ def run_ours(args, cfg, world, rank, local):
     flops_up = 4.0 * d * I * T * k
     flops_down = 2.0 * d * I * T * k
     b = 2  # bytes per bf16 element (x, x_sfd); y_epd and y are fp32
-    kernels = {
+    kernels = {c: {"ms": per_call[c]} for c in names}
+    kernels.update({
         "route": {"ms": per_call["route"]},
         "build_brim": {"ms": per_call["build_brim"]},
         "dispatch": {"ms": per_call["dispatch"],
@@ -374,8 +398,13 @@ def run_ours(args, cfg, world, rank, local):
                         "TFLOP/s": flops_down / per_call["expert_down"] / 1e9},
         "combine": {"ms": per_call["combine"],
                     "GB/s": (T * k * d * 4 + T * d * 4) / per_call["combine"] / 1e6},
-    }
-    dom = max(("expert_up", "expert_down"), key=lambda c: per_call[c])
+    })
+    gemms = ["expert_up", "expert_down"]
+    if train:
+        # dgrad through W_d and W1, wgrad of W_d and W1: twice the forward FLOPs
+        kernels["expert_bwd"]["TFLOP/s"] = 2 * (flops_up + flops_down) / per_call["expert_bwd"] / 1e9
+        gemms.append("expert_bwd")
+    dom = max(gemms, key=lambda c: per_call[c])
     achieved = kernels[dom]["TFLOP/s"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops,
                 "unit": "TFLOP/s", "frac": achieved / tflops, "traffic": recorded_traffic(dom),
@@ -397,9 +426,11 @@ def run_ours(args, cfg, world, rank, local):
         "E[C_T]": n_sfd / T,
         "a2a_bytes_per_direction": n_sfd * d * b,
         "clocks": clk.summary(),
-        "gpu_launches": moe.launches_per_forward * args.steps,
+        "gpu_launches": (moe.launches_per_forward + (moe.launches_per_backward if train else 0))
+                        * args.steps,
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * 4,
+                "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * 4
+                                      + (dy.numel() * dy.element_size() if train else 0),
                 "d2h_bytes_per_step": T * d * 4},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
