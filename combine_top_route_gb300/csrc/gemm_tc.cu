@@ -462,7 +462,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           src_k[i] = p.g_ptr + static_cast<int64_t>(p.gather[ti.m0 + rr]) * p.g_ld + chunk * 8;
         }
       }
+      // MN-major gathers: a warp touches 16 K rows of a stage; lane j < 16 holds
+      // the source row of the warp's j-th one, loaded one stage ahead (-1 past the
+      // segment's end) and handed to the copying lanes by shuffle
+      constexpr int CPR = (AM == OP_GATHER_MN ? BM : BN) / 8;   // chunks per K row
+      const int gw = warp - kGatherWarp0;
+      const int jrow = CPR == 32 ? gw + 4 * (lane & 15) : 2 * gw + (lane & 1) + 8 * ((lane & 15) >> 1);
+      auto load_idx = [&](int kb) -> int {
+        const int r = ti.k0 + kb * BK + jrow;
+        return r < ti.k1 ? p.gather[r] : -1;
+      };
+      int idx_cur = (WGRAD && ti.kb > 0) ? load_idx(0) : -1;
       for (int kb = 0; kb < ti.kb; ++kb) {
+        const int idx_next = (WGRAD && kb + 1 < ti.kb) ? load_idx(kb + 1) : -1;
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
         if (AM == OP_GATHER_K) {
@@ -473,8 +485,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           // k0 + kb*64 + k; chunk c covers MN elements 8c..8c+7 of the tile; rows
           // past the segment's end and columns past the matrix are zero-filled
           constexpr bool kOnA = (AM == OP_GATHER_MN);
-          constexpr int MNT = kOnA ? BM : BN;
-          constexpr int CPR = MNT / 8;
           uint8_t* base = kOnA ? sa : sa + kATileBytes;
           const int mn0 = kOnA ? ti.m0 : ti.nt * BN;
           const int mn_total = kOnA ? p.M_total : p.N_out;
@@ -482,15 +492,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           for (int i = 0; i < CPR / 2; ++i) {
             const int q = gt + 128 * i;
             const int k = q / CPR, c = q % CPR;
-            const int r = ti.k0 + kb * BK + k;
-            const bool in = r < ti.k1 && mn0 + c * 8 < mn_total;
+            const int j = CPR == 32 ? i : (lane >> 4) + 2 * i;
+            const int src_row = __shfl_sync(0xffffffffu, idx_cur, j);
+            const bool in = src_row >= 0 && mn0 + c * 8 < mn_total;
             const __nv_bfloat16* src = p.g_ptr;
-            if (in) src = p.g_ptr + static_cast<int64_t>(p.gather[r]) * p.g_ld + mn0 + c * 8;
+            if (in) src = p.g_ptr + static_cast<int64_t>(src_row) * p.g_ld + mn0 + c * 8;
             const int off = (c >> 3) * kMnAtomBytes + (k >> 3) * 1024 + (k & 7) * 128 +
                             (((c & 7) ^ (k & 7)) << 4);
             cp_async_16_zfill(base + off, src, in ? 16u : 0u);
           }
         }
+        idx_cur = idx_next;
         cp_async_commit();
         if (++inflight > kInFlight) {
           cp_async_wait<kInFlight>();
