@@ -171,6 +171,15 @@ __device__ __forceinline__ void cp_async_16_zfill(void* smem_dst, const void* gs
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
                :: "r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes) : "memory");
 }
+// The mbarrier receives one arrival (counted in its expected arrivals) once every
+// cp.async this thread issued so far has completed; the thread does not wait.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -60,7 +60,10 @@ __host__ __device__ constexpr uint32_t idesc_for(int am, int bm) {
   return idesc_bf16_f32(BM, BN) | (op_mn(am) ? (1u << 15) : 0u) | (op_mn(bm) ? (1u << 16) : 0u);
 }
 
+constexpr int kEpiStride = 36;  // words per staged row (32 + 4 padding)
+
 struct SmemTail {
+  uint32_t epi[4][32 * kEpiStride];  // per epilogue warp: 32 rows x 32 words
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
@@ -146,6 +149,32 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
   return ti;
 }
 
+// Writes a warp's 32 rows x W words (one row per lane, W = 16: 32 bf16, W = 32:
+// 32 fp32) through shared memory so that the global stores cover whole
+// row segments: W/4 lanes per row, 128/W rows per instruction.  Rows >= valid
+// are not written.  `out` is the address of the warp's first row at this column.
+template <int W>
+__device__ __forceinline__ void store_rows(uint32_t* buf, const uint32_t* v, char* out,
+                                           int64_t row_bytes, int valid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < W / 4; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * kEpiStride + 4 * j) =
+        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  __syncwarp();
+  constexpr int LPR = W / 4;     // lanes per row
+  constexpr int RPI = 32 / LPR;  // rows per instruction
+#pragma unroll
+  for (int it = 0; it < 32 / RPI; ++it) {
+    const int r = it * RPI + lane / LPR;
+    const int c4 = lane % LPR;
+    if (r < valid)
+      st_v4(out + r * row_bytes + c4 * 16,
+            *reinterpret_cast<const uint4*>(buf + r * kEpiStride + 4 * c4));
+  }
+  __syncwarp();
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 __device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
@@ -182,8 +211,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // ---- prologue ------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // the TMA arrival, plus one per cp.async producer warp
-      mbar_init(&tail->full[s], kGather ? 5 : 1);
+      // the TMA arrival, plus one per cp.async producer thread
+      mbar_init(&tail->full[s], kGather ? 1 + 128 : 1);
       mbar_init(&tail->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -277,6 +306,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t d_tmem = tbase + a * BN;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&tail->full[stage], phase, abort_flag)) { ok = false; break; }
+          // cp.async data arrived through the generic proxy: make it visible to
+          // the tensor cores' (async proxy) operand reads
+          if (kGather) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kATileBytes;
@@ -312,6 +344,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t t_row = tbase + a * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const bool valid = row < ti.rows;
       const int64_t grow = ti.m0 + row;
+      const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
+      const int64_t wrow0 = ti.m0 + quarter * 32;
+      uint32_t* ebuf = tail->epi[quarter];
       uint32_t v0[32], v1[32];
       if (EPI == EPI_SWIGLU) {
         const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
@@ -321,7 +356,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           tmem_ld32(t_row + c, v0);
           tmem_ld32(t_row + BN / 2 + c, v1);
           tmem_ld_wait();
-          if (valid && col0 + c < p.N_out) {
+          if (col0 + c < p.N_out) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -330,29 +365,31 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                   g * silu_f(__uint_as_float(v0[2 * i + 1])) * __uint_as_float(v1[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                  grow * p.ldo + col0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            if (p.gu_out) {
-              // G and U for the backward, rows [G | U] of 2*N_out
-              __nv_bfloat16* gu = p.gu_out + grow * (2 * static_cast<int64_t>(p.N_out)) + col0 + c;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                pk[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-              }
+            // one 64-byte row segment per thread (stores were measured not to limit
+            // this kernel, and staging them costs more than it saves)
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                    grow * p.ldo + col0 + c);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
-                reinterpret_cast<uint4*>(gu)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              if (p.gu_out) {
+                // G and U for the backward, rows [G | U] of 2*N_out
+                uint4* gu = reinterpret_cast<uint4*>(p.gu_out + grow * (2 * static_cast<int64_t>(p.N_out)) + col0 + c);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                pk[i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+                for (int i = 0; i < 4; ++i)
+                  gu[i] = make_uint4(pack_bf16x2(__uint_as_float(v0[8 * i]), __uint_as_float(v0[8 * i + 1])),
+                                     pack_bf16x2(__uint_as_float(v0[8 * i + 2]), __uint_as_float(v0[8 * i + 3])),
+                                     pack_bf16x2(__uint_as_float(v0[8 * i + 4]), __uint_as_float(v0[8 * i + 5])),
+                                     pack_bf16x2(__uint_as_float(v0[8 * i + 6]), __uint_as_float(v0[8 * i + 7])));
+                gu += p.N_out / 8;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  gu[i] = make_uint4(pack_bf16x2(__uint_as_float(v1[8 * i]), __uint_as_float(v1[8 * i + 1])),
+                                     pack_bf16x2(__uint_as_float(v1[8 * i + 2]), __uint_as_float(v1[8 * i + 3])),
+                                     pack_bf16x2(__uint_as_float(v1[8 * i + 4]), __uint_as_float(v1[8 * i + 5])),
+                                     pack_bf16x2(__uint_as_float(v1[8 * i + 6]), __uint_as_float(v1[8 * i + 7])));
               }
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                reinterpret_cast<uint4*>(gu + p.N_out)[i] =
-                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
           }
         }
@@ -367,9 +404,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int c = 0; c < BN; c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
-          if (valid && col0 + c < p.N_out) {
-            const uint4* gp = reinterpret_cast<const uint4*>(p.gu_in + grow * (2 * static_cast<int64_t>(I)) + col0 + c);
-            const uint4* up = reinterpret_cast<const uint4*>(p.gu_in + grow * (2 * static_cast<int64_t>(I)) + I + col0 + c);
+          if (col0 + c < p.N_out) {
+            const int64_t grow_c = valid ? grow : ti.m0;  // rows past the tile read its first row
+            const uint4* gp = reinterpret_cast<const uint4*>(p.gu_in + grow_c * (2 * static_cast<int64_t>(I)) + col0 + c);
+            const uint4* up = reinterpret_cast<const uint4*>(p.gu_in + grow_c * (2 * static_cast<int64_t>(I)) + I + col0 + c);
             uint32_t pg[16], pu[16];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -396,12 +434,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
               og[i] = pack_bf16x2(dG[0], dG[1]);
               ou[i] = pack_bf16x2(dU[0], dU[1]);
             }
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + col0 + c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              reinterpret_cast<uint4*>(o)[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
-              reinterpret_cast<uint4*>(o + I)[i] = make_uint4(ou[4 * i], ou[4 * i + 1], ou[4 * i + 2], ou[4 * i + 3]);
-            }
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0 + c;
+            store_rows<16>(ebuf, og, reinterpret_cast<char*>(o), p.ldo * 2, wrows);
+            store_rows<16>(ebuf, ou, reinterpret_cast<char*>(o + I), p.ldo * 2, wrows);
           }
         }
         if (valid) p.dg_part[grow * p.n_tiles_n + ti.nt] = dg;
@@ -413,16 +448,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int c = 0; c < BN; c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
-          if (valid && col0 + c < p.N_out) {
-            uint4* dst = reinterpret_cast<uint4*>(obase + grow * p.ldo + col0 + c);
+          if (col0 + c < p.N_out) {
             if (WGRAD && ti.kb == 0) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_uint4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
+              for (int i = 0; i < 32; ++i) v0[i] = 0u;
             }
+            store_rows<32>(ebuf, v0, reinterpret_cast<char*>(obase + wrow0 * p.ldo + col0 + c),
+                           p.ldo * 4, wrows);
           }
         }
       }
@@ -438,11 +470,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 
   if (kGather && warp >= kGatherWarp0) {
     // ---- cp.async producers for the gathered operand ---------------------------
-    // A stage is signalled full kInFlight stages late, once this thread's copies
-    // for it have landed and been fenced for the async proxy.
-    constexpr int kInFlight = kStages - 1;
+    // Every thread arrives on a stage's full barrier asynchronously, when its
+    // copies for that stage have landed (cp.async.mbarrier.arrive); the MMA thread
+    // fences them for the async proxy after its wait.
     const int gt = (warp - kGatherWarp0) * 32 + lane;   // 0..127
-    int stage = 0, arr_stage = 0, inflight = 0;
+    int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
@@ -503,28 +535,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
         idx_cur = idx_next;
-        cp_async_commit();
-        if (++inflight > kInFlight) {
-          cp_async_wait<kInFlight>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tail->full[arr_stage]);
-          if (++arr_stage == kStages) arr_stage = 0;
-          --inflight;
-        }
+        cp_async_arrive_noinc(&tail->full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
     // every copy lands before the CTA may exit, also after an abort
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (ok) {
-      for (; inflight > 0; --inflight) {
-        if (lane == 0) mbar_arrive(&tail->full[arr_stage]);
-        if (++arr_stage == kStages) arr_stage = 0;
-      }
-    } else {
+    cp_async_wait_all();
+    if (!ok) {
       if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
       *abort_flag = 1;
     }
