@@ -374,7 +374,7 @@ int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
     g.gu_in = gu_epd; g.dg_part = dg_part;
     rc = launch_grouped_gemm_bf16(ctx, g);
     if (rc) return rc;
-    rc = launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), (I + 255) / 256, dg_epd);
+    rc = launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), 2 * ((I + 255) / 256), dg_epd);
     if (rc) return rc;
     // dx_epd = [dG|dU] . [W_g; W_u] (W1 read MN-major), fp32
     GroupedGemm h;

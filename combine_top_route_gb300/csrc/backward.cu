@@ -48,7 +48,8 @@ int blocks_for(const LaunchCtx& ctx, int64_t n) {
 }  // namespace
 
 size_t expert_bwd_ws_bytes(const occult_desc_t& ds) {
-  const size_t n_part = (static_cast<size_t>(ds.inter) + 255) / 256;
+  // one partial gate gradient per EPD row, 256-column tile of I and column half
+  const size_t n_part = 2 * ((static_cast<size_t>(ds.inter) + 255) / 256);
   return static_cast<size_t>(ds.T) * ds.top_k * n_part * sizeof(float);
 }
 

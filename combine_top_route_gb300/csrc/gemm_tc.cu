@@ -45,14 +45,16 @@ constexpr int kATileBytes = BM * BK * 2;   // 16 KB
 constexpr int kBTileBytes = BN * BK * 2;   // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kMnAtomBytes = BK * 128;     // one 64-element MN atom over the 64 K rows
-constexpr int kGatherWarp0 = 6;            // first cp.async producer warp
+constexpr int kEpiWarp0 = 2;               // first epilogue warp
+constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, half the columns each
+constexpr int kGatherWarp0 = kEpiWarp0 + kEpiWarps;  // first cp.async producer warp
 constexpr int kMaxSeg = OCCULT_MAX_EXPERTS;
 constexpr uint32_t kTmemCols = 512;
 
 __host__ __device__ constexpr bool op_gathered(int m) { return m == OP_GATHER_K || m == OP_GATHER_MN; }
 __host__ __device__ constexpr bool op_mn(int m) { return m == OP_TMA_MN || m == OP_GATHER_MN; }
 __host__ __device__ constexpr int threads_for(int am, int bm) {
-  return (op_gathered(am) || op_gathered(bm)) ? 320 : 192;
+  return 32 * (kGatherWarp0 + ((op_gathered(am) || op_gathered(bm)) ? 4 : 0));
 }
 // kind::f16 instruction descriptor, bf16 A/B, fp32 D, M = 128, N = 256; bits 15
 // and 16 select MN-major A and B
@@ -60,10 +62,8 @@ __host__ __device__ constexpr uint32_t idesc_for(int am, int bm) {
   return idesc_bf16_f32(BM, BN) | (op_mn(am) ? (1u << 15) : 0u) | (op_mn(bm) ? (1u << 16) : 0u);
 }
 
-constexpr int kEpiStride = 36;  // words per staged row (32 + 4 padding)
-
 struct SmemTail {
-  uint32_t epi[4][32 * kEpiStride];  // per epilogue warp: 32 rows x 32 words
+  uint32_t epi[kEpiWarps][32 * 32];  // per epilogue warp: 32 rows x 32 words, XOR-swizzled
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
@@ -98,7 +98,7 @@ struct Params {
   int64_t out_group_stride;    // wgrad: elements between output matrices
   __nv_bfloat16* gu_out;       // SwiGLU: optional copy of G|U for the backward
   const __nv_bfloat16* gu_in;  // SwiGLU bwd: G|U saved by the forward
-  float* dg_part;              // SwiGLU bwd: [rows, n_tiles_n] partial gate gradients
+  float* dg_part;              // SwiGLU bwd: [rows, 2 * n_tiles_n] partial gate gradients
   int* dev_err;
 };
 
@@ -150,16 +150,18 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
 }
 
 // Writes a warp's 32 rows x W words (one row per lane, W = 16: 32 bf16, W = 32:
-// 32 fp32) through shared memory so that the global stores cover whole
-// row segments: W/4 lanes per row, 128/W rows per instruction.  Rows >= valid
-// are not written.  `out` is the address of the warp's first row at this column.
+// 32 fp32) through shared memory so that the global stores cover whole row
+// segments: W/4 lanes per row, 128/W rows per instruction.  16-byte chunk c of
+// row r is kept at chunk c ^ (r % 8) of its 128-byte row (no bank conflicts on
+// either side).  Rows >= valid are not written.  `out` is the address of the
+// warp's first row at this column.
 template <int W>
 __device__ __forceinline__ void store_rows(uint32_t* buf, const uint32_t* v, char* out,
                                            int64_t row_bytes, int valid) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < W / 4; ++j)
-    *reinterpret_cast<uint4*>(buf + lane * kEpiStride + 4 * j) =
+    *reinterpret_cast<uint4*>(buf + lane * 32 + 4 * (j ^ (lane & 7))) =
         make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   __syncwarp();
   constexpr int LPR = W / 4;     // lanes per row
@@ -170,7 +172,7 @@ __device__ __forceinline__ void store_rows(uint32_t* buf, const uint32_t* v, cha
     const int c4 = lane % LPR;
     if (r < valid)
       st_v4(out + r * row_bytes + c4 * 16,
-            *reinterpret_cast<const uint4*>(buf + r * kEpiStride + 4 * c4));
+            *reinterpret_cast<const uint4*>(buf + r * 32 + 4 * (c4 ^ (r & 7))));
   }
   __syncwarp();
 }
@@ -217,7 +219,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
-      mbar_init(&tail->tempty[a], 4);
+      mbar_init(&tail->tempty[a], kEpiWarps);
     }
     tail->abort_flag = 0;
     mbar_fence_init();
@@ -332,6 +334,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp < kGatherWarp0) {
     // ---- epilogue ----------------------------------------------------------
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = (warp - kEpiWarp0) / 4;  // which half of the tile's columns
     const int row = quarter * 32 + lane;
     int it = 0;
     bool ok = true;
@@ -346,13 +349,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const int64_t grow = ti.m0 + row;
       const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
       const int64_t wrow0 = ti.m0 + quarter * 32;
-      uint32_t* ebuf = tail->epi[quarter];
+      uint32_t* ebuf = tail->epi[warp - kEpiWarp0];
       uint32_t v0[32], v1[32];
       if (EPI == EPI_SWIGLU) {
         const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
         const int col0 = ti.nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld32(t_row + BN / 2 + c, v1);
           tmem_ld_wait();
@@ -401,7 +404,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int I = p.half_n;
         float dg = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
           if (col0 + c < p.N_out) {
@@ -439,13 +442,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             store_rows<16>(ebuf, ou, reinterpret_cast<char*>(o + I), p.ldo * 2, wrows);
           }
         }
-        if (valid) p.dg_part[grow * p.n_tiles_n + ti.nt] = dg;
+        // one partial per (row, N tile, column half)
+        if (valid) p.dg_part[grow * (2 * p.n_tiles_n) + 2 * ti.nt + half] = dg;
       } else {
         // plain fp32 tile; a weight-gradient tile without rows is zero
         const int col0 = ti.nt * BN;
         float* obase = static_cast<float*>(p.out) + (WGRAD ? ti.grp * p.out_group_stride : 0);
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           tmem_ld32(t_row + c, v0);
           tmem_ld_wait();
           if (col0 + c < p.N_out) {

@@ -71,7 +71,7 @@ struct GroupedGemm {
   int64_t out_group_stride = 0;
   void* gu_out = nullptr;             // EPI_SWIGLU: optional G|U [rows, 2*N_out]
   const void* gu_in = nullptr;        // EPI_SWIGLU_BWD: G|U [rows, 2*N_out]
-  float* dg_part = nullptr;           // EPI_SWIGLU_BWD: [rows, ceil(N_out/256)]
+  float* dg_part = nullptr;           // EPI_SWIGLU_BWD: [rows, 2 * ceil(N_out/256)]
 };
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g);
