@@ -34,6 +34,7 @@ ERR_DEVICE_TIMEOUT = -5
 WS_BUILD_BRIM = 0
 WS_PROFILE_COACT = 1
 WS_EXPERT_BWD = 2
+STATIC_SCRATCH_BYTES = 1183744   # OCCULT_STATIC_SCRATCH_BYTES
 
 
 class occult_desc_t(ctypes.Structure):

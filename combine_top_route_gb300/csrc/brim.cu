@@ -9,8 +9,9 @@
 // and the BRIM0 entry of (d, t) is seg_off[d] + #{tokens t' < t using device d}.
 // So both are exclusive prefix counts over tokens, one column per device and one
 // per expert slot, computed with warp ballots and popcounts:
-//   1. count  -- every CTA counts its 256-token tile per column;
-//   2. scan   -- one CTA turns the tile counts into per-tile column offsets, and
+//   1. count  -- every CTA counts its 64-token tile per column;
+//   2. scan   -- one CTA (a warp scan per column) turns the tile counts into per-tile
+//                column offsets, and
 //                the column totals into seg_off / exp_off;
 //   3. fill   -- every CTA re-counts per warp, adds the warp prefix to its tile
 //                offsets and writes BRIM0, BRIM1, epd_src and epd_gate.
@@ -22,8 +23,8 @@ namespace occult {
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kTile = kWarps * 32;  // tokens per CTA
+constexpr int kWarps = 2;
+constexpr int kTile = kWarps * 32;  // tokens per CTA (small tiles: many CTAs in flight)
 constexpr int kDevCols = 32;        // device columns (padded to the ballot width)
 
 __host__ __device__ constexpr int ncols(int Ne) { return kDevCols + Ne + 1; }  // + max C_T
@@ -107,7 +108,8 @@ brim_count_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ 
   }
 }
 
-// One CTA: exclusive scan of every column over tiles, then the offsets.
+// One CTA: exclusive scan of every column over tiles (one warp per column, 32
+// tiles per step), then the offsets.
 __global__ void __launch_bounds__(1024)
 brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ tile_cnt,
                  int32_t* __restrict__ seg_off, int32_t* __restrict__ exp_off,
@@ -115,19 +117,30 @@ brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ tile_cnt,
   __shared__ int s_tot[kDevCols + OCCULT_MAX_EXPERTS + 1];
   __shared__ int s_off[kDevCols + OCCULT_MAX_EXPERTS + 1];
   const int nc = ncols(Ne);
-  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  for (int c = threadIdx.x >> 5; c < nc; c += blockDim.x >> 5) {
     int run = 0;
-    for (int b = 0; b < n_tiles; ++b) {
-      int32_t* p = tile_cnt + static_cast<size_t>(b) * nc + c;
-      const int v = *p;
+    for (int b0 = 0; b0 < n_tiles; b0 += 32) {
+      const int b = b0 + lane;
+      int32_t* pcell = tile_cnt + static_cast<size_t>(b) * nc + c;
+      const int v = b < n_tiles ? *pcell : 0;
       if (c == nc - 1) {
-        run = max(run, v);
+        int m = v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        run = max(run, m);
       } else {
-        *p = run;
-        run += v;
+        int inc = v;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, inc, sh);
+          if (lane >= sh) inc += u;
+        }
+        if (b < n_tiles) *pcell = run + inc - v;
+        run += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
-    s_tot[c] = run;
+    if (lane == 0) s_tot[c] = run;
   }
   __syncthreads();
   if (threadIdx.x == 0) {

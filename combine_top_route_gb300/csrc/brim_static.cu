@@ -26,7 +26,7 @@ namespace occult {
 namespace {
 
 // Enough for any layer with T <= 65536 tokens and Ne <= 256 experts:
-// ceil(T/256) tiles x (32 + Ne + 1) int32 columns.
+// ceil(T/64) tiles x (32 + Ne + 1) int32 columns.
 static __device__ __align__(256) int32_t g_brim_scratch[OCCULT_STATIC_SCRATCH_BYTES / sizeof(int32_t)];
 
 constexpr int kMaxDevices = 64;

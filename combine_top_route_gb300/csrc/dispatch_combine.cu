@@ -57,13 +57,14 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ brim0,
 // With y_sfd given, also writes each device's stage-one sum there (and does not
 // write y: the stage-two kernel does, from y_sfd).  Everything is fp32.
 template <bool WRITE_SFD>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 3)
 combine_fused_kernel(const float* __restrict__ y_epd, const int32_t* __restrict__ brim0,
                      const int32_t* __restrict__ seg_off, const int32_t* __restrict__ brim1,
                      const int32_t* __restrict__ exp_off, const float* __restrict__ y_shared,
                      int ntok, int Nd, int n_loc, int D, float* __restrict__ y_sfd,
                      float* __restrict__ y) {
   constexpr int VN = 4;
+  constexpr int kChunk = 8;  // EPD rows loaded per pass (all of them for k <= 8)
   __shared__ int s_rows[kWarps][OCCULT_MAX_TOPK];
   __shared__ int s_devs[kWarps][OCCULT_MAX_TOPK];
   __shared__ int s_sfd[kWarps][OCCULT_MAX_VDEV];
@@ -112,26 +113,29 @@ combine_fused_kernel(const float* __restrict__ y_epd, const int32_t* __restrict_
       float acc[VN], part[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f, part[i] = 0.f;
-      float4 buf[OCCULT_MAX_TOPK];
+      for (int j0 = 0; j0 < n; j0 += kChunk) {
+        float4 buf[kChunk];
 #pragma unroll
-      for (int j = 0; j < OCCULT_MAX_TOPK; ++j)
-        if (j < n) {
-          const uint4 u = ld_nc_v4(reinterpret_cast<const float4*>(y_epd + static_cast<size_t>(rows[j]) * D) + v);
-          buf[j] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                               __uint_as_float(u.w));
-        }
+        for (int j = 0; j < kChunk; ++j)
+          if (j0 + j < n) {
+            const uint4 u = ld_nc_v4(reinterpret_cast<const float4*>(y_epd + static_cast<size_t>(rows[j0 + j]) * D) + v);
+            buf[j] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                 __uint_as_float(u.w));
+          }
 #pragma unroll
-      for (int j = 0; j < OCCULT_MAX_TOPK; ++j) {
-        if (j < n) {
-          part[0] += buf[j].x; part[1] += buf[j].y; part[2] += buf[j].z; part[3] += buf[j].w;
-          // close the device's stage-one sum at its last expert
-          if (j + 1 == n || devs[j + 1] != devs[j]) {
-            if (WRITE_SFD) {
-              st_v4(reinterpret_cast<float4*>(y_sfd + static_cast<size_t>(sfd[devs[j]]) * D) + v,
-                    pack16(part, float()));
+        for (int j = 0; j < kChunk; ++j) {
+          const int jj = j0 + j;
+          if (jj < n) {
+            part[0] += buf[j].x; part[1] += buf[j].y; part[2] += buf[j].z; part[3] += buf[j].w;
+            // close the device's stage-one sum at its last expert
+            if (jj + 1 == n || devs[jj + 1] != devs[jj]) {
+              if (WRITE_SFD) {
+                st_v4(reinterpret_cast<float4*>(y_sfd + static_cast<size_t>(sfd[devs[jj]]) * D) + v,
+                      pack16(part, float()));
+              }
+#pragma unroll
+              for (int i = 0; i < VN; ++i) acc[i] += part[i], part[i] = 0.f;
             }
-#pragma unroll
-            for (int i = 0; i < VN; ++i) acc[i] += part[i], part[i] = 0.f;
           }
         }
       }
@@ -181,7 +185,7 @@ combine_sfd_kernel(const float* __restrict__ y_sfd, const int32_t* __restrict__ 
 
 int grid_for(const LaunchCtx& ctx, int ntok) {
   int blocks = (ntok + kWarps - 1) / kWarps;
-  const int cap = ctx.num_sms * 8;
+  const int cap = ctx.num_sms * 16;
   return blocks < cap ? (blocks > 0 ? blocks : 1) : cap;
 }
 

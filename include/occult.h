@@ -188,7 +188,7 @@ int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float
  *             with that device current; make that first call before any stream
  *             capture on the device.
  */
-#define OCCULT_STATIC_SCRATCH_BYTES 295936
+#define OCCULT_STATIC_SCRATCH_BYTES 1183744
 int occult_build_brim_noalloc(const occult_desc_t* desc, const int32_t* ids, const float* gates,
                               const uint32_t* vmask, const int32_t* placement,
                               int32_t* brim0, int32_t* seg_off, int32_t* brim1,
