@@ -23,8 +23,8 @@ namespace occult {
 
 namespace {
 
-constexpr int kWarps = 2;
-constexpr int kTile = kWarps * 32;  // tokens per CTA (small tiles: many CTAs in flight)
+constexpr int kTile = 32;           // tokens per tile: one warp
+constexpr int kWarpsPerCta = 4;
 constexpr int kDevCols = 32;        // device columns (padded to the ballot width)
 
 __host__ __device__ constexpr int ncols(int Ne) { return kDevCols + Ne + 1; }  // + max C_T
@@ -39,6 +39,7 @@ __device__ __forceinline__ unsigned mask_bit(const uint64_t* m, int s) {
   return static_cast<unsigned>(w >> (s & 63)) & 1u;
 }
 
+// slot mask of token t: bit s set iff the token chose the expert in slot s
 template <int W64>
 __device__ __forceinline__ void slot_mask(const int32_t* __restrict__ ids, int t, int k, bool valid,
                                           const int* s_slot_of, uint64_t* m) {
@@ -53,77 +54,54 @@ __device__ __forceinline__ void slot_mask(const int32_t* __restrict__ ids, int t
   }
 }
 
-// Per-warp column counts of one 32-token chunk into s_wcnt[warp][col].
+// 1. count: one warp per 32-token tile writes its column counts, column-major
+//    (cnt[c * n_tiles + tile]); the last column holds the tile's max C_T.
 template <int W64>
-__device__ __forceinline__ void warp_counts(const int32_t* __restrict__ ids,
-                                           const uint32_t* __restrict__ vmask, int T, int k,
-                                           int Ne, int Nd, const int* s_slot_of, int t0,
-                                           int* wcnt, uint64_t* m, uint32_t* vm_out) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+brim_count_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ vmask,
+                  const int32_t* __restrict__ placement, int T, int k, int Ne, int Nd,
+                  int n_tiles, int32_t* __restrict__ cnt) {
+  constexpr int NS = 64 * W64;
+  __shared__ int s_slot_of[NS];
+  for (int s = threadIdx.x; s < Ne; s += blockDim.x) s_slot_of[placement[s]] = s;
+  __syncthreads();
   const int lane = threadIdx.x & 31;
-  const int t = t0 + lane;
+  const int tile = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (tile >= n_tiles) return;
+  const int t = tile * kTile + lane;
   const bool valid = t < T;
   const uint32_t vm = valid ? vmask[t] : 0u;
+  uint64_t m[W64];
   slot_mask<W64>(ids, t, k, valid, s_slot_of, m);
-  for (int d = lane; d < kDevCols; d += 32) wcnt[d] = 0;
-  for (int d = 0; d < Nd; ++d) {
-    const unsigned bal = __ballot_sync(0xffffffffu, (vm >> d) & 1u);
-    if (lane == 0) wcnt[d] = __popc(bal);
+  for (int d = 0; d < kDevCols; ++d) {
+    const unsigned bal = __ballot_sync(0xffffffffu, d < Nd && ((vm >> d) & 1u));
+    if (lane == 0) cnt[static_cast<size_t>(d) * n_tiles + tile] = __popc(bal);
   }
   for (int s = 0; s < Ne; ++s) {
     const unsigned bal = __ballot_sync(0xffffffffu, mask_bit<W64>(m, s));
-    if (lane == 0) wcnt[kDevCols + s] = __popc(bal);
+    if (lane == 0) cnt[static_cast<size_t>(kDevCols + s) * n_tiles + tile] = __popc(bal);
   }
   int ct = __popc(vm);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ct = max(ct, __shfl_xor_sync(0xffffffffu, ct, o));
-  if (lane == 0) wcnt[kDevCols + Ne] = ct;
-  *vm_out = vm;
+  if (lane == 0) cnt[static_cast<size_t>(kDevCols + Ne) * n_tiles + tile] = ct;
 }
 
-template <int W64>
-__global__ void __launch_bounds__(kTile)
-brim_count_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ vmask,
-                  const int32_t* __restrict__ placement, int T, int k, int Ne, int Nd,
-                  int32_t* __restrict__ tile_cnt) {
-  constexpr int NS = 64 * W64;
-  __shared__ int s_slot_of[NS];
-  __shared__ int s_wcnt[kWarps][kDevCols + NS + 1];
-  const int warp = threadIdx.x >> 5;
-  for (int s = threadIdx.x; s < Ne; s += kTile) s_slot_of[placement[s]] = s;
-  __syncthreads();
-  uint64_t m[W64];
-  uint32_t vm;
-  warp_counts<W64>(ids, vmask, T, k, Ne, Nd, s_slot_of, blockIdx.x * kTile + warp * 32,
-                   s_wcnt[warp], m, &vm);
-  __syncthreads();
-  const int nc = ncols(Ne);
-  for (int c = threadIdx.x; c < nc; c += kTile) {
-    int v = 0;
-    if (c == nc - 1) {
-      for (int w = 0; w < kWarps; ++w) v = max(v, s_wcnt[w][c]);
-    } else {
-      for (int w = 0; w < kWarps; ++w) v += s_wcnt[w][c];
-    }
-    tile_cnt[static_cast<size_t>(blockIdx.x) * nc + c] = v;
-  }
-}
-
-// One CTA: exclusive scan of every column over tiles (one warp per column, 32
-// tiles per step), then the offsets.
+// 2. scan: one CTA, one warp per column: exclusive prefix over tiles (32 tiles
+//    per step, coalesced), then seg_off / exp_off from the column totals.
 __global__ void __launch_bounds__(1024)
-brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ tile_cnt,
+brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ cnt,
                  int32_t* __restrict__ seg_off, int32_t* __restrict__ exp_off,
                  int32_t* __restrict__ counts) {
   __shared__ int s_tot[kDevCols + OCCULT_MAX_EXPERTS + 1];
-  __shared__ int s_off[kDevCols + OCCULT_MAX_EXPERTS + 1];
   const int nc = ncols(Ne);
   const int lane = threadIdx.x & 31;
   for (int c = threadIdx.x >> 5; c < nc; c += blockDim.x >> 5) {
+    int32_t* col = cnt + static_cast<size_t>(c) * n_tiles;
     int run = 0;
     for (int b0 = 0; b0 < n_tiles; b0 += 32) {
       const int b = b0 + lane;
-      int32_t* pcell = tile_cnt + static_cast<size_t>(b) * nc + c;
-      const int v = b < n_tiles ? *pcell : 0;
+      const int v = b < n_tiles ? col[b] : 0;
       if (c == nc - 1) {
         int m = v;
 #pragma unroll
@@ -136,7 +114,7 @@ brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ tile_cnt,
           const int u = __shfl_up_sync(0xffffffffu, inc, sh);
           if (lane >= sh) inc += u;
         }
-        if (b < n_tiles) *pcell = run + inc - v;
+        if (b < n_tiles) col[b] = run + inc - v;
         run += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
@@ -145,97 +123,80 @@ brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ tile_cnt,
   __syncthreads();
   if (threadIdx.x == 0) {
     int a = 0;
-    for (int d = 0; d < Nd; ++d) s_off[d] = a, a += s_tot[d];
-    s_off[Nd] = a;
+    for (int d = 0; d < Nd; ++d) seg_off[d] = a, a += s_tot[d];
+    seg_off[Nd] = a;
     counts[0] = a;
     int e = 0;
-    for (int s = 0; s < Ne; ++s) s_off[kDevCols + s] = e, e += s_tot[kDevCols + s];
-    s_off[kDevCols + Ne] = e;
+    for (int s = 0; s < Ne; ++s) exp_off[s] = e, e += s_tot[kDevCols + s];
+    exp_off[Ne] = e;
     counts[1] = e;
     counts[2] = s_tot[nc - 1];
     counts[3] = 0;
   }
-  __syncthreads();
-  for (int d = threadIdx.x; d <= Nd; d += blockDim.x) seg_off[d] = s_off[d];
-  for (int s = threadIdx.x; s <= Ne; s += blockDim.x) exp_off[s] = s_off[kDevCols + s];
-  // tile offsets become absolute: tile prefix + column offset
-  for (int i = threadIdx.x; i < n_tiles * nc; i += blockDim.x) {
-    const int c = i % nc;
-    if (c < Nd) tile_cnt[i] += s_off[c];
-    else if (c >= kDevCols && c < kDevCols + Ne) tile_cnt[i] += s_off[c];
-  }
 }
 
+// 3. fill: one warp per (tile, device): BRIM0 of device d for the tile's tokens,
+//    then BRIM1 and the EPD arrays of d's expert slots.  Offsets are the tile's
+//    exclusive prefix plus the column offset (seg_off / exp_off).
 template <int W64>
-__global__ void __launch_bounds__(kTile)
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
 brim_fill_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gates,
                  const uint32_t* __restrict__ vmask, const int32_t* __restrict__ placement,
-                 int T, int k, int Ne, int Nd, int n_loc, const int32_t* __restrict__ tile_off,
-                 const int32_t* __restrict__ seg_off, const int32_t* __restrict__ exp_off,
-                 int32_t* __restrict__ brim0, int32_t* __restrict__ brim1,
-                 int32_t* __restrict__ epd_src, float* __restrict__ epd_gate) {
+                 int T, int k, int Ne, int Nd, int n_loc, int n_tiles,
+                 const int32_t* __restrict__ pre, const int32_t* __restrict__ seg_off,
+                 const int32_t* __restrict__ exp_off, int32_t* __restrict__ brim0,
+                 int32_t* __restrict__ brim1, int32_t* __restrict__ epd_src,
+                 float* __restrict__ epd_gate) {
   constexpr int NS = 64 * W64;
   __shared__ int s_slot_of[NS];
   __shared__ int s_expert[NS];
-  __shared__ int s_wcnt[kWarps][kDevCols + NS + 1];
-  __shared__ int s_seg[kDevCols + 1];
-  __shared__ int s_ebase[kDevCols];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int nc = ncols(Ne);
-  for (int s = threadIdx.x; s < Ne; s += kTile) {
+  for (int s = threadIdx.x; s < Ne; s += blockDim.x) {
     s_slot_of[placement[s]] = s;
     s_expert[s] = placement[s];
   }
-  for (int d = threadIdx.x; d <= Nd; d += kTile) s_seg[d] = seg_off[d];
-  for (int d = threadIdx.x; d < Nd; d += kTile) s_ebase[d] = exp_off[d * n_loc];
   __syncthreads();
-  uint64_t m[W64];
-  uint32_t vm;
-  const int t0 = blockIdx.x * kTile + warp * 32;
-  warp_counts<W64>(ids, vmask, T, k, Ne, Nd, s_slot_of, t0, s_wcnt[warp], m, &vm);
-  __syncthreads();
-  // exclusive prefix over the warps of this tile, plus the tile's offsets
-  const int32_t* toff = tile_off + static_cast<size_t>(blockIdx.x) * nc;
-  for (int c = threadIdx.x; c < nc - 1; c += kTile) {
-    int run = (c < Nd || (c >= kDevCols && c < kDevCols + Ne)) ? toff[c] : 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int v = s_wcnt[w][c];
-      s_wcnt[w][c] = run;
-      run += v;
-    }
-  }
-  __syncthreads();
-  const int t = t0 + lane;
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (w >= n_tiles * Nd) return;
+  const int tile = w / Nd, d = w - tile * Nd;
+  const int t = tile * kTile + lane;
   const bool valid = t < T;
-  if (t0 >= T) return;
+  const unsigned lt = lanemask_lt();
+  // BRIM0 (Algorithm 3)
+  const uint32_t vm = valid ? vmask[t] : 0u;
+  const unsigned bit = (vm >> d) & 1u;
+  const unsigned bal = __ballot_sync(0xffffffffu, bit);
+  const int dbase = pre[static_cast<size_t>(d) * n_tiles + tile] + seg_off[d];
+  const int sfd = bit ? dbase + __popc(bal & lt) : -1;
+  if (valid) brim0[static_cast<size_t>(d) * T + t] = sfd;
+  if (bal == 0) return;
+  // BRIM1 (Algorithm 5) of device d and the condensed EPD arrays
+  uint64_t m[W64];
+  slot_mask<W64>(ids, t, k, valid, s_slot_of, m);
   int my_ids[OCCULT_MAX_TOPK];
   float my_g[OCCULT_MAX_TOPK];
 #pragma unroll
   for (int j = 0; j < OCCULT_MAX_TOPK; ++j) {
-    my_ids[j] = (valid && j < k) ? ids[static_cast<size_t>(t) * k + j] : -1;
-    my_g[j] = (valid && j < k) ? gates[static_cast<size_t>(t) * k + j] : 0.f;
+    my_ids[j] = (bit && j < k) ? ids[static_cast<size_t>(t) * k + j] : -1;
+    my_g[j] = (bit && j < k) ? gates[static_cast<size_t>(t) * k + j] : 0.f;
   }
-  const int* wb = s_wcnt[warp];
-  const unsigned lt = lanemask_lt();
-  for (int d = 0; d < Nd; ++d) {
-    // BRIM0 (Algorithm 3)
-    const unsigned bit = (vm >> d) & 1u;
-    const unsigned bal = __ballot_sync(0xffffffffu, bit);
-    const int sfd = bit ? wb[d] + __popc(bal & lt) : -1;
-    if (valid) brim0[static_cast<size_t>(d) * T + t] = sfd;
-    if (bal == 0) continue;
-    // BRIM1 (Algorithm 5) of device d and the condensed EPD arrays
-    const int r_local = sfd - s_seg[d];
-    const int ebase = s_ebase[d];
-    for (int j = 0; j < n_loc; ++j) {
-      const int s = d * n_loc + j;
+  const int r_local = sfd - seg_off[d];
+  const int ebase = exp_off[d * n_loc];
+  for (int j0 = 0; j0 < n_loc; j0 += 32) {
+    // lane i holds the row base of slot d*n_loc + j0 + i
+    const int sl = d * n_loc + j0 + lane;
+    const int sbase_l = (j0 + lane < n_loc)
+        ? pre[static_cast<size_t>(kDevCols + sl) * n_tiles + tile] + exp_off[sl] : 0;
+    const int jn = min(32, n_loc - j0);
+    for (int j = 0; j < jn; ++j) {
+      const int s = d * n_loc + j0 + j;
       const unsigned sbit = mask_bit<W64>(m, s);
       const unsigned sbal = __ballot_sync(0xffffffffu, sbit);
+      const int sbase = __shfl_sync(0xffffffffu, sbase_l, j);
       if (bit) {
         int val = -1;
         if (sbit) {
-          const int row = wb[kDevCols + s] + __popc(sbal & lt);
+          const int row = sbase + __popc(sbal & lt);
           val = row - ebase;
           const int e = s_expert[s];
           float g = 0.f;
@@ -264,21 +225,23 @@ int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32
                       int32_t* epd_src, float* epd_gate, int32_t* counts, void* ws) {
   const int n_loc = ds.n_experts / ds.n_vdev;
   const int tiles = (ds.T + kTile - 1) / kTile;
-  int32_t* tile_cnt = static_cast<int32_t*>(ws);
+  int32_t* cnt = static_cast<int32_t*>(ws);
   const int T = ds.T, k = ds.top_k, Ne = ds.n_experts, Nd = ds.n_vdev;
+  const int cgrid = (tiles + kWarpsPerCta - 1) / kWarpsPerCta;
+  const int fgrid = (tiles * Nd + kWarpsPerCta - 1) / kWarpsPerCta;
 #define OCCULT_BRIM_COUNT(W)                                                                   \
-  brim_count_kernel<W><<<tiles, kTile, 0, ctx.stream>>>(ids, vmask, placement, T, k, Ne, Nd,    \
-                                                        tile_cnt)
+  brim_count_kernel<W><<<cgrid, kWarpsPerCta * 32, 0, ctx.stream>>>(ids, vmask, placement, T, k, \
+                                                                    Ne, Nd, tiles, cnt)
 #define OCCULT_BRIM_FILL(W)                                                                    \
-  brim_fill_kernel<W><<<tiles, kTile, 0, ctx.stream>>>(ids, gates, vmask, placement, T, k, Ne,  \
-                                                       Nd, n_loc, tile_cnt, seg_off, exp_off,   \
-                                                       brim0, brim1, epd_src, epd_gate)
+  brim_fill_kernel<W><<<fgrid, kWarpsPerCta * 32, 0, ctx.stream>>>(                            \
+      ids, gates, vmask, placement, T, k, Ne, Nd, n_loc, tiles, cnt, seg_off, exp_off, brim0,  \
+      brim1, epd_src, epd_gate)
   if (tiles > 0) {
     if (Ne <= 64) OCCULT_BRIM_COUNT(1);
     else if (Ne <= 128) OCCULT_BRIM_COUNT(2);
     else OCCULT_BRIM_COUNT(4);
   }
-  brim_scan_kernel<<<1, 1024, 0, ctx.stream>>>(tiles, Ne, Nd, tile_cnt, seg_off, exp_off, counts);
+  brim_scan_kernel<<<1, 1024, 0, ctx.stream>>>(tiles, Ne, Nd, cnt, seg_off, exp_off, counts);
   if (tiles > 0) {
     if (Ne <= 64) OCCULT_BRIM_FILL(1);
     else if (Ne <= 128) OCCULT_BRIM_FILL(2);

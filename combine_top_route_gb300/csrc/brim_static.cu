@@ -25,8 +25,8 @@ namespace occult {
 
 namespace {
 
-// Enough for any layer with T <= 65536 tokens and Ne <= 256 experts:
-// ceil(T/64) tiles x (32 + Ne + 1) int32 columns.
+// Enough for any layer with T <= 32768 tokens and Ne <= 256 experts:
+// ceil(T/32) tiles x (32 + Ne + 1) int32 columns.
 static __device__ __align__(256) int32_t g_brim_scratch[OCCULT_STATIC_SCRATCH_BYTES / sizeof(int32_t)];
 
 constexpr int kMaxDevices = 64;

@@ -178,8 +178,8 @@ int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float
  *   Scratch:  a static device array of OCCULT_STATIC_SCRATCH_BYTES inside the
  *             library, loaded on every GPU that uses the library and kept until
  *             the process exits.  A layer needing more scratch than that (more
- *             than 65536 tokens at 256 experts) gets OCCULT_ERR_WORKSPACE and no
- *             launch.  Nothing in the array has to start at zero, and each call
+ *             than 32768 tokens at 256 experts, 97600 at 64) gets
+ *             OCCULT_ERR_WORKSPACE and no launch.  Nothing in the array has to start at zero, and each call
  *             leaves its contents behind.
  *   Sharing:  every call on a device uses the same array, so calls that overlap
  *             on the GPU (unordered streams) race and give wrong results; order
