@@ -11,21 +11,30 @@
 // parts of BRIM1 into fixed-length sub-vectors, one thread block each.  Here those
 // sub-vectors are the 128-row M tiles of every expert's contiguous EPD segment
 // (or, for weight gradients, the 64-row K blocks of that segment), scheduled by a
-// persistent kernel with one CTA per SM.
+// persistent kernel.
 //
-// CTA = 6 warps, plus 4 when an operand is gathered; warp-specialised:
-//   warp 0      TMA producer for every operand held as a plain 2-D matrix.
-//   warps 6..9  cp.async producers for a gathered operand (rows picked by the
-//               condensed BRIM1), written straight into the 128-byte swizzle the
-//               tensor cores read; zero-filled past a segment's end.  (TMA
-//               tile::gather4 measured 2.3x slower on the up-projection.)
-//   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators); lane 0
-//               issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate).
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one row per thread).
-// Tile 128 x 256 x 64, a 4-stage ring of 48 KB, accumulators double-buffered so
-// one tile's epilogue overlaps the next tile's main loop.  Operands are K-major
-// (rows along K) or MN-major (rows along K of a matrix stored K x MN); both use
-// the 128-byte swizzle.  Every wait is bounded (2 s).
+// GEMMs whose A is a plain matrix (the second linear layer, the dgrad through
+// [W_g; W_u], the shared experts) run on CTA pairs (2-CTA clusters, one CTA per
+// SM): tcgen05.mma.cta_group::2 computes a 256 x 256 tile, rows 0..127 in the
+// even CTA, 128..255 (the segment's next M tile) in the odd one; each CTA stages
+// its own 128 A rows and half of the 256 B rows, so a 64-deep k block moves
+// 32 KB into each SM instead of 48 KB and six stages fit.  GEMMs with gathered
+// rows run one 128 x 256 tile per CTA with four 48 KB stages.
+//
+// CTA = 10 warps, plus 4 when an operand is gathered; warp-specialised:
+//   warp 0       TMA producer for every operand held as a plain 2-D matrix.
+//   warp 1       owns TMEM (512 columns = two 128x256 fp32 accumulators, double-
+//                buffered so one tile's epilogue overlaps the next main loop);
+//                lane 0 issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate)
+//                -- in a pair only the even CTA's, for both.
+//   warps 2..9   epilogue: tcgen05.ld of the accumulator, two warps per TMEM
+//                lane quarter (half of the columns each).
+//   warps 10..13 cp.async producers for a gathered operand (rows picked by the
+//                condensed BRIM1), written straight into the 128-byte swizzle the
+//                tensor cores read; zero-filled past a segment's end.  (TMA
+//                tile::gather4 measured 2.3x slower on the up-projection.)
+// Operands are K-major (rows along K) or MN-major (rows along K of a matrix
+// stored K x MN); both use the 128-byte swizzle.  Every wait is bounded (2 s).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -40,10 +49,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int kStages = 4;
 constexpr int kATileBytes = BM * BK * 2;   // 16 KB
 constexpr int kBTileBytes = BN * BK * 2;   // 32 KB
-constexpr int kStageBytes = kATileBytes + kBTileBytes;
+constexpr int kMaxStages = 6;
 constexpr int kMnAtomBytes = BK * 128;     // one 64-element MN atom over the 64 K rows
 constexpr int kEpiWarp0 = 2;               // first epilogue warp
 constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, half the columns each
@@ -51,28 +59,37 @@ constexpr int kGatherWarp0 = kEpiWarp0 + kEpiWarps;  // first cp.async producer 
 constexpr int kMaxSeg = OCCULT_MAX_EXPERTS;
 constexpr uint32_t kTmemCols = 512;
 
+// A CTA pair keeps half of the B tile per CTA: 32 KB stages, six of them, in the
+// shared memory that holds four 48 KB stages of a single CTA.
+__host__ __device__ constexpr int stages_for(bool pair) { return pair ? 6 : 4; }
+__host__ __device__ constexpr int b_stage_bytes(bool pair) { return pair ? kBTileBytes / 2 : kBTileBytes; }
+__host__ __device__ constexpr int stage_bytes(bool pair) { return kATileBytes + b_stage_bytes(pair); }
 __host__ __device__ constexpr bool op_gathered(int m) { return m == OP_GATHER_K || m == OP_GATHER_MN; }
 __host__ __device__ constexpr bool op_mn(int m) { return m == OP_TMA_MN || m == OP_GATHER_MN; }
 __host__ __device__ constexpr int threads_for(int am, int bm) {
   return 32 * (kGatherWarp0 + ((op_gathered(am) || op_gathered(bm)) ? 4 : 0));
 }
-// kind::f16 instruction descriptor, bf16 A/B, fp32 D, M = 128, N = 256; bits 15
-// and 16 select MN-major A and B
-__host__ __device__ constexpr uint32_t idesc_for(int am, int bm) {
-  return idesc_bf16_f32(BM, BN) | (op_mn(am) ? (1u << 15) : 0u) | (op_mn(bm) ? (1u << 16) : 0u);
+// kind::f16 instruction descriptor, bf16 A/B, fp32 D, M = 128 (a CTA pair: 256),
+// N = 256; bits 15 and 16 select MN-major A and B
+__host__ __device__ constexpr uint32_t idesc_for(int am, int bm, bool pair) {
+  return idesc_bf16_f32(pair ? 2 * BM : BM, BN) | (op_mn(am) ? (1u << 15) : 0u) |
+         (op_mn(bm) ? (1u << 16) : 0u);
 }
 
 struct SmemTail {
   uint32_t epi[kEpiWarps][32 * 32];  // per epilogue warp: 32 rows x 32 words, XOR-swizzled
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
   int abort_flag;
   int mt_off[kMaxSeg + 1];
 };
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + sizeof(SmemTail);
+__host__ __device__ constexpr int smem_bytes(bool pair) {
+  return 1024 /*alignment slack*/ + stages_for(pair) * stage_bytes(pair) + static_cast<int>(sizeof(SmemTail));
+}
+static_assert(smem_bytes(false) <= 232448 && smem_bytes(true) <= 232448, "shared memory");
 
 struct Params {
   // schedule
@@ -116,8 +133,13 @@ struct TileInfo {
   int kb;       // k blocks
 };
 
-template <bool WGRAD>
-__device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const int* mt_off) {
+// Tile tau of the schedule.  For a CTA pair tau is a unit of
+// two consecutive M tiles of one segment and `rank` picks one; a segment with an
+// odd number of M tiles ends with a unit whose second tile has no rows (it
+// repeats the first tile's rows and stores nothing).
+template <bool WGRAD, bool PAIR>
+__device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const int* mt_off,
+                                                int rank) {
   TileInfo ti;
   if (WGRAD) {
     const int per = p.n_tiles_m * p.n_tiles_n;
@@ -140,8 +162,12 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
       if (mt_off[mid] <= mt) lo = mid; else hi = mid;
     }
     ti.seg = lo;
-    ti.m0 = seg_at(p, lo) + (mt - mt_off[lo]) * BM;
+    ti.m0 = seg_at(p, lo) + (PAIR ? 2 * (mt - mt_off[lo]) + rank : mt - mt_off[lo]) * BM;
     ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
+    if (PAIR && ti.rows <= 0) {
+      ti.m0 -= BM;
+      ti.rows = 0;
+    }
     ti.k0 = ti.k1 = 0;
     ti.kb = p.K / BK;
   }
@@ -195,20 +221,34 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 namespace {
 
-template <int AM, int BMODE, int EPI, bool WGRAD>
+template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+  static_assert(!(PAIR && (WGRAD || AM != OP_TMA_K || op_gathered(BMODE))),
+                "CTA pairs run the forward / dgrad GEMMs whose A is a plain matrix");
+  constexpr int kStages = stages_for(PAIR);
+  constexpr int kStageBytes = stage_bytes(PAIR);
+  constexpr int kBBytes = b_stage_bytes(PAIR);
   constexpr bool kGather = op_gathered(AM) || op_gathered(BMODE);
-  constexpr uint32_t kIdesc = idesc_for(AM, BMODE);
-  constexpr uint32_t kTmaBytes =
-      (op_gathered(AM) ? 0u : uint32_t(kATileBytes)) + (op_gathered(BMODE) ? 0u : uint32_t(kBTileBytes));
+  constexpr uint32_t kIdesc = idesc_for(AM, BMODE, PAIR);
+  // TMA bytes of one stage of one CTA; a pair's even CTA expects both CTAs' bytes
+  constexpr uint32_t kTmaCta =
+      (op_gathered(AM) ? 0u : uint32_t(kATileBytes)) + (op_gathered(BMODE) ? 0u : uint32_t(kBBytes));
+  constexpr uint32_t kTmaBytes = PAIR ? 2 * kTmaCta : kTmaCta;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SmemTail* tail = reinterpret_cast<SmemTail*>(smem + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // A CTA pair (2-CTA cluster) walks the schedule as one unit; its even CTA
+  // (rank 0) issues the MMAs for both and owns the full / accumulator-empty
+  // barriers they wait on.
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+  const int n_units = PAIR ? gridDim.x >> 1 : gridDim.x;
 
   // ---- prologue ------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -219,7 +259,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
-      mbar_init(&tail->tempty[a], kEpiWarps);
+      mbar_init(&tail->tempty[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     tail->abort_flag = 0;
     mbar_fence_init();
@@ -227,11 +267,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     if (lane == 0) {
       if (!WGRAD) {
-        // M-tile prefix over segments (at most 256)
+        // M-tile (pair: two-tile unit) prefix over segments (at most 256)
         int acc = 0;
         for (int s = 0; s < p.n_seg; ++s) {
           tail->mt_off[s] = acc;
-          acc += (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
+          const int mt = (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
+          acc += PAIR ? (mt + 1) / 2 : mt;
         }
         tail->mt_off[p.n_seg] = acc;
       }
@@ -239,24 +280,29 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       prefetch_tmap(&tmB);
     }
   } else if (warp == 1) {
-    tmem_alloc(&tail->tmem_base, kTmemCols);
+    if (PAIR) tmem_alloc_pair(&tail->tmem_base, kTmemCols);
+    else tmem_alloc(&tail->tmem_base, kTmemCols);
   }
   tc_fence_before();
-  __syncthreads();
+  // a pair: both CTAs' barriers exist before either signals the other's
+  if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
 
   const int total = WGRAD ? p.n_seg * p.n_tiles_m * p.n_tiles_n
                           : tail->mt_off[p.n_seg] * p.n_tiles_n;
   const uint32_t tbase = tail->tmem_base;
   volatile int* abort_flag = &tail->abort_flag;
+  // the even CTA's full and accumulator-empty barriers, as cluster addresses
+  const uint32_t full_lead = PAIR ? smem_addr_in_rank(&tail->full[0], 0) : 0u;
+  const uint32_t tempty_lead = PAIR ? smem_addr_in_rank(&tail->tempty[0], 0) : 0u;
 
   if (warp == 0) {
     // ---- TMA producer ------------------------------------------------------
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+    for (int tau = unit0; tau < total && ok; tau += n_units) {
+      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
       const int n0 = ti.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -264,27 +310,52 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint8_t* sb = sa + kATileBytes;
         uint64_t* bar = &tail->full[stage];
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar, kTmaBytes);
           // K row of an MN-major operand: weight rows (dgrad) or EPD rows (wgrad)
           const int krow = WGRAD ? ti.k0 + kb * BK : static_cast<int>(ti.grp * p.b_group_rows) + kb * BK;
-          if (AM == OP_TMA_K) {
-            tma_load_2d(sa, &tmA, kb * BK, ti.m0, bar);
-          } else if (AM == OP_TMA_MN) {
-            for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, bar);
-          }
-          if (BMODE == OP_TMA_K) {
-            const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0;
-            if (EPI == EPI_SWIGLU) {
-              tma_load_2d(sb, &tmB, kb * BK, brow, bar);
-              tma_load_2d(sb + kBTileBytes / 2, &tmB, kb * BK, brow + p.half_n, bar);
+          if (PAIR) {
+            // this CTA's A rows and its half of the B tile (SwiGLU: the gate rows
+            // in the even CTA, the up rows in the odd one), all counted on the
+            // even CTA's barrier
+            if (leader) mbar_arrive_expect_tx(bar, kTmaBytes);
+            const uint32_t lbar = full_lead + stage * 8;
+            if (AM == OP_TMA_K) tma_load_2d_pair(sa, &tmA, kb * BK, ti.m0, lbar);
+            if (BMODE == OP_TMA_K) {
+              const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0 +
+                               rank * (EPI == EPI_SWIGLU ? p.half_n : BN / 2);
+              tma_load_2d_pair(sb, &tmB, kb * BK, brow, lbar);
             } else {
-              tma_load_2d(sb, &tmB, kb * BK, brow, bar);
+              for (int a = 0; a < 2; ++a)
+                tma_load_2d_pair(sb + a * kMnAtomBytes, &tmB, n0 + rank * (BN / 2) + 64 * a, krow, lbar);
             }
-          } else if (BMODE == OP_TMA_MN) {
-            for (int a = 0; a < BN / 64; ++a) tma_load_2d(sb + a * kMnAtomBytes, &tmB, n0 + 64 * a, krow, bar);
+          } else {
+            mbar_arrive_expect_tx(bar, kTmaBytes);
+            if (AM == OP_TMA_K) {
+              tma_load_2d(sa, &tmA, kb * BK, ti.m0, bar);
+            } else if (AM == OP_TMA_MN) {
+              for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, bar);
+            }
+            if (BMODE == OP_TMA_K) {
+              const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0;
+              if (EPI == EPI_SWIGLU) {
+                tma_load_2d(sb, &tmB, kb * BK, brow, bar);
+                tma_load_2d(sb + kBTileBytes / 2, &tmB, kb * BK, brow + p.half_n, bar);
+              } else {
+                tma_load_2d(sb, &tmB, kb * BK, brow, bar);
+              }
+            } else if (BMODE == OP_TMA_MN) {
+              for (int a = 0; a < BN / 64; ++a) tma_load_2d(sb + a * kMnAtomBytes, &tmB, n0 + 64 * a, krow, bar);
+            }
           }
         }
         __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (PAIR && ok) {
+      // the even CTA's commits release this CTA's stages: wait for the release of
+      // every stage, so that none lands after the CTA has exited
+      for (int i = 0; i < kStages && ok; ++i) {
+        if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) ok = false;
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -293,21 +364,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       *abort_flag = 1;
     }
   } else if (warp == 1) {
-    // ---- MMA issuer --------------------------------------------------------
-    if (lane == 0) {
+    if (lane == 0 && leader) {
+      // ---- MMA issuer --------------------------------------------------------
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x, ++it) {
-        const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+      for (int tau = unit0; tau < total && ok; tau += n_units, ++it) {
+        const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
-        if (!mbar_wait(&tail->tempty[a], aph ^ 1u, abort_flag)) { ok = false; break; }
+        if (!(PAIR ? mbar_wait_cluster(&tail->tempty[a], aph ^ 1u, abort_flag)
+                   : mbar_wait(&tail->tempty[a], aph ^ 1u, abort_flag))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tbase + a * BN;
         for (int kb = 0; kb < ti.kb; ++kb) {
-          if (!mbar_wait(&tail->full[stage], phase, abort_flag)) { ok = false; break; }
+          if (!(PAIR ? mbar_wait_cluster(&tail->full[stage], phase, abort_flag)
+                     : mbar_wait(&tail->full[stage], phase, abort_flag))) { ok = false; break; }
           // cp.async data arrived through the generic proxy: make it visible to
           // the tensor cores' (async proxy) operand reads
           if (kGather) fence_proxy_async_smem();
@@ -316,14 +389,22 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sb = sa + kATileBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            tc_mma_f16(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
-                       kIdesc, (kb | kk) != 0);
+            if (PAIR)
+              tc_mma_f16_pair(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
+                              kIdesc, (kb | kk) != 0);
+            else
+              tc_mma_f16(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
+                         kIdesc, (kb | kk) != 0);
           }
-          tc_commit(&tail->empty[stage]);
+          if (PAIR) tc_commit_pair(&tail->empty[stage], 0x3);
+          else tc_commit(&tail->empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         // with no k block the commit arrives at once and the epilogue writes zeros
-        if (ok) tc_commit(&tail->tfull[a]);
+        if (ok) {
+          if (PAIR) tc_commit_pair(&tail->tfull[a], 0x3);
+          else tc_commit(&tail->tfull[a]);
+        }
       }
       if (!ok) {
         latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
@@ -338,8 +419,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int row = quarter * 32 + lane;
     int it = 0;
     bool ok = true;
-    for (int tau = blockIdx.x; tau < total; tau += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+    for (int tau = unit0; tau < total; tau += n_units, ++it) {
+      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
       const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tail->tfull[a], aph, abort_flag)) { ok = false; break; }
@@ -464,7 +545,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tail->tempty[a]);
+      if (lane == 0) {
+        // the accumulator may be overwritten: tell the CTA that issues the MMAs
+        if (PAIR && !leader) mbar_arrive_cluster(tempty_lead + a * 8);
+        else mbar_arrive(&tail->tempty[a]);
+      }
     }
     if (!ok) {
       if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
@@ -481,8 +566,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tau = blockIdx.x; tau < total && ok; tau += gridDim.x) {
-      const TileInfo ti = decode_tile<WGRAD>(tau, p, tail->mt_off);
+    for (int tau = unit0; tau < total && ok; tau += n_units) {
+      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
       // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
       // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
       // at r*128 + ((c ^ (r % 8)) * 16)
@@ -552,9 +637,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   }
 
   tc_fence_before();
-  __syncthreads();
+  // a pair: neither CTA exits (or frees its TMEM) while the other may still
+  // signal it or run MMAs into it
+  if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+  if (warp == 1) {
+    if (PAIR) tmem_dealloc_pair(tbase, kTmemCols);
+    else tmem_dealloc(tbase, kTmemCols);
+  }
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -598,17 +688,34 @@ int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t
   return make_map(m, ptr, rows, cols, BK, BK);
 }
 
-template <int AM, int BMODE, int EPI, bool WGRAD>
+template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
 int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb, const Params& p) {
-  auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD>;
+  auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR>;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(threads_for(AM, BMODE));
+  cfg.dynamicSmemBytes = smem_bytes(PAIR);
+  cfg.stream = ctx.stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  // persistent grid: one CTA per SM, or as many co-resident CTA pairs as fit
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int n_pairs = 0;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(PAIR));
+    if (PAIR && attr_err == cudaSuccess) {
+      cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
+      attr_err = cudaOccupancyMaxActiveClusters(&n_pairs, kern, &cfg);
+    }
   });
-  if (attr_err != cudaSuccess) return OCCULT_ERR_CUDA;
-  kern<<<ctx.num_sms, threads_for(AM, BMODE), kSmemBytes, ctx.stream>>>(ma, mb, p);
-  return cuda_status(cudaGetLastError());
+  if (attr_err != cudaSuccess || (PAIR && n_pairs < 1)) return OCCULT_ERR_CUDA;
+  cfg.gridDim = dim3(PAIR ? 2 * n_pairs : ctx.num_sms);
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, p));
 }
 
 }  // namespace
@@ -617,10 +724,17 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
   if (!g.wgrad && g.K % BK != 0) return OCCULT_ERR_UNSUPPORTED;
   if (g.n_seg == 0 || (!g.wgrad && g.max_rows == 0)) return OCCULT_OK;
+  // Forward and dgrad GEMMs whose A is a plain matrix run on CTA pairs (one
+  // 256 x 256 tile per pair, each CTA holding 128 rows of B).  Gathered A rows
+  // stay on single CTAs: with cp.async producers beside them the pair's MMAs
+  // measured 2x slower, and TMA tile::gather4 (one instruction per four 128-byte
+  // rows) 2.6x slower than cp.async.
+  const int am = g.a_mode;
+  const bool pair = !g.wgrad && !op_gathered(am);
   CUtensorMap ma, mb;
-  int rc = operand_map(&ma, g.a_mode, g.A, g.a_rows, g.a_cols, BM);
+  int rc = operand_map(&ma, am, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
-  rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols, g.epi == EPI_SWIGLU ? BN / 2 : BN);
+  rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols, (pair || g.epi == EPI_SWIGLU) ? BN / 2 : BN);
   if (rc) return rc;
   Params p{};
   p.seg_off = g.seg_off;
@@ -647,24 +761,24 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.gu_in = static_cast<const __nv_bfloat16*>(g.gu_in);
   p.dg_part = g.dg_part;
   p.dev_err = ctx.dev_err;
-  const int am = g.a_mode, bm = g.b_mode, ep = g.epi;
+  const int bm = g.b_mode, ep = g.epi;
   // the instantiations the layer uses
   if (!g.wgrad) {
     if (am == OP_GATHER_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
-      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false>(ctx, ma, mb, p);
+      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false, false>(ctx, ma, mb, p);
     if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_SWIGLU, false>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_SWIGLU, false, true>(ctx, ma, mb, p);
     if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_F32)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false, true>(ctx, ma, mb, p);
     if (am == OP_GATHER_K && bm == OP_TMA_MN && ep == EPI_SWIGLU_BWD)
-      return launch_tc<OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD, false>(ctx, ma, mb, p);
+      return launch_tc<OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD, false, false>(ctx, ma, mb, p);
     if (am == OP_TMA_K && bm == OP_TMA_MN && ep == EPI_F32)
-      return launch_tc<OP_TMA_K, OP_TMA_MN, EPI_F32, false>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_K, OP_TMA_MN, EPI_F32, false, true>(ctx, ma, mb, p);
   } else if (ep == EPI_F32) {
     if (am == OP_GATHER_MN && bm == OP_TMA_MN)
-      return launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true>(ctx, ma, mb, p);
+      return launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, p);
     if (am == OP_TMA_MN && bm == OP_GATHER_MN)
-      return launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, p);
   }
   return OCCULT_ERR_UNSUPPORTED;
 }
