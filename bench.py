@@ -155,14 +155,14 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def recorded_traffic(kernel: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
-    e = j.get(kernel)
+    e = j.get(workload, {}).get(kernel)
     if not e:
         return None
     src = os.path.join(ROOT, "combine_top_route_gb300", "csrc", e["source"])
@@ -383,42 +383,56 @@ def run_ours(args, cfg, world, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
 
     hbm, tflops, peak_src = peaks()
-    flops_up = 4.0 * d * I * T * k
-    flops_down = 2.0 * d * I * T * k
-    b = 2  # bytes per bf16 element (x, x_sfd); y_epd and y are fp32
-    kernels = {c: {"ms": per_call[c]} for c in names}
-    kernels.update({
-        "route": {"ms": per_call["route"]},
-        "build_brim": {"ms": per_call["build_brim"]},
-        "dispatch": {"ms": per_call["dispatch"],
-                     "GB/s": (T * d * b + n_sfd * d * b) / per_call["dispatch"] / 1e6},
-        "expert_up": {"ms": per_call["expert_up"],
-                      "TFLOP/s": flops_up / per_call["expert_up"] / 1e9},
-        "expert_down": {"ms": per_call["expert_down"],
-                        "TFLOP/s": flops_down / per_call["expert_down"] / 1e9},
-        "combine": {"ms": per_call["combine"],
-                    "GB/s": (T * k * d * 4 + T * d * 4) / per_call["combine"] / 1e6},
-    })
-    gemms = ["expert_up", "expert_down"]
+    b = 2  # bytes per bf16 element (x, x_sfd, weights, h); y_epd, y_shared and y are fp32
+    n_epd = T * k
+    S = cfg.n_shared * cfg.shared_inter
+    # algorithmic work per launch: FLOPs and the bytes that must cross HBM once
+    work = {
+        "expert_up": (4.0 * d * I * n_epd,
+                      cfg.n_experts * 2 * I * d * b + n_sfd * d * b + n_epd * I * b),
+        "expert_down": (2.0 * d * I * n_epd,
+                        cfg.n_experts * I * d * b + n_epd * I * b + n_epd * d * 4),
+    }
+    if S:
+        work["shared_ffn"] = (6.0 * d * S * T, 3 * S * d * b + T * d * b + T * S * b + T * d * 4)
     if train:
-        # dgrad through W_d and W1, wgrad of W_d and W1: twice the forward FLOPs
-        kernels["expert_bwd"]["TFLOP/s"] = 2 * (flops_up + flops_down) / per_call["expert_bwd"] / 1e9
-        gemms.append("expert_bwd")
-    dom = max(gemms, key=lambda c: per_call[c])
-    achieved = kernels[dom]["TFLOP/s"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": tflops,
-                "unit": "TFLOP/s", "frac": achieved / tflops, "traffic": recorded_traffic(dom),
-                "peak_source": f"{peak_src} bf16 dense burst"}
+        # dgrad through W_d and [W_g; W_u], wgrad of both: twice the forward FLOPs.
+        # Bytes: dy_sfd (twice) and x_sfd gathered rows, the weights read and their
+        # fp32 gradients written, G|U read, dG|dU written and read twice, h read,
+        # fp32 dx_epd written
+        work["expert_bwd"] = (2 * 6.0 * d * I * n_epd,
+                              3 * n_sfd * d * b + 3 * cfg.n_experts * I * d * (b + 4)
+                              + 9 * n_epd * I * b + n_epd * d * 4)
+    ridge = tflops * 1e12 / (hbm * 1e9)  # flop per byte where the two roofs meet
+    kernels = {c: {"ms": per_call[c]} for c in names}
+    kernels["dispatch"].update({"GB/s": (T * d * b + n_sfd * d * b) / per_call["dispatch"] / 1e6})
+    kernels["combine"].update({"GB/s": (n_epd * d * 4 + T * d * 4 + (T * d * 4 if S else 0))
+                                       / per_call["combine"] / 1e6})
+    for c, (fl, by) in work.items():
+        kernels[c].update({"TFLOP/s": fl / per_call[c] / 1e9, "GB/s": by / per_call[c] / 1e6,
+                           "bound": "tensor" if fl / by > ridge else "hbm"})
+    dom = max(work, key=lambda c: per_call[c])
+    if kernels[dom]["bound"] == "tensor":
+        achieved, peak, unit = kernels[dom]["TFLOP/s"], tflops, "TFLOP/s"
+        src = f"{peak_src} bf16 dense burst"
+    else:
+        achieved, peak, unit = kernels[dom]["GB/s"], hbm, "GB/s"
+        src = f"{peak_src} HBM copy bandwidth"
+    roofline = {"bound": kernels[dom]["bound"], "kernel": dom, "achieved": achieved,
+                "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": recorded_traffic(cfg.name, dom), "peak_source": src}
     for c in ("dispatch", "combine"):
         kernels[c]["hbm_frac"] = kernels[c]["GB/s"] / hbm
 
+    w_bytes = (3 * cfg.n_experts * I + 3 * S) * d * b
     result = {
         "metric": METRIC, "value": world * T / (ms_step / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg),
-                   "l2": "inputs larger than L2 (805 MB of expert weights read every step)",
+                   "l2": f"inputs larger than L2 ({w_bytes / 1e6:.0f} MB of expert weights read "
+                         "every step)",
                    "parallelism": f"{world} independent replica(s), Nd={cfg.n_vdev} virtual "
                                   "expert-parallel devices each"},
         "roofline": roofline,

@@ -91,6 +91,13 @@ CONFIGS: Dict[str, LayerConfig] = {
                                    inter=1408, n_vdev=8, dtype="bf16", n_clusters=16,
                                    experts_per_cluster=10, prof_tokens=16384, n_shared=2,
                                    shared_inter=1408),
+    # the same decode layer with device-limited routing: the 2 virtual devices of
+    # largest gate mass, renormalised top-k among their experts
+    "deepseek_decode_limited": LayerConfig("deepseek_decode_limited", T=512, d=2048,
+                                           n_experts=64, top_k=6, inter=1408, n_vdev=8,
+                                           dtype="bf16", n_clusters=16, experts_per_cluster=10,
+                                           prof_tokens=16384, n_shared=2, shared_inter=1408,
+                                           route_mode="device_limited", renorm=True),
     # OLMoE-shaped training step (forward + backward)
     "olmoe_train": LayerConfig("olmoe_train", T=32768, d=2048, n_experts=64, top_k=8,
                                inter=1024, n_vdev=16, dtype="bf16", n_clusters=16,

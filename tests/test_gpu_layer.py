@@ -23,9 +23,7 @@ pytestmark = pytest.mark.gpu
 GATE_RTOL = 2e-6
 
 CFG = dict(synth.CONFIGS)
-CFG["deepseek_limited"] = CFG["deepseek_decode"].with_(name="deepseek_limited",
-                                                       route_mode="device_limited", renorm=True)
-ALL = ["tiny_f32", "olmoe_fwd", "qwen_prefill", "deepseek_decode", "deepseek_limited",
+ALL = ["tiny_f32", "olmoe_fwd", "qwen_prefill", "deepseek_decode", "deepseek_decode_limited",
        "olmoe_train"]
 # shapes that exercise edges: ragged T, one token, one device, one expert per
 # device, k = 1, k = Nd
