@@ -9,14 +9,17 @@ and an upstream gradient dy_t:
     dh       = g W_d[e]^T dy_t               dG = dh * U * silu'(G),  dU = dh * s
     dW_g[e] += dG x_t^T,  dW_u[e] += dU x_t^T
     dx_t    += W_g[e]^T dG + W_u[e]^T dU
-with silu'(G) = sigma(G) (1 + G (1 - sigma(G))).  The router logits are an input
-here, so no gradient flows into them.
+with silu'(G) = sigma(G) (1 + G (1 - sigma(G))).  moe_backward takes the gates as
+given; router_grad carries dgates on into the router logits through the softmax
+of Eq. 2.
 """
 from __future__ import annotations
 
 from typing import Dict, Optional, Sequence
 
 import numpy as np
+
+from .routing import softmax
 
 
 def _sigmoid(z: np.ndarray) -> np.ndarray:
@@ -67,3 +70,37 @@ def moe_backward(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, w1: np.ndarr
         dw1[e, :I] = dG.T @ a
         dw1[e, I:] = dU.T @ a
     return {"dx": dx, "dw1": dw1, "dw2": dw2, "dgates": dgates}
+
+
+def router_grad(logits: np.ndarray, gate_ids: np.ndarray, dgates: np.ndarray,
+                renorm: bool = False) -> np.ndarray:
+    """Gradient of sum_tj dgates_tj * g_tj with respect to the router logits z.
+
+    The gates are g_tj = p_t[gate_ids_tj] with p_t = softmax(z_t) (Eq. 2), divided
+    by their sum over j when ``renorm``.  The selection of experts is piecewise
+    constant in z, so no gradient flows through it.  With q_j = p[e_j] and
+    S = sum_j q_j:
+        plain:   dz_i = p_i * (sum_j [e_j = i] dg_j - sum_j dg_j g_j)
+        renorm:  dz_i = sum_j [e_j = i] g_j * (dg_j - sum_m dg_m g_m),
+    (in the renormalised case the logits of unselected experts get no gradient).
+    Returns dz fp64 [T, Ne].
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    ids = np.asarray(gate_ids)
+    dg = np.asarray(dgates, dtype=np.float64)
+    p = softmax(z)
+    T, Ne = z.shape
+    dz = np.zeros((T, Ne))
+    for t in range(T):
+        q = p[t, ids[t]]
+        g = q / q.sum() if renorm else q
+        inner = float(np.dot(dg[t], g))
+        if renorm:
+            for j, e in enumerate(ids[t]):
+                dz[t, e] += g[j] * (dg[t, j] - inner)
+        else:
+            sel = np.zeros(Ne)
+            for j, e in enumerate(ids[t]):
+                sel[e] += dg[t, j]
+            dz[t] = p[t] * (sel - inner)
+    return dz

@@ -17,6 +17,25 @@ devices): the devices kept for a token are the ``n_keep`` devices with the
 largest summed softmax probability over all of their experts (equal masses go
 to the lower device id); top-k is then taken among the experts of the kept
 devices, and the gates are renormalised over the k chosen experts.
+
+Collaboration pruning as Sec. 3.3 itself states it: the kept devices are found
+by walking the token's k routed experts in descending routing score and
+collecting their devices until ``n_keep`` are reached (all of them when the k
+experts cover fewer).  Then either
+* routing-score-based pruning: all Ne scores are sorted in descending order and
+  the top k experts lying on the kept devices are selected, or
+* expert-similarity-based pruning: the k routed experts are walked in
+  descending score; an expert on a kept device stays, one outside is replaced
+  by the most similar expert of the table T (App. A.3) that lies on a kept
+  device and is not selected yet.
+Readings where Sec. 3.3 is silent: scores are compared on the fp32 logits with
+ties to the lower id, as for top-k; the gates of score-based pruning are the
+softmax probabilities of the selected experts (renormalised over them when
+``renorm``); in similarity-based pruning the experts kept in place are counted
+as selected before any replacement is made, a replacement takes over the
+replaced slot and its routing weight, similarities are compared as fp32 with
+ties to the lower id, and the slots keep the routed experts' descending-score
+order.
 """
 from __future__ import annotations
 
@@ -116,3 +135,89 @@ def token_devices(ids: np.ndarray, expert_to_vdev: np.ndarray, n_vdev: int) -> n
         for e in ids[t]:
             act[t, e2v[e]] = True
     return act
+
+
+def _check_pruning(expert_to_vdev, k: int, n_keep: int) -> None:
+    """Every expert set inside n_keep devices must be able to hold k experts."""
+    counts = np.bincount(np.asarray(expert_to_vdev))
+    if n_keep < 1 or np.sort(counts)[:n_keep].sum() < k:
+        raise ValueError("pruning needs n_keep devices that hold at least k experts")
+
+
+def pruning_devices(ids: np.ndarray, expert_to_vdev: np.ndarray, n_keep: int) -> list:
+    """Sec. 3.3: per token, the devices of its routed experts (``ids`` in descending
+    score) in order of first appearance, stopping once ``n_keep`` are collected."""
+    e2v = np.asarray(expert_to_vdev)
+    out = []
+    for row in np.asarray(ids):
+        kept = []
+        for e in row:
+            d = int(e2v[int(e)])
+            if d not in kept:
+                if len(kept) == n_keep:
+                    break
+                kept.append(d)
+        out.append(kept)
+    return out
+
+
+def route_score_pruned(logits: np.ndarray, k: int, expert_to_vdev: np.ndarray, n_keep: int,
+                       renorm: bool = False):
+    """Routing-score-based pruning (Sec. 3.3, steps 1-2).
+
+    Returns ``ids`` int32 [T, k] (descending logit), ``gates`` fp64 [T, k] and the
+    kept devices of every token (a list of lists, order of first appearance).
+    """
+    _check_pruning(expert_to_vdev, k, n_keep)
+    logits = np.asarray(logits, dtype=np.float32)
+    e2v = np.asarray(expert_to_vdev)
+    T = logits.shape[0]
+    routed, _ = route_topk(logits, k)
+    kept = pruning_devices(routed, e2v, n_keep)
+    p = softmax(logits)
+    ranked = _rank_by_logit(logits)          # step 1: all scores, descending
+    ids = np.empty((T, k), dtype=np.int32)
+    gates = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        allowed = set(kept[t])
+        chosen = [int(e) for e in ranked[t] if int(e2v[e]) in allowed][:k]   # step 2
+        ids[t] = chosen
+        g = p[t, chosen]
+        gates[t] = g / g.sum() if renorm else g
+    return ids, gates, kept
+
+
+def route_similarity_pruned(logits: np.ndarray, k: int, expert_to_vdev: np.ndarray,
+                            n_keep: int, table: np.ndarray, renorm: bool = False):
+    """Expert-similarity-based pruning (Sec. 3.3) with similarity table ``table``
+    [Ne, Ne] (row e: similarity of expert e to every expert).
+
+    Returns ``ids`` int32 [T, k] (slot j holds routed expert j or its
+    replacement), ``gates`` fp64 [T, k] (the routed experts' weights, top-k
+    softmax probabilities renormalised when ``renorm``), ``routed`` int32 [T, k]
+    (the experts whose probabilities the gates are) and the kept devices.
+    """
+    _check_pruning(expert_to_vdev, k, n_keep)
+    logits = np.asarray(logits, dtype=np.float32)
+    e2v = np.asarray(expert_to_vdev)
+    tab = np.asarray(table, dtype=np.float32)
+    T, Ne = logits.shape
+    routed, gates = route_topk(logits, k, renorm=renorm)
+    kept = pruning_devices(routed, e2v, n_keep)
+    ids = routed.copy()
+    for t in range(T):
+        allowed = set(kept[t])
+        selected = set(int(e) for e in routed[t] if int(e2v[e]) in allowed)
+        for j, e in enumerate(routed[t]):
+            e = int(e)
+            if int(e2v[e]) in allowed:
+                continue
+            best = None
+            for c in range(Ne):                  # ascending id: ties keep the lower id
+                if int(e2v[c]) not in allowed or c in selected:
+                    continue
+                if best is None or tab[e, c] > tab[e, best]:
+                    best = c
+            selected.add(best)
+            ids[t, j] = best
+    return ids, gates, routed, kept

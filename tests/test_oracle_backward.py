@@ -88,3 +88,68 @@ def test_expert_subsets_add_up_to_the_full_gradient():
     assert not a["dw1"][1].any() and not a["dw2"][3].any()
     np.testing.assert_allclose(a["dx"] + b["dx"], full["dx"], rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(a["dgates"] + b["dgates"], full["dgates"], rtol=1e-13, atol=1e-14)
+
+
+# ---- router gradient (d-logits through the softmax of Eq. 2) -------------------
+
+_routing = routing
+
+
+def _router_case(seed, T=20, Ne=10, k=3):
+    rng = np.random.default_rng(seed)
+    z = rng.standard_normal((T, Ne))
+    ids, _ = _routing.route_topk(z.astype(np.float32), k)
+    dg = rng.standard_normal((T, k))
+    return z, ids, dg
+
+
+@pytest.mark.parametrize("renorm", [False, True])
+def test_router_grad_finite_differences(renorm):
+    z, ids, dg = _router_case(0)
+    dz = backward.router_grad(z, ids, dg, renorm=renorm)
+
+    def loss(zz):
+        p = np.exp(zz - zz.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        g = np.take_along_axis(p, ids.astype(int), 1)
+        if renorm:
+            g = g / g.sum(1, keepdims=True)
+        return float((dg * g).sum())
+
+    h = 1e-6
+    num = np.zeros_like(z)
+    for t in range(z.shape[0]):
+        for i in range(z.shape[1]):
+            zp, zm = z.copy(), z.copy()
+            zp[t, i] += h
+            zm[t, i] -= h
+            num[t, i] = (loss(zp) - loss(zm)) / (2 * h)
+    np.testing.assert_allclose(dz, num, rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("renorm", [False, True])
+def test_router_grad_matches_autograd(renorm):
+    z, ids, dg = _router_case(1, T=64, Ne=16, k=4)
+    zt = torch.tensor(z, dtype=torch.float64, requires_grad=True)
+    g = torch.softmax(zt, dim=1).gather(1, torch.tensor(ids, dtype=torch.int64))
+    if renorm:
+        g = g / g.sum(1, keepdim=True)
+    (g * torch.tensor(dg)).sum().backward()
+    np.testing.assert_allclose(backward.router_grad(z, ids, dg, renorm=renorm),
+                               zt.grad.numpy(), rtol=1e-11, atol=1e-14)
+
+
+def test_router_grad_special_cases():
+    z, ids, dg = _router_case(2, k=1)
+    # one renormalised gate is the constant 1: no gradient
+    assert not backward.router_grad(z, ids, dg, renorm=True).any()
+    # all experts chosen: renormalisation changes nothing
+    z, ids, dg = _router_case(3, Ne=6, k=6)
+    np.testing.assert_allclose(backward.router_grad(z, ids, dg, renorm=True),
+                               backward.router_grad(z, ids, dg, renorm=False), rtol=1e-12,
+                               atol=1e-15)
+    # the gradient of a softmax sums to zero over the logits of a token
+    z, ids, dg = _router_case(4)
+    for r in (False, True):
+        np.testing.assert_allclose(backward.router_grad(z, ids, dg, renorm=r).sum(1), 0.0,
+                                   atol=1e-14)
