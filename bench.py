@@ -267,15 +267,30 @@ def run_ours(args, cfg, world, rank, local):
     x = synth.hidden_states(cfg, device=dev)
     w = synth.expert_weights(cfg, device=dev)
     train = bool(cfg.backward)
-    moe = occ.OccultMoE(ds, w, L, device=dev, train=train)
+    table = None
+    if cfg.route_mode == "similarity_pruned":
+        # the similarity table of App. A.3 from the profiling batch (Eq. 8), built
+        # by the library; not part of the timed step
+        G = torch.zeros(cfg.n_experts, cfg.n_experts, dtype=torch.float64, device=dev)
+        H = synth.profiling_logits(cfg).to(dev)
+        occ.occult_similarity_accumulate(ds, H, H.shape[0], G)
+        table = torch.empty(cfg.n_experts, cfg.n_experts, dtype=torch.float32, device=dev)
+        occ.occult_similarity_finish(ds, G, table)
+    moe = occ.OccultMoE(ds, w, L, device=dev, train=train, sim_table=table)
     dy = synth.upstream_grad(cfg, device=dev) if train else None
     stream = torch.cuda.current_stream(dev)
     T, k, d, I = cfg.T, cfg.top_k, cfg.d, cfg.inter
 
     # one step as named C-ABI calls, in Algorithm 2's order (+ the backward)
+    if cfg.route_mode == "similarity_pruned":
+        route = lambda: occ.occult_route_similarity(  # noqa: E731
+            ds, logits, moe.expert_to_vdev, moe.sim_table, moe.ids, moe.gates, moe.vmask,
+            moe.routed, stream)
+    else:
+        route = lambda: occ.occult_route(ds, logits, moe.expert_to_vdev, moe.ids,  # noqa: E731
+                                         moe.gates, moe.vmask, stream)
     calls = [
-        ("route", lambda: occ.occult_route(ds, logits, moe.expert_to_vdev, moe.ids, moe.gates,
-                                           moe.vmask, stream)),
+        ("route", route),
         ("build_brim", lambda: occ.occult_build_brim(
             ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0, moe.seg_off, moe.brim1,
             moe.exp_off, moe.epd_src, moe.epd_gate, moe.counts, moe.brim_ws, stream)),
@@ -308,6 +323,8 @@ def run_ours(args, cfg, world, rank, local):
             ("gate_grad", lambda: occ.occult_gate_grad(ds, moe.ids, moe.placement, moe.brim0,
                                                        moe.seg_off, moe.brim1, moe.exp_off,
                                                        moe.dg_epd, moe.dgates, stream)),
+            ("router_grad", lambda: occ.occult_router_grad(ds, logits, moe.routed, moe.dgates,
+                                                           moe.dlogits, stream)),
         ]
     names = [c[0] for c in calls]
 

@@ -22,6 +22,8 @@ OCCULT_F32 = 0
 OCCULT_BF16 = 1
 ROUTE_EXACT = 0
 ROUTE_DEVICE_LIMITED = 1
+ROUTE_SCORE_PRUNED = 2
+ROUTE_SIMILARITY_PRUNED = 3
 MAX_EXPERTS = 256
 MAX_VDEV = 32
 MAX_TOPK = 16
@@ -73,6 +75,10 @@ _SIGNATURES = {
     "occult_device_error": (ctypes.c_int, [ctypes.POINTER(_I32)]),
     "occult_place": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP]),
     "occult_route": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_route_similarity": (ctypes.c_int, [_D] + [_VP] * 8),
+    "occult_similarity_accumulate": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP]),
+    "occult_similarity_finish": (ctypes.c_int, [_D, _VP, _VP, _VP]),
+    "occult_router_grad": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP]),
     "occult_build_brim": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP, _VP, ctypes.c_size_t, _VP]),
     "occult_build_brim_noalloc": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -178,6 +184,39 @@ def occult_route(desc, logits, expert_to_vdev, ids, gates, vmask, stream=None):
           _dev(expert_to_vdev, torch.int32, Ne, "expert_to_vdev"),
           _dev(ids, torch.int32, T * k, "ids"), _dev(gates, torch.float32, T * k, "gates"),
           _dev(vmask, torch.int32, T, "vmask"), _stream(stream))
+
+
+def occult_route_similarity(desc, logits, expert_to_vdev, table, ids, gates, vmask, routed=None,
+                            stream=None):
+    T, Ne, k = desc.T, desc.n_experts, desc.top_k
+    _call("occult_route_similarity", ctypes.byref(desc),
+          _dev(logits, torch.float32, T * Ne, "logits"),
+          _dev(expert_to_vdev, torch.int32, Ne, "expert_to_vdev"),
+          _dev(table, torch.float32, Ne * Ne, "table"),
+          _dev(ids, torch.int32, T * k, "ids"), _dev(gates, torch.float32, T * k, "gates"),
+          _dev(routed, torch.int32, T * k, "routed", nullable=True),
+          _dev(vmask, torch.int32, T, "vmask"), _stream(stream))
+
+
+def occult_similarity_accumulate(desc, logits, n_tok, G, stream=None):
+    Ne = desc.n_experts
+    _call("occult_similarity_accumulate", ctypes.byref(desc),
+          _dev(logits, torch.float32, n_tok * Ne, "logits", nullable=n_tok == 0), n_tok,
+          _dev(G, torch.float64, Ne * Ne, "G"), _stream(stream))
+
+
+def occult_similarity_finish(desc, G, table, stream=None):
+    Ne = desc.n_experts
+    _call("occult_similarity_finish", ctypes.byref(desc), _dev(G, torch.float64, Ne * Ne, "G"),
+          _dev(table, torch.float32, Ne * Ne, "table"), _stream(stream))
+
+
+def occult_router_grad(desc, logits, gate_ids, dgates, dlogits, stream=None):
+    T, Ne, k = desc.T, desc.n_experts, desc.top_k
+    _call("occult_router_grad", ctypes.byref(desc), _dev(logits, torch.float32, T * Ne, "logits"),
+          _dev(gate_ids, torch.int32, T * k, "gate_ids"),
+          _dev(dgates, torch.float32, T * k, "dgates"),
+          _dev(dlogits, torch.float32, T * Ne, "dlogits"), _stream(stream))
 
 
 def occult_build_brim(desc, ids, gates, vmask, placement, brim0, seg_off, brim1, exp_off,

@@ -70,13 +70,13 @@ int check(const occult_desc_t* ds) {
   if (ds->n_experts % ds->n_vdev != 0) return OCCULT_ERR_INVALID_ARG;
   if (ds->top_k > ds->n_experts) return OCCULT_ERR_INVALID_ARG;
   if (ds->dtype != OCCULT_F32 && ds->dtype != OCCULT_BF16) return OCCULT_ERR_INVALID_ARG;
-  if (ds->route_mode != OCCULT_ROUTE_EXACT && ds->route_mode != OCCULT_ROUTE_DEVICE_LIMITED)
+  if (ds->route_mode < OCCULT_ROUTE_EXACT || ds->route_mode > OCCULT_ROUTE_SIMILARITY_PRUNED)
     return OCCULT_ERR_INVALID_ARG;
   if (ds->n_experts > OCCULT_MAX_EXPERTS || ds->n_vdev > OCCULT_MAX_VDEV ||
       ds->top_k > OCCULT_MAX_TOPK)
     return OCCULT_ERR_UNSUPPORTED;
   const int n_loc = ds->n_experts / ds->n_vdev;
-  if (ds->route_mode == OCCULT_ROUTE_DEVICE_LIMITED) {
+  if (ds->route_mode != OCCULT_ROUTE_EXACT) {
     if (ds->limit_devices < 1 || ds->limit_devices > ds->n_vdev) return OCCULT_ERR_INVALID_ARG;
     if (ds->limit_devices * n_loc < ds->top_k) return OCCULT_ERR_INVALID_ARG;
   }
@@ -148,9 +148,50 @@ int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* 
                  int32_t* ids, float* gates, uint32_t* vmask, occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
+  OCCULT_REQUIRE(desc->route_mode != OCCULT_ROUTE_SIMILARITY_PRUNED);
   OCCULT_REQUIRE(desc->T == 0 || (logits && expert_to_vdev && ids && gates && vmask));
   OCCULT_CTX(stream);
-  return launch_route(ctx, *desc, logits, expert_to_vdev, ids, gates, vmask);
+  return launch_route(ctx, *desc, logits, expert_to_vdev, nullptr, ids, gates, nullptr, vmask);
+}
+
+int occult_route_similarity(const occult_desc_t* desc, const float* logits,
+                            const int32_t* expert_to_vdev, const float* table, int32_t* ids,
+                            float* gates, int32_t* routed, uint32_t* vmask,
+                            occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(desc->route_mode == OCCULT_ROUTE_SIMILARITY_PRUNED);
+  OCCULT_REQUIRE(desc->T == 0 || (logits && expert_to_vdev && table && ids && gates && vmask));
+  OCCULT_CTX(stream);
+  return launch_route(ctx, *desc, logits, expert_to_vdev, table, ids, gates, routed, vmask);
+}
+
+int occult_similarity_accumulate(const occult_desc_t* desc, const float* logits, int32_t n_tok,
+                                 double* G, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(n_tok >= 0 && G && (n_tok == 0 || logits));
+  OCCULT_REQUIRE(static_cast<int64_t>(n_tok) * desc->n_experts < (1ll << 31));
+  OCCULT_CTX(stream);
+  return launch_similarity_accumulate(ctx, desc->n_experts, logits, n_tok, G);
+}
+
+int occult_similarity_finish(const occult_desc_t* desc, const double* G, float* table,
+                             occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(G && table);
+  OCCULT_CTX(stream);
+  return launch_similarity_finish(ctx, desc->n_experts, G, table);
+}
+
+int occult_router_grad(const occult_desc_t* desc, const float* logits, const int32_t* gate_ids,
+                       const float* dgates, float* dlogits, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(desc->T == 0 || (logits && gate_ids && dgates && dlogits));
+  OCCULT_CTX(stream);
+  return launch_router_grad(ctx, *desc, logits, gate_ids, dgates, dlogits);
 }
 
 int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float* gates,

@@ -10,7 +10,10 @@
 namespace occult {
 
 int launch_route(const LaunchCtx& ctx, const occult_desc_t& ds, const float* logits,
-                 const int32_t* e2v, int32_t* ids, float* gates, uint32_t* vmask);
+                 const int32_t* e2v, const float* table, int32_t* ids, float* gates,
+                 int32_t* routed, uint32_t* vmask);
+int launch_router_grad(const LaunchCtx& ctx, const occult_desc_t& ds, const float* logits,
+                       const int32_t* gate_ids, const float* dgates, float* dlogits);
 
 int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids,
                       const float* gates, const uint32_t* vmask, const int32_t* placement,
@@ -24,6 +27,10 @@ int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x
 int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
                    const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y);
+
+int launch_similarity_accumulate(const LaunchCtx& ctx, int Ne, const float* logits, int n_tok,
+                                 double* G);
+int launch_similarity_finish(const LaunchCtx& ctx, int Ne, const double* G, float* table);
 
 size_t profile_ws_bytes(const occult_desc_t& ds, int n_tok);
 int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t* ids, int n_tok,

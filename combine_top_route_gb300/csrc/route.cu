@@ -1,6 +1,11 @@
 // Router kernel: Occult paper Sec. 2.1 Eq. 2 (top-k of the softmax of the
-// router logits) and the device-limited pruning mode of Sec. 3.3 (keep a few
-// devices, choose the top-k among their experts).
+// router logits) and the collaboration pruning of Sec. 3.3: the device-limited
+// mode (keep the devices of largest gate mass, top-k among their experts) and
+// the pages' own two rules, whose kept devices are those of the routed experts
+// in descending score -- routing-score-based pruning (top-k of all sorted
+// scores within them) and expert-similarity-based pruning (each routed expert
+// outside them replaced by its most similar free expert inside, table T of
+// App. A.3).
 //
 // One warp per token.  Lane l holds experts l, l+32, ... (up to 8 per lane for
 // 256 experts).  The softmax denominator is a fixed-order warp tree, so the
@@ -41,11 +46,58 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// One top-k pass over the experts whose device is in `allowed`: lane j < k
+// receives slot j's expert and probability (exp / Z), `vm` the devices used,
+// `gsum` the sum of the k probabilities.  With `walk`, the devices of the chosen
+// experts are also collected in slot order into `kept` until `n_keep` are found
+// (Sec. 3.3's device range).
+template <int PER_LANE>
+__device__ __forceinline__ void topk_pass(const float (&v)[PER_LANE], const float (&ex)[PER_LANE],
+                                          const int (&dev)[PER_LANE], int Ne, int k, float Z,
+                                          uint32_t allowed, bool walk, int n_keep, int& my_id,
+                                          float& my_g, uint32_t& vm, float& gsum,
+                                          uint32_t& kept) {
+  const int lane = threadIdx.x & 31;
+  const float NEG = -__int_as_float(0x7f800000);
+  bool taken[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i)
+    taken[i] = (lane + 32 * i >= Ne) || !((allowed >> (dev[i] & 31)) & 1u);
+  vm = 0;
+  gsum = 0.f;
+  int n_kept = 0;
+  for (int j = 0; j < k; ++j) {
+    Cand c{NEG, 0x7fffffff};
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i)
+      if (!taken[i] && before(v[i], lane + 32 * i, c.v, c.id)) { c.v = v[i]; c.id = lane + 32 * i; }
+    Cand b = warp_best(c);
+    const int owner = b.id & 31, slot = b.id >> 5;
+    float g = 0.f;
+    int d = 0;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i)
+      if (lane == owner && slot == i) { taken[i] = true; g = ex[i]; d = dev[i]; }
+    g = __shfl_sync(0xffffffffu, g, owner) / Z;
+    d = __shfl_sync(0xffffffffu, d, owner);
+    vm |= 1u << d;
+    gsum += g;
+    if (walk && !((kept >> d) & 1u) && n_kept < n_keep) {
+      kept |= 1u << d;
+      ++n_kept;
+    }
+    if (lane == j) { my_id = b.id; my_g = g; }
+  }
+}
+
+// mode: 0 top-k, 1 device-limited (gate mass), 2 routing-score-based pruning,
+// 3 expert-similarity-based pruning with `table` [Ne, Ne]
 template <int PER_LANE>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v, int T, int Ne,
-             int k, int Nd, int renorm, int limited, int n_keep, int32_t* __restrict__ ids,
-             float* __restrict__ gates, uint32_t* __restrict__ vmask) {
+route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v,
+             const float* __restrict__ table, int T, int Ne, int k, int Nd, int renorm, int mode,
+             int n_keep, int32_t* __restrict__ ids, float* __restrict__ gates,
+             int32_t* __restrict__ routed, uint32_t* __restrict__ vmask) {
   __shared__ float s_ex[kWarpsPerBlock][PER_LANE * 32];
   __shared__ int s_dev[PER_LANE * 32];
   for (int e = threadIdx.x; e < PER_LANE * 32; e += blockDim.x) s_dev[e] = e < Ne ? e2v[e] : -1;
@@ -79,7 +131,7 @@ route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v, 
 
     // device-limited mode: devices allowed for this token
     uint32_t allowed = 0xffffffffu;
-    if (limited) {
+    if (mode == 1) {
 #pragma unroll
       for (int i = 0; i < PER_LANE; ++i) s_ex[warp][lane + 32 * i] = ex[i];
       __syncwarp();
@@ -101,32 +153,54 @@ route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v, 
       __syncwarp();
     }
 
-    // top-k by logit among allowed experts
-    bool taken[PER_LANE];
-#pragma unroll
-    for (int i = 0; i < PER_LANE; ++i)
-      taken[i] = (lane + 32 * i >= Ne) || !((allowed >> (dev[i] & 31)) & 1u);
-    uint32_t vm = 0;
+    // top-k by logit among the allowed experts; for the pages' pruning rules this
+    // is the routed set, whose devices (in descending score) give the kept range
+    uint32_t vm = 0, kept = 0;
     float gsum = 0.f;
     int my_id = 0;
     float my_g = 0.f;
-    for (int j = 0; j < k; ++j) {
-      Cand c{NEG, 0x7fffffff};
+    topk_pass<PER_LANE>(v, ex, dev, Ne, k, Z, allowed, mode >= 2, n_keep, my_id, my_g, vm, gsum,
+                        kept);
+    if (mode == 3 && routed && lane < k) routed[static_cast<size_t>(t) * k + lane] = my_id;
+    if (mode == 2) {
+      // routing-score-based pruning: the top k of all sorted scores that lie on
+      // the kept devices
+      topk_pass<PER_LANE>(v, ex, dev, Ne, k, Z, kept, false, 0, my_id, my_g, vm, gsum, kept);
+    } else if (mode == 3) {
+      // expert-similarity-based pruning: routed experts on the kept devices stay
+      // (and count as selected); each other slot, in descending score, takes the
+      // most similar free expert of the kept devices and keeps its routing weight
+      uint32_t sel = 0;  // bit i: expert lane + 32 i selected
+      for (int j = 0; j < k; ++j) {
+        const int rid = __shfl_sync(0xffffffffu, my_id, j);
+        if ((kept >> s_dev[rid]) & 1u)
 #pragma unroll
-      for (int i = 0; i < PER_LANE; ++i)
-        if (!taken[i] && before(v[i], lane + 32 * i, c.v, c.id)) { c.v = v[i]; c.id = lane + 32 * i; }
-      Cand b = warp_best(c);
-      const int owner = b.id & 31, slot = b.id >> 5;
-      float g = 0.f;
-      int d = 0;
+          for (int i = 0; i < PER_LANE; ++i)
+            if (lane + 32 * i == rid) sel |= 1u << i;
+      }
+      for (int j = 0; j < k; ++j) {
+        const int rid = __shfl_sync(0xffffffffu, my_id, j);
+        if ((kept >> s_dev[rid]) & 1u) continue;
+        const float* trow = table + static_cast<size_t>(rid) * Ne;
+        Cand c{NEG, 0x7fffffff};
 #pragma unroll
-      for (int i = 0; i < PER_LANE; ++i)
-        if (lane == owner && slot == i) { taken[i] = true; g = ex[i]; d = dev[i]; }
-      g = __shfl_sync(0xffffffffu, g, owner) / Z;
-      d = __shfl_sync(0xffffffffu, d, owner);
-      vm |= 1u << d;
-      gsum += g;
-      if (lane == j) { my_id = b.id; my_g = g; }
+        for (int i = 0; i < PER_LANE; ++i) {
+          const int e = lane + 32 * i;
+          if (e < Ne && ((kept >> (dev[i] & 31)) & 1u) && !((sel >> i) & 1u)) {
+            float s = trow[e];
+            if (s != s) s = NEG;  // a NaN entry ranks last
+            if (before(s, e, c.v, c.id)) { c.v = s; c.id = e; }
+          }
+        }
+        const Cand b = warp_best(c);
+#pragma unroll
+        for (int i = 0; i < PER_LANE; ++i)
+          if (lane + 32 * i == b.id) sel |= 1u << i;
+        if (lane == j) my_id = b.id;
+      }
+      // devices of the final experts
+      const int my_dev = lane < k ? s_dev[my_id] : 0;
+      vm = __reduce_or_sync(0xffffffffu, lane < k ? 1u << my_dev : 0u);
     }
     if (renorm) my_g = my_g / gsum;
     if (lane < k) {
@@ -140,15 +214,15 @@ route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v, 
 }  // namespace
 
 int launch_route(const LaunchCtx& ctx, const occult_desc_t& ds, const float* logits,
-                 const int32_t* e2v, int32_t* ids, float* gates, uint32_t* vmask) {
+                 const int32_t* e2v, const float* table, int32_t* ids, float* gates,
+                 int32_t* routed, uint32_t* vmask) {
   if (ds.T == 0) return OCCULT_OK;
-  const int limited = ds.route_mode == OCCULT_ROUTE_DEVICE_LIMITED;
   int blocks = (ds.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > ctx.num_sms * 16) blocks = ctx.num_sms * 16;
 #define OCCULT_ROUTE_LAUNCH(PL)                                                              \
   route_kernel<PL><<<blocks, kWarpsPerBlock * 32, 0, ctx.stream>>>(                          \
-      logits, e2v, ds.T, ds.n_experts, ds.top_k, ds.n_vdev, ds.renorm, limited,              \
-      ds.limit_devices, ids, gates, vmask)
+      logits, e2v, table, ds.T, ds.n_experts, ds.top_k, ds.n_vdev, ds.renorm, ds.route_mode, \
+      ds.limit_devices, ids, gates, routed, vmask)
   if (ds.n_experts <= 32) OCCULT_ROUTE_LAUNCH(1);
   else if (ds.n_experts <= 64) OCCULT_ROUTE_LAUNCH(2);
   else if (ds.n_experts <= 128) OCCULT_ROUTE_LAUNCH(4);

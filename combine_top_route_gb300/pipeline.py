@@ -16,10 +16,11 @@ from typing import Dict, Optional
 
 import torch
 
-from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, WS_BUILD_BRIM,
-               WS_EXPERT_BWD, occult_build_brim, occult_combine, occult_desc_t, occult_dispatch,
-               occult_expert_bwd, occult_expert_down, occult_expert_up, occult_gate_grad,
-               occult_route, occult_shared_ffn, workspace_size)
+from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, ROUTE_SCORE_PRUNED,
+               ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD, occult_build_brim,
+               occult_combine, occult_desc_t, occult_dispatch, occult_expert_bwd,
+               occult_expert_down, occult_expert_up, occult_gate_grad, occult_route,
+               occult_route_similarity, occult_router_grad, occult_shared_ffn, workspace_size)
 
 
 def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
@@ -32,7 +33,9 @@ def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
     ds.inter = cfg.inter
     ds.n_vdev = cfg.n_vdev
     ds.dtype = OCCULT_BF16 if cfg.dtype == "bf16" else OCCULT_F32
-    ds.route_mode = ROUTE_DEVICE_LIMITED if cfg.route_mode == "device_limited" else ROUTE_EXACT
+    ds.route_mode = {"exact": ROUTE_EXACT, "device_limited": ROUTE_DEVICE_LIMITED,
+                     "score_pruned": ROUTE_SCORE_PRUNED,
+                     "similarity_pruned": ROUTE_SIMILARITY_PRUNED}[cfg.route_mode]
     ds.limit_devices = cfg.limit_devices
     ds.renorm = int(bool(cfg.renorm))
     ds.n_shared = cfg.n_shared
@@ -46,8 +49,10 @@ class OccultMoE:
 
     def __init__(self, desc: occult_desc_t, weights: Dict[str, torch.Tensor],
                  placement: torch.Tensor, device="cuda", materialize_sfd: bool = False,
-                 train: bool = False):
+                 train: bool = False, sim_table: Optional[torch.Tensor] = None):
         self.desc = desc
+        if desc.route_mode == ROUTE_SIMILARITY_PRUNED and sim_table is None:
+            raise ValueError("similarity-based pruning needs sim_table [Ne, Ne] (fp32)")
         dev = torch.device(device)
         dt = desc.torch_dtype
         self.device = dev
@@ -64,6 +69,11 @@ class OccultMoE:
         i32, f32 = torch.int32, torch.float32
         e = lambda *s, dtype=i32: torch.empty(*s, dtype=dtype, device=dev)  # noqa: E731
         self.ids, self.gates, self.vmask = e(T, k), e(T, k, dtype=f32), e(T)
+        self.sim_table = (sim_table.to(dev, f32).contiguous() if sim_table is not None else None)
+        # the experts whose probabilities the gates are (differs from ids only
+        # under similarity-based pruning)
+        self.routed = e(T, k) if desc.route_mode == ROUTE_SIMILARITY_PRUNED else self.ids
+        self.logits = None
         self.brim0, self.seg_off, self.brim1 = e(Nd, T), e(Nd + 1), e(Ne, T)
         self.exp_off, self.epd_src, self.epd_gate = e(Ne + 1), e(T * k), e(T * k, dtype=f32)
         self.counts = e(4)
@@ -85,6 +95,7 @@ class OccultMoE:
             self.dg_epd = e(T * k, dtype=f32)
             self.dgates = e(T, k, dtype=f32)
             self.dx = e(T, d, dtype=f32)
+            self.dlogits = e(T, Ne, dtype=f32)
             self.bwd_ws = e(max(1, workspace_size(desc, WS_EXPERT_BWD)), dtype=torch.uint8)
         else:
             self.gu_epd = None
@@ -107,7 +118,13 @@ class OccultMoE:
 
     def route_and_index(self, logits: torch.Tensor, stream=None) -> None:
         ds = self.desc
-        occult_route(ds, logits, self.expert_to_vdev, self.ids, self.gates, self.vmask, stream)
+        self.logits = logits
+        if ds.route_mode == ROUTE_SIMILARITY_PRUNED:
+            occult_route_similarity(ds, logits, self.expert_to_vdev, self.sim_table, self.ids,
+                                    self.gates, self.vmask, self.routed, stream)
+        else:
+            occult_route(ds, logits, self.expert_to_vdev, self.ids, self.gates, self.vmask,
+                         stream)
         occult_build_brim(ds, self.ids, self.gates, self.vmask, self.placement, self.brim0,
                           self.seg_off, self.brim1, self.exp_off, self.epd_src, self.epd_gate,
                           self.counts, self.brim_ws, stream)
@@ -131,15 +148,19 @@ class OccultMoE:
     @property
     def launches_per_backward(self) -> int:
         """Kernels one backward call launches."""
-        return 8  # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad
+        # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad,
+        # router grad
+        return 9
 
     def backward(self, dy: torch.Tensor, stream=None):
-        """Gradients of sum(dy * y) after `forward` (train=True): (dx, dw1, dw2, dgates).
+        """Gradients of sum(dy * y) after `forward` (train=True): (dx, dw1, dw2, dgates);
+        the gradient of the router logits is left in ``self.dlogits`` [T, Ne].
 
         dy [T, d] in the layer dtype.  Stage one of scattering sends dy to the SFD
         rows (BRIM0), the expert backward runs on the EPD rows (BRIM1), and the
         two-stage merge brings dx back to the tokens; dgates return through
-        BRIM0 -> BRIM1 as well.  Router logits get no gradient here.
+        BRIM0 -> BRIM1 as well, and on through the softmax of Eq. 2 to the logits
+        the forward was given.
         """
         if not self.train:
             raise RuntimeError("OccultMoE was built without train=True")
@@ -155,4 +176,5 @@ class OccultMoE:
                        stream=stream)
         occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
                          self.exp_off, self.dg_epd, self.dgates, stream)
+        occult_router_grad(ds, self.logits, self.routed, self.dgates, self.dlogits, stream)
         return self.dx, self.dw1, self.dw2, self.dgates

@@ -59,6 +59,9 @@ extern "C" {
 
 #define OCCULT_ROUTE_EXACT           0  /* Eq. 2 top-k                                 */
 #define OCCULT_ROUTE_DEVICE_LIMITED  1  /* keep `limit_devices` devices, then top-k   */
+#define OCCULT_ROUTE_SCORE_PRUNED    2  /* Sec. 3.3 routing-score-based pruning       */
+#define OCCULT_ROUTE_SIMILARITY_PRUNED 3 /* Sec. 3.3 expert-similarity-based pruning:
+                                            occult_route_similarity only           */
 
 /* Largest supported sizes. */
 #define OCCULT_MAX_EXPERTS  256
@@ -78,8 +81,9 @@ typedef struct occult_desc {
   int32_t inter;
   int32_t n_vdev;
   int32_t dtype;          /* OCCULT_F32 | OCCULT_BF16                              */
-  int32_t route_mode;     /* OCCULT_ROUTE_EXACT | OCCULT_ROUTE_DEVICE_LIMITED      */
-  int32_t limit_devices;  /* devices kept per token in device-limited mode         */
+  int32_t route_mode;     /* OCCULT_ROUTE_*                                        */
+  int32_t limit_devices;  /* devices kept per token by the pruning modes (>= 1,
+                             and they must hold at least top_k experts)            */
   int32_t renorm;         /* 1: renormalise the k gates to sum to one              */
   int32_t n_shared;       /* always-on shared experts (0 = none)                   */
   int32_t shared_inter;   /* intermediate size of each shared expert               */
@@ -133,9 +137,75 @@ int occult_place(const int64_t* C, int32_t n_experts, int32_t n_vdev,
  * Device-limited mode keeps the desc->limit_devices devices with the largest
  * summed softmax mass over all their experts (ties: lower device), takes the
  * top-k among their experts and renormalises the gates.
+ * Score-pruned mode is Sec. 3.3's routing-score-based pruning: the kept devices
+ * are those of the token's routed (top-k) experts taken in descending score
+ * until desc->limit_devices are found; ids are then the top-k of all sorted
+ * scores among the experts of the kept devices, gates their probabilities
+ * (renormalised if desc->renorm).
+ * OCCULT_ROUTE_SIMILARITY_PRUNED needs occult_route_similarity (INVALID_ARG).
  */
 int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* expert_to_vdev,
                  int32_t* ids, float* gates, uint32_t* vmask, occult_stream_t stream);
+
+/*
+ * occult_route_similarity -- Sec. 3.3 expert-similarity-based pruning
+ * (desc->route_mode must be OCCULT_ROUTE_SIMILARITY_PRUNED).
+ *   logits, expert_to_vdev  as occult_route.
+ *   table           fp32 [Ne, Ne] similarity table T (row e: similarity of expert
+ *                   e to every expert; occult_similarity_finish builds it).  A NaN
+ *                   entry ranks below every number.
+ *   ids      out    int32 [T, k]: slot j holds the token's j-th routed expert
+ *                   (descending score) if it lies on a kept device, else the
+ *                   expert of a kept device, not selected yet, with the largest
+ *                   table[routed_j, .] (ties: lower id).  The kept devices are
+ *                   found as in score-pruned mode; routed experts on them count
+ *                   as selected before any replacement.
+ *   gates    out    fp32 [T, k] the routed experts' probabilities (renormalised
+ *                   over the k if desc->renorm): a replacement keeps its slot's
+ *                   routing weight.
+ *   routed   out    int32 [T, k] the routed experts (nullable): the experts whose
+ *                   probabilities the gates are, for occult_router_grad.
+ *   vmask    out    as occult_route, for the final ids.
+ */
+int occult_route_similarity(const occult_desc_t* desc, const float* logits,
+                            const int32_t* expert_to_vdev, const float* table, int32_t* ids,
+                            float* gates, int32_t* routed, uint32_t* vmask,
+                            occult_stream_t stream);
+
+/*
+ * occult_similarity_accumulate -- App. A.3 Eq. 8 accumulator over one batch of
+ * profiled router logits.
+ *   logits    fp32 [n_tok, Ne] (Ne = desc->n_experts).
+ *   G         fp64 [Ne, Ne] in/out: G += logits^T logits.  The caller zeroes G
+ *             before the first batch; batches may be of any size (n_tok >= 0).
+ * Deterministic: each entry adds its batch's products in token order.
+ */
+int occult_similarity_accumulate(const occult_desc_t* desc, const float* logits, int32_t n_tok,
+                                 double* G, occult_stream_t stream);
+
+/*
+ * occult_similarity_finish -- the similarity table from the accumulated G:
+ *   table[i, j] = sign(G_ij) G_ij^2 / (G_ii G_jj)  (fp32 [Ne, Ne]; 0 where G_ii G_jj = 0),
+ * Eq. 8's squared cosine similarity with the sign of Eq. 6's cosine kept, so
+ * that it orders experts as the cosine does.
+ */
+int occult_similarity_finish(const occult_desc_t* desc, const double* G, float* table,
+                             occult_stream_t stream);
+
+/*
+ * occult_router_grad -- gradient of sum_tj dgates_tj * gates_tj with respect to
+ * the router logits, through the softmax of Eq. 2 (the choice of experts is
+ * piecewise constant: no gradient through it).
+ *   logits     fp32 [T, Ne] the router logits the gates came from.
+ *   gate_ids   int32 [T, k] the experts whose probabilities the gates are (the
+ *              ids of occult_route; `routed` of occult_route_similarity).
+ *   dgates     fp32 [T, k] upstream gradient of the gates (occult_gate_grad).
+ *   dlogits    out fp32 [T, Ne].  With p = softmax(logits), A = sum_j dg_j g_j:
+ *              plain gates  dz_e = p_e (sum_{j: id_j = e} dg_j - A);
+ *              desc->renorm dz_e = sum_{j: id_j = e} g_j (dg_j - A).
+ */
+int occult_router_grad(const occult_desc_t* desc, const float* logits, const int32_t* gate_ids,
+                       const float* dgates, float* dlogits, occult_stream_t stream);
 
 /*
  * occult_build_brim -- BRIM0 (Algorithm 3) and BRIM1 (Algorithm 5).

@@ -35,6 +35,7 @@ SEED_WEIGHTS = 1001
 SEED_BATCH = 1002
 SEED_PROFILE = 1003
 SEED_DY = 1004
+SEED_TABLE = 1005
 
 
 @dataclasses.dataclass(frozen=True)
@@ -53,7 +54,9 @@ class LayerConfig:
     experts_per_cluster: int   # m experts boosted per cluster
     prof_tokens: int           # tokens in the profiling batch
     renorm: bool = False       # renormalise the k gates to sum to one
-    route_mode: str = "exact"  # "exact" or "device_limited"
+    # "exact", "device_limited" (gate mass), or the pages' own rules
+    # "score_pruned" and "similarity_pruned"
+    route_mode: str = "exact"
     limit_devices: int = 2     # devices kept in device-limited mode
     n_shared: int = 0          # always-on shared experts
     shared_inter: int = 0      # intermediate size of each shared expert
@@ -98,6 +101,16 @@ CONFIGS: Dict[str, LayerConfig] = {
                                            dtype="bf16", n_clusters=16, experts_per_cluster=10,
                                            prof_tokens=16384, n_shared=2, shared_inter=1408,
                                            route_mode="device_limited", renorm=True),
+    # the OLMoE-shaped forward under the pages' collaboration pruning to 2 devices
+    "olmoe_fwd_score_pruned": LayerConfig("olmoe_fwd_score_pruned", T=4096, d=2048,
+                                          n_experts=64, top_k=8, inter=1024, n_vdev=8,
+                                          dtype="bf16", n_clusters=16, experts_per_cluster=10,
+                                          prof_tokens=16384, route_mode="score_pruned"),
+    "olmoe_fwd_similarity_pruned": LayerConfig("olmoe_fwd_similarity_pruned", T=4096, d=2048,
+                                               n_experts=64, top_k=8, inter=1024, n_vdev=8,
+                                               dtype="bf16", n_clusters=16,
+                                               experts_per_cluster=10, prof_tokens=16384,
+                                               route_mode="similarity_pruned"),
     # OLMoE-shaped training step (forward + backward)
     "olmoe_train": LayerConfig("olmoe_train", T=32768, d=2048, n_experts=64, top_k=8,
                                inter=1024, n_vdev=16, dtype="bf16", n_clusters=16,
@@ -186,3 +199,13 @@ def measured_logits(cfg: LayerConfig, n_tokens: Optional[int] = None) -> torch.T
 
 def profiling_logits(cfg: LayerConfig) -> torch.Tensor:
     return router_logits(cfg, cfg.prof_tokens, SEED_PROFILE)
+
+
+def random_similarity_table(cfg: LayerConfig, seed: int = SEED_TABLE) -> torch.Tensor:
+    """A seeded symmetric fp32 [Ne, Ne] table of values in [-1, 1] (diagonal 1), the
+    shape of a similarity table, for checking pruning by similarity apart from how
+    a table is built."""
+    g = torch.Generator().manual_seed(seed)
+    a = torch.rand(cfg.n_experts, cfg.n_experts, generator=g, dtype=torch.float32) * 2 - 1
+    a = torch.triu(a, diagonal=1)
+    return a + a.T + torch.eye(cfg.n_experts)

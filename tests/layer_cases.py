@@ -38,13 +38,23 @@ class Case:
         t = self.x if name == "x" else self.weights[name]
         return t.detach().float().cpu().numpy()
 
-    def oracle_route(self):
+    def oracle_route(self, table: Optional[np.ndarray] = None):
+        """Oracle routing: ids, gates and the relative margin of a float decision
+        (inf where none is taken); ``table`` for similarity-based pruning."""
         cfg = self.cfg
         lg = self.logits.numpy()
         if cfg.route_mode == "device_limited":
             ids, gates, kept, margin = orouting.route_device_limited(
                 lg, cfg.top_k, self.e2v, cfg.n_vdev, cfg.limit_devices)
             return ids, gates, margin
+        if cfg.route_mode == "score_pruned":
+            ids, gates, _ = orouting.route_score_pruned(lg, cfg.top_k, self.e2v,
+                                                        cfg.limit_devices, renorm=cfg.renorm)
+            return ids, gates, np.full(lg.shape[0], np.inf)
+        if cfg.route_mode == "similarity_pruned":
+            ids, gates, _, _ = orouting.route_similarity_pruned(
+                lg, cfg.top_k, self.e2v, cfg.limit_devices, table, renorm=cfg.renorm)
+            return ids, gates, np.full(lg.shape[0], np.inf)
         ids, gates = orouting.route_topk(lg, cfg.top_k, renorm=cfg.renorm)
         return ids, gates, np.full(lg.shape[0], np.inf)
 

@@ -54,13 +54,17 @@ def _desc(occ, **kw):
     (dict(top_k=65), -1),             # k > Ne
     (dict(T=-1), -1),
     (dict(dtype=5), -1),
-    (dict(route_mode=3), -1),
+    (dict(route_mode=4), -1),
+    (dict(route_mode=-1), -1),
     (dict(n_vdev=64), -2),            # more than 32 virtual devices
     (dict(top_k=17), -2),             # more than 16 experts per token
     (dict(d=2050), -2),               # bf16 rows must be multiples of 64
     (dict(inter=1000), -2),
     (dict(route_mode=1, limit_devices=0), -1),
     (dict(route_mode=1, limit_devices=1, top_k=9), -1),  # 1 device of 8 experts < k
+    (dict(route_mode=2, limit_devices=0), -1),
+    (dict(route_mode=2, limit_devices=1, top_k=9), -1),
+    (dict(route_mode=3, limit_devices=9), -1),          # more than Nd devices
     (dict(n_shared=1, shared_inter=0), -1),
 ])
 def test_bad_descriptors_are_rejected(occ, kw, code):
@@ -91,6 +95,17 @@ def test_calls_reject_bad_arguments_before_launching(occ):
                                   ctypes.c_void_p(16), null, null, ctypes.c_void_p(16),
                                   ctypes.c_size_t(need - 1), null) == occ.ERR_WORKSPACE
     assert L.occult_place(null, 8, 4, null, null) == -1
+    # the similarity mode needs its own entry point and its table, and the
+    # table entry points their buffers
+    sim = _desc(occ, route_mode=occ.ROUTE_SIMILARITY_PRUNED, limit_devices=2)
+    v = ctypes.c_void_p(16)
+    assert L.occult_route(ctypes.byref(sim), v, v, v, v, v, null) == -1
+    assert L.occult_route_similarity(ctypes.byref(good), v, v, v, v, v, null, v, null) == -1
+    assert L.occult_route_similarity(ctypes.byref(sim), v, v, null, v, v, null, v, null) == -1
+    assert L.occult_similarity_accumulate(ctypes.byref(good), null, 16, v, null) == -1
+    assert L.occult_similarity_accumulate(ctypes.byref(good), v, -1, v, null) == -1
+    assert L.occult_similarity_finish(ctypes.byref(good), null, v, null) == -1
+    assert L.occult_router_grad(ctypes.byref(good), v, null, v, v, null) == -1
 
 
 def test_host_placement_matches_oracle(occ, golden):

@@ -89,6 +89,22 @@ def test_backward_full_check(occ, name):
     dx_b += 2 * k * F32_EPS * dx_abs          # the fp32 two-stage merge
     check("dx", dx, ref["dx"], dx_b + 1e-30)
     check("dgates", dgates, ref["dgates"], dg_b)
+    # router logits: the oracle's d-logits of the oracle's dgates; the GPU's carry
+    # the dgates error through p_e (sel_e - A), plus their own fp32 rounding
+    z = case.logits.numpy().astype(np.float64)
+    dz_ref = obackward.router_grad(z, ids, ref["dgates"])
+    p = np.exp(z - z.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    g = np.take_along_axis(p, ids.astype(int), 1)
+    sel_b = np.zeros_like(z)
+    sel_a = np.zeros_like(z)
+    for j in range(k):
+        np.add.at(sel_b, (np.arange(T), ids[:, j]), dg_b[:, j])
+        np.add.at(sel_a, (np.arange(T), ids[:, j]), np.abs(ref["dgates"][:, j]) + dg_b[:, j])
+    A_b = (dg_b * g).sum(1, keepdims=True)
+    A_a = ((np.abs(ref["dgates"]) + dg_b) * g).sum(1, keepdims=True)
+    dz_b = p * (sel_b + A_b) + 4 * (cfg.n_experts + k + 8) * F32_EPS * p * (sel_a + A_a) + 1e-30
+    check("dlogits", moe.dlogits.cpu().numpy(), dz_ref, dz_b)
     w1_b = np.zeros_like(ref["dw1"])
     w2_b = np.zeros_like(ref["dw2"])
     for e, (_, _, b) in B.items():
