@@ -87,6 +87,8 @@ def max_over_ranks(v: float, world: int) -> float:
 def workload_desc(cfg) -> str:
     s = (f"{cfg.name}: T={cfg.T} d={cfg.d} Ne={cfg.n_experts} k={cfg.top_k} I={cfg.inter} "
          f"Nd={cfg.n_vdev} {cfg.dtype} {cfg.route_mode}")
+    if cfg.n_src > 1:
+        s += f" n_src={cfg.n_src}"
     if cfg.n_shared:
         s += f" shared={cfg.n_shared}x{cfg.shared_inter}"
     return s + ", Algorithm 1 placement"
@@ -276,7 +278,9 @@ def run_ours(args, cfg, world, rank, local):
         occ.occult_similarity_accumulate(ds, H, H.shape[0], G)
         table = torch.empty(cfg.n_experts, cfg.n_experts, dtype=torch.float32, device=dev)
         occ.occult_similarity_finish(ds, G, table)
-    moe = occ.OccultMoE(ds, w, L, device=dev, train=train, sim_table=table)
+    sharded = cfg.n_src > 1
+    src_off = synth.source_offsets(cfg) if sharded else None
+    moe = occ.OccultMoE(ds, w, L, device=dev, train=train, sim_table=table, src_off=src_off)
     dy = synth.upstream_grad(cfg, device=dev) if train else None
     stream = torch.cuda.current_stream(dev)
     T, k, d, I = cfg.T, cfg.top_k, cfg.d, cfg.inter
@@ -294,8 +298,24 @@ def run_ours(args, cfg, world, rank, local):
         ("build_brim", lambda: occ.occult_build_brim(
             ds, moe.ids, moe.gates, moe.vmask, moe.placement, moe.brim0, moe.seg_off, moe.brim1,
             moe.exp_off, moe.epd_src, moe.epd_gate, moe.counts, moe.brim_ws, stream)),
-        ("dispatch", lambda: occ.occult_dispatch(ds, x, moe.brim0, moe.vmask, moe.x_sfd,
-                                                 moe.sfd_tok, stream)),
+    ]
+    if sharded:
+        # the sources' send buffers, then the first all-to-all into the devices'
+        # receive buffers
+        calls += [
+            ("shard_plan", lambda: occ.occult_shard_plan(
+                ds, src_off, moe.vmask, moe.brim0, moe.brim0_send, moe.blk_counts, moe.send_off,
+                moe.recv_off, stream)),
+            ("dispatch", lambda: occ.occult_dispatch(ds, x, moe.brim0_send, moe.vmask,
+                                                     moe.x_send, None, stream)),
+            ("all_to_all_0", lambda: occ.occult_all_to_all(
+                ds, moe.n_src, moe.blk_counts, moe.send_off, moe.recv_off, moe.x_send, moe.x_sfd,
+                reverse=False, stream=stream)),
+        ]
+    else:
+        calls.append(("dispatch", lambda: occ.occult_dispatch(ds, x, moe.brim0, moe.vmask,
+                                                              moe.x_sfd, moe.sfd_tok, stream)))
+    calls += [
         ("expert_up", lambda: occ.occult_expert_up(ds, moe.x_sfd, moe.epd_src, moe.epd_gate,
                                                    moe.exp_off, moe.placement, moe.w["w1"],
                                                    moe.h_epd, moe.gu_epd, stream=stream)),
@@ -306,9 +326,25 @@ def run_ours(args, cfg, world, rank, local):
         calls.append(("shared_ffn", lambda: occ.occult_shared_ffn(
             ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s, moe.s_gate, moe.y_s,
             stream)))
-    calls.append(("combine", lambda: occ.occult_combine(ds, moe.y_epd, moe.brim0, moe.seg_off,
-                                                        moe.brim1, moe.exp_off, moe.y,
-                                                        y_shared=moe.y_s, stream=stream)))
+    if sharded:
+        # stage one, the second all-to-all back to the sources, stage two there
+        calls += [
+            ("merge_sfd", lambda: occ.occult_merge_sfd(ds, moe.y_epd, moe.brim0, moe.seg_off,
+                                                       moe.brim1, moe.exp_off, moe.y_sfd,
+                                                       stream)),
+            ("all_to_all_1", lambda: occ.occult_all_to_all(
+                ds, moe.n_src, moe.blk_counts, moe.send_off, moe.recv_off, moe.y_sfd, moe.y_send,
+                reverse=True, stream=stream)),
+            ("combine_sfd", lambda: occ.occult_combine_sfd(ds, moe.y_send, moe.brim0_send, moe.y,
+                                                           y_shared=moe.y_s, stream=stream)),
+        ]
+    else:
+        calls.append(("combine", lambda: occ.occult_combine(ds, moe.y_epd, moe.brim0,
+                                                            moe.seg_off, moe.brim1, moe.exp_off,
+                                                            moe.y, y_shared=moe.y_s,
+                                                            stream=stream)))
+    if train and sharded:
+        raise SystemExit("the timed training step runs single-source")
     if train:
         calls += [
             ("dispatch_dy", lambda: occ.occult_dispatch(ds, dy, moe.brim0, moe.vmask, moe.dy_sfd,
@@ -423,8 +459,21 @@ def run_ours(args, cfg, world, rank, local):
     ridge = tflops * 1e12 / (hbm * 1e9)  # flop per byte where the two roofs meet
     kernels = {c: {"ms": per_call[c]} for c in names}
     kernels["dispatch"].update({"GB/s": (T * d * b + n_sfd * d * b) / per_call["dispatch"] / 1e6})
-    kernels["combine"].update({"GB/s": (n_epd * d * 4 + T * d * 4 + (T * d * 4 if S else 0))
-                                       / per_call["combine"] / 1e6})
+    shared_bytes = T * d * 4 if S else 0
+    hbm_kernels = ["dispatch"]
+    if sharded:
+        # the exchanges read and write every SFD row once; stage one reads the
+        # EPD rows and writes the SFD rows, stage two reads them back
+        kernels["all_to_all_0"]["GB/s"] = 2 * n_sfd * d * b / per_call["all_to_all_0"] / 1e6
+        kernels["all_to_all_1"]["GB/s"] = 2 * n_sfd * d * 4 / per_call["all_to_all_1"] / 1e6
+        kernels["merge_sfd"]["GB/s"] = (n_epd * d * 4 + n_sfd * d * 4) / per_call["merge_sfd"] / 1e6
+        kernels["combine_sfd"]["GB/s"] = ((n_sfd * d * 4 + T * d * 4 + shared_bytes)
+                                          / per_call["combine_sfd"] / 1e6)
+        hbm_kernels += ["all_to_all_0", "all_to_all_1", "merge_sfd", "combine_sfd"]
+    else:
+        kernels["combine"].update({"GB/s": (n_epd * d * 4 + T * d * 4 + shared_bytes)
+                                           / per_call["combine"] / 1e6})
+        hbm_kernels.append("combine")
     for c, (fl, by) in work.items():
         kernels[c].update({"TFLOP/s": fl / per_call[c] / 1e9, "GB/s": by / per_call[c] / 1e6,
                            "bound": "tensor" if fl / by > ridge else "hbm"})
@@ -438,7 +487,7 @@ def run_ours(args, cfg, world, rank, local):
     roofline = {"bound": kernels[dom]["bound"], "kernel": dom, "achieved": achieved,
                 "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": recorded_traffic(cfg.name, dom), "peak_source": src}
-    for c in ("dispatch", "combine"):
+    for c in hbm_kernels:
         kernels[c]["hbm_frac"] = kernels[c]["GB/s"] / hbm
 
     w_bytes = (3 * cfg.n_experts * I + 3 * S) * d * b
@@ -451,7 +500,9 @@ def run_ours(args, cfg, world, rank, local):
                    "l2": f"inputs larger than L2 ({w_bytes / 1e6:.0f} MB of expert weights read "
                          "every step)",
                    "parallelism": f"{world} independent replica(s), Nd={cfg.n_vdev} virtual "
-                                  "expert-parallel devices each"},
+                                  "expert-parallel devices each"
+                                  + (f", batch split over {cfg.n_src} source shards exchanging "
+                                     "row blocks" if sharded else "")},
         "roofline": roofline,
         "kernels": kernels,
         "E[C_T]": n_sfd / T,

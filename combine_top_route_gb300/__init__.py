@@ -27,6 +27,7 @@ ROUTE_SIMILARITY_PRUNED = 3
 MAX_EXPERTS = 256
 MAX_VDEV = 32
 MAX_TOPK = 16
+MAX_SOURCES = 32
 
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED = -2
@@ -90,6 +91,11 @@ _SIGNATURES = {
                                          _VP]),
     "occult_shared_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_combine": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_merge_sfd": (ctypes.c_int, [_D] + [_VP] * 7),
+    "occult_combine_sfd": (ctypes.c_int, [_D] + [_VP] * 5),
+    "occult_shard_plan": (ctypes.c_int, [_D, _I32] + [_VP] * 8),
+    "occult_all_to_all": (ctypes.c_int, [_D, _I32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int64,
+                                         _I32, _VP]),
     "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 16 + [ctypes.c_size_t, _VP]),
     "occult_gate_grad": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
@@ -351,6 +357,57 @@ def occult_combine(desc, y_epd, brim0, seg_off, brim1, exp_off, y, y_shared=None
           _dev(y_shared, f32, T * d, "y_shared", nullable=True),
           _dev(y_sfd, f32, T * min(k, Nd) * d, "y_sfd", nullable=True),
           _dev(y, f32, T * d, "y"), _stream(stream))
+
+
+def occult_merge_sfd(desc, y_epd, brim0, seg_off, brim1, exp_off, y_sfd, stream=None):
+    T, d, Ne, k, Nd = desc.T, desc.d, desc.n_experts, desc.top_k, desc.n_vdev
+    f32, i32 = torch.float32, torch.int32
+    _call("occult_merge_sfd", ctypes.byref(desc), _dev(y_epd, f32, T * k * d, "y_epd"),
+          _dev(brim0, i32, Nd * T, "brim0"), _dev(seg_off, i32, Nd + 1, "seg_off"),
+          _dev(brim1, i32, Ne * T, "brim1"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(y_sfd, f32, T * min(k, Nd) * d, "y_sfd"), _stream(stream))
+
+
+def occult_combine_sfd(desc, y_sfd, row_map, y, y_shared=None, stream=None):
+    T, d, k, Nd = desc.T, desc.d, desc.top_k, desc.n_vdev
+    f32 = torch.float32
+    _call("occult_combine_sfd", ctypes.byref(desc),
+          _dev(y_sfd, f32, T * min(k, Nd) * d, "y_sfd"),
+          _dev(row_map, torch.int32, Nd * T, "row_map"),
+          _dev(y_shared, f32, T * d, "y_shared", nullable=True), _dev(y, f32, T * d, "y"),
+          _stream(stream))
+
+
+def occult_shard_plan(desc, src_off, vmask, brim0, brim0_send, counts, send_off, recv_off,
+                      stream=None):
+    """``src_off``: host sequence of n_src + 1 token offsets of the source shards."""
+    T, Nd = desc.T, desc.n_vdev
+    off = [int(v) for v in src_off]
+    n_src = len(off) - 1
+    host = (ctypes.c_int32 * len(off))(*off)
+    i32 = torch.int32
+    _call("occult_shard_plan", ctypes.byref(desc), n_src, ctypes.cast(host, ctypes.c_void_p),
+          _dev(vmask, i32, T, "vmask"), _dev(brim0, i32, Nd * T, "brim0"),
+          _dev(brim0_send, i32, Nd * T, "brim0_send"),
+          _dev(counts, i32, max(n_src, 1) * Nd, "counts"),
+          _dev(send_off, i32, max(n_src, 1) * Nd, "send_off"),
+          _dev(recv_off, i32, max(n_src, 1) * Nd, "recv_off"), _stream(stream))
+
+
+def occult_all_to_all(desc, n_src, counts, send_off, recv_off, src, dst, reverse=False,
+                      stream=None):
+    """Row blocks between the send and receive layouts; the row size is src's last dim."""
+    T, Nd = desc.T, desc.n_vdev
+    rows = T * min(desc.top_k, Nd)
+    if src.dtype != dst.dtype or src.shape[-1] != dst.shape[-1]:
+        raise ValueError("src and dst must have the same dtype and row length")
+    row_bytes = src.shape[-1] * src.element_size()
+    i32 = torch.int32
+    _call("occult_all_to_all", ctypes.byref(desc), int(n_src),
+          _dev(counts, i32, n_src * Nd, "counts"), _dev(send_off, i32, n_src * Nd, "send_off"),
+          _dev(recv_off, i32, n_src * Nd, "recv_off"),
+          _dev(src, None, rows * src.shape[-1], "src"), _dev(dst, None, rows * dst.shape[-1], "dst"),
+          ctypes.c_int64(row_bytes), int(bool(reverse)), _stream(stream))
 
 
 def occult_profile_coact(desc, ids, n_tok, C, ws, P=None, vmask=None, ct_hist=None,

@@ -486,6 +486,72 @@ int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* 
                         static_cast<float*>(y));
 }
 
+int occult_merge_sfd(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,
+                     const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
+                     void* y_sfd, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(desc->T == 0 || (y_epd && brim0 && seg_off && brim1 && exp_off && y_sfd));
+  OCCULT_CTX(stream);
+  return launch_merge_sfd(ctx, *desc, static_cast<const float*>(y_epd), brim0, seg_off, brim1,
+                          exp_off, static_cast<float*>(y_sfd));
+}
+
+int occult_combine_sfd(const occult_desc_t* desc, const void* y_sfd, const int32_t* row_map,
+                       const void* y_shared, void* y, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(desc->T == 0 || (y_sfd && row_map && y));
+  OCCULT_CTX(stream);
+  return launch_combine_sfd(ctx, *desc, static_cast<const float*>(y_sfd), row_map,
+                            static_cast<const float*>(y_shared), static_cast<float*>(y));
+}
+
+int occult_shard_plan(const occult_desc_t* desc, int32_t n_src, const int32_t* src_off,
+                      const uint32_t* vmask, const int32_t* brim0, int32_t* brim0_send,
+                      int32_t* counts, int32_t* send_off, int32_t* recv_off,
+                      occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(n_src >= 1 && n_src <= OCCULT_MAX_SOURCES && src_off);
+  OCCULT_REQUIRE(counts && send_off && recv_off);
+  OCCULT_REQUIRE(desc->T == 0 || (vmask && brim0 && brim0_send));
+  ShardSplit split;
+  split.n = n_src;
+  OCCULT_REQUIRE(src_off[0] == 0 && src_off[n_src] == desc->T);
+  for (int s = 0; s <= n_src; ++s) {
+    OCCULT_REQUIRE(s == 0 || src_off[s] >= src_off[s - 1]);
+    split.off[s] = src_off[s];
+  }
+  OCCULT_CTX(stream);
+  return launch_shard_plan(ctx, *desc, split, vmask, brim0, brim0_send, counts, send_off,
+                           recv_off);
+}
+
+int occult_all_to_all(const occult_desc_t* desc, int32_t n_src, const int32_t* counts,
+                      const int32_t* send_off, const int32_t* recv_off, const void* src,
+                      void* dst, int64_t row_bytes, int32_t reverse, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(n_src >= 1 && n_src <= OCCULT_MAX_SOURCES);
+  OCCULT_REQUIRE(counts && send_off && recv_off);
+  OCCULT_REQUIRE(row_bytes > 0 && row_bytes % 16 == 0);
+  OCCULT_REQUIRE(reverse == 0 || reverse == 1);
+  OCCULT_REQUIRE(desc->T == 0 || (src && dst));
+  OCCULT_REQUIRE(reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(dst) % 16 == 0);
+  if (desc->T > 0) {
+    // the two buffers must not overlap
+    const int64_t rows = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+    const uintptr_t n = static_cast<uintptr_t>(rows * row_bytes);
+    OCCULT_REQUIRE(a + n <= b || b + n <= a);
+  }
+  OCCULT_CTX(stream);
+  return launch_all_to_all(ctx, *desc, n_src, src, dst, row_bytes, counts, send_off, recv_off,
+                           reverse);
+}
+
 int occult_profile_coact(const occult_desc_t* desc, const int32_t* ids, int32_t n_tok,
                          const uint32_t* vmask, int64_t* C, float* P, int64_t* ct_hist, void* ws,
                          size_t ws_bytes, occult_stream_t stream) {

@@ -206,6 +206,26 @@ int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x
   return cuda_status(cudaGetLastError());
 }
 
+int launch_merge_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
+                     const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
+                     const int32_t* exp_off, float* y_sfd) {
+  if (ds.T == 0) return OCCULT_OK;
+  const int g = grid_for(ctx, ds.T);
+  combine_fused_kernel<true><<<g, kWarps * 32, 0, ctx.stream>>>(
+      y_epd, brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev, ds.n_experts / ds.n_vdev,
+      ds.d, y_sfd, nullptr);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_combine_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_sfd,
+                       const int32_t* brim0, const float* y_shared, float* y) {
+  if (ds.T == 0) return OCCULT_OK;
+  const int g = grid_for(ctx, ds.T);
+  combine_sfd_kernel<<<g, kWarps * 32, 0, ctx.stream>>>(y_sfd, brim0, y_shared, ds.T, ds.n_vdev,
+                                                        ds.d, y);
+  return cuda_status(cudaGetLastError());
+}
+
 int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
                    const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y) {

@@ -28,6 +28,25 @@ int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
                    const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y);
 
+// stage one only (EPD -> SFD, y_sfd written) / stage two only (SFD -> ORI)
+int launch_merge_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
+                     const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
+                     const int32_t* exp_off, float* y_sfd);
+int launch_combine_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_sfd,
+                       const int32_t* brim0, const float* y_shared, float* y);
+
+// Contiguous source shards of the sharded-source mode, passed by value.
+struct ShardSplit {
+  int n;                                 // shards (source devices)
+  int off[OCCULT_MAX_SOURCES + 1];       // shard s holds tokens [off[s], off[s+1])
+};
+int launch_shard_plan(const LaunchCtx& ctx, const occult_desc_t& ds, const ShardSplit& split,
+                      const uint32_t* vmask, const int32_t* brim0, int32_t* brim0_send,
+                      int32_t* counts, int32_t* send_off, int32_t* recv_off);
+int launch_all_to_all(const LaunchCtx& ctx, const occult_desc_t& ds, int n_src, const void* src,
+                      void* dst, int64_t row_bytes, const int32_t* counts,
+                      const int32_t* send_off, const int32_t* recv_off, int reverse);
+
 int launch_similarity_accumulate(const LaunchCtx& ctx, int Ne, const float* logits, int n_tok,
                                  double* G);
 int launch_similarity_finish(const LaunchCtx& ctx, int Ne, const double* G, float* table);

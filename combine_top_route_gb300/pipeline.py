@@ -7,20 +7,30 @@ of the pipeline, sized for the worst case so that no step waits on the host:
     -> expert_up (SFD -> EPD, SwiGLU, modulation) -> expert_down
     -> [shared experts] -> combine (EPD -> SFD -> ORI)
 
+With ``src_off`` (contiguous source shards standing for the source devices of
+App. A.1) the two all-to-alls are real exchanges of row blocks:
+
+    route -> build BRIMs -> shard plan -> dispatch into the sources' send layout
+    -> all_to_all (send -> receive) -> expert_up -> expert_down -> [shared]
+    -> merge_sfd (stage one) -> all_to_all back (receive -> send)
+    -> combine_sfd (stage two over each token's rows at its source)
+
 PyTorch only allocates the buffers and provides the stream; all work runs in
 the library's kernels.
 """
 from __future__ import annotations
 
-from typing import Dict, Optional
+from typing import Dict, Optional, Sequence
 
 import torch
 
-from . import (OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT, ROUTE_SCORE_PRUNED,
-               ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD, occult_build_brim,
-               occult_combine, occult_desc_t, occult_dispatch, occult_expert_bwd,
-               occult_expert_down, occult_expert_up, occult_gate_grad, occult_route,
-               occult_route_similarity, occult_router_grad, occult_shared_ffn, workspace_size)
+from . import (MAX_SOURCES, OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT,
+               ROUTE_SCORE_PRUNED, ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD,
+               occult_all_to_all, occult_build_brim, occult_combine, occult_combine_sfd,
+               occult_desc_t, occult_dispatch, occult_expert_bwd, occult_expert_down,
+               occult_expert_up, occult_gate_grad, occult_merge_sfd, occult_route,
+               occult_route_similarity, occult_router_grad, occult_shard_plan,
+               occult_shared_ffn, workspace_size)
 
 
 def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
@@ -49,7 +59,8 @@ class OccultMoE:
 
     def __init__(self, desc: occult_desc_t, weights: Dict[str, torch.Tensor],
                  placement: torch.Tensor, device="cuda", materialize_sfd: bool = False,
-                 train: bool = False, sim_table: Optional[torch.Tensor] = None):
+                 train: bool = False, sim_table: Optional[torch.Tensor] = None,
+                 src_off: Optional[Sequence[int]] = None):
         self.desc = desc
         if desc.route_mode == ROUTE_SIMILARITY_PRUNED and sim_table is None:
             raise ValueError("similarity-based pruning needs sim_table [Ne, Ne] (fp32)")
@@ -99,6 +110,19 @@ class OccultMoE:
             self.bwd_ws = e(max(1, workspace_size(desc, WS_EXPERT_BWD)), dtype=torch.uint8)
         else:
             self.gu_epd = None
+        # sharded-source mode: the sources' send layout and the exchange plan
+        self.src_off = None if src_off is None else [int(v) for v in src_off]
+        if self.src_off is not None:
+            n_src = len(self.src_off) - 1
+            if not (1 <= n_src <= MAX_SOURCES) or self.src_off[0] != 0 or self.src_off[-1] != T:
+                raise ValueError("src_off must run from 0 to T over 1..32 shards")
+            self.n_src = n_src
+            self.brim0_send = e(Nd, T)
+            self.blk_counts, self.send_off, self.recv_off = e(n_src, Nd), e(n_src, Nd), e(n_src, Nd)
+            self.x_send = e(n_sfd_max, d, dtype=dt)
+            if self.y_sfd is None:
+                self.y_sfd = e(n_sfd_max, d, dtype=f32)
+            self.y_send = e(n_sfd_max, d, dtype=f32)
         if desc.n_shared:
             S = desc.n_shared * desc.shared_inter
             self.h_s, self.y_s = e(T, S, dtype=dt), e(T, d, dtype=f32)
@@ -110,6 +134,8 @@ class OccultMoE:
     def launches_per_forward(self) -> int:
         """Kernels this object launches per forward call."""
         n = 8  # route, 3 BRIM kernels, dispatch, up, down, combine
+        if self.src_off is not None:
+            n += 4  # 2 plan kernels, 2 exchanges; combine runs as stage one + stage two
         if self.y_sfd is not None:
             n += 1
         if self.desc.n_shared:
@@ -128,12 +154,39 @@ class OccultMoE:
         occult_build_brim(ds, self.ids, self.gates, self.vmask, self.placement, self.brim0,
                           self.seg_off, self.brim1, self.exp_off, self.epd_src, self.epd_gate,
                           self.counts, self.brim_ws, stream)
+        if self.src_off is not None:
+            occult_shard_plan(ds, self.src_off, self.vmask, self.brim0, self.brim0_send,
+                              self.blk_counts, self.send_off, self.recv_off, stream)
+
+    def _scatter(self, src: torch.Tensor, out_sfd: torch.Tensor, sfd_tok, stream) -> None:
+        """Stage one of scattering (Algorithm 4) and, sharded, the first all-to-all."""
+        ds = self.desc
+        if self.src_off is None:
+            occult_dispatch(ds, src, self.brim0, self.vmask, out_sfd, sfd_tok, stream)
+            return
+        occult_dispatch(ds, src, self.brim0_send, self.vmask, self.x_send, None, stream)
+        occult_all_to_all(ds, self.n_src, self.blk_counts, self.send_off, self.recv_off,
+                          self.x_send, out_sfd, reverse=False, stream=stream)
+
+    def _merge(self, y_epd: torch.Tensor, out: torch.Tensor, y_shared, stream) -> None:
+        """The two-stage merge; sharded, the second all-to-all runs between the stages."""
+        ds = self.desc
+        if self.src_off is None:
+            occult_combine(ds, y_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, out,
+                           y_shared=y_shared, y_sfd=self.y_sfd, stream=stream)
+            return
+        occult_merge_sfd(ds, y_epd, self.brim0, self.seg_off, self.brim1, self.exp_off,
+                         self.y_sfd, stream)
+        occult_all_to_all(ds, self.n_src, self.blk_counts, self.send_off, self.recv_off,
+                          self.y_sfd, self.y_send, reverse=True, stream=stream)
+        occult_combine_sfd(ds, self.y_send, self.brim0_send, out, y_shared=y_shared,
+                           stream=stream)
 
     def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
         """y = MoE(x) (fp32 [T, d]) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""
         ds = self.desc
         self.route_and_index(logits, stream)
-        occult_dispatch(ds, x, self.brim0, self.vmask, self.x_sfd, self.sfd_tok, stream)
+        self._scatter(x, self.x_sfd, self.sfd_tok, stream)
         occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
                          self.placement, self.w["w1"], self.h_epd, self.gu_epd, stream)
         occult_expert_down(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
@@ -141,16 +194,16 @@ class OccultMoE:
         if ds.n_shared:
             occult_shared_ffn(ds, x, self.w["ws1"], self.w["ws2"], self.w.get("w_sg"), self.h_s,
                               self.s_gate, self.y_s, stream)
-        occult_combine(ds, self.y_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, self.y,
-                       y_shared=self.y_s, y_sfd=self.y_sfd, stream=stream)
+        self._merge(self.y_epd, self.y, self.y_s, stream)
         return self.y
 
     @property
     def launches_per_backward(self) -> int:
         """Kernels one backward call launches."""
         # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad,
-        # router grad
-        return 9
+        # router grad (+ 2 exchanges and the split merge when sharded)
+        n = 9 + (1 if self.y_sfd is not None else 0)
+        return n + (2 if self.src_off is not None else 0)
 
     def backward(self, dy: torch.Tensor, stream=None):
         """Gradients of sum(dy * y) after `forward` (train=True): (dx, dw1, dw2, dgates);
@@ -167,13 +220,12 @@ class OccultMoE:
         ds = self.desc
         if ds.n_shared:
             raise NotImplementedError("backward of shared experts is not provided")
-        occult_dispatch(ds, dy, self.brim0, self.vmask, self.dy_sfd, None, stream)
+        self._scatter(dy, self.dy_sfd, None, stream)
         occult_expert_bwd(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate, self.exp_off,
                           self.placement, self.w["w1"], self.w["w2"], self.h_epd, self.gu_epd,
                           self.dgu_epd, self.dx_epd, self.dw1, self.dw2, self.dg_epd, self.bwd_ws,
                           stream)
-        occult_combine(ds, self.dx_epd, self.brim0, self.seg_off, self.brim1, self.exp_off, self.dx,
-                       stream=stream)
+        self._merge(self.dx_epd, self.dx, None, stream)
         occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
                          self.exp_off, self.dg_epd, self.dgates, stream)
         occult_router_grad(ds, self.logits, self.routed, self.dgates, self.dlogits, stream)

@@ -339,6 +339,76 @@ int occult_combine(const occult_desc_t* desc, const void* y_epd, const int32_t* 
                    const void* y_shared, void* y_sfd, void* y, occult_stream_t stream);
 
 /*
+ * occult_merge_sfd -- stage one of the merge alone (EPD -> SFD, the aggregation
+ * of Algorithm 8): y_sfd[v] = sum_j y_epd[exp_off[d*n_loc] + brim1[d*n_loc + j,
+ * v - seg_off[d]]] for every received row v of every device d, fp32, local
+ * experts in placement order.  y_sfd out fp32 [T*min(k,Nd), d] in the receive
+ * layout of brim0 (the second all-to-all's send buffer); rows >= N_sfd
+ * untouched.  Other arguments as occult_combine.
+ */
+int occult_merge_sfd(const occult_desc_t* desc, const void* y_epd, const int32_t* brim0,
+                     const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
+                     void* y_sfd, occult_stream_t stream);
+
+/*
+ * occult_combine_sfd -- stage two alone (SFD -> ORI, Algorithm 9):
+ *   y[t] = sum over d = 0..Nd-1 with row_map[d, t] >= 0 of y_sfd[row_map[d, t]]
+ *          (+ y_shared[t]),   fp32, devices in ascending order.
+ *   row_map   int32 [Nd, T]: brim0 of occult_build_brim when y_sfd is in the
+ *             receive layout, brim0_send of occult_shard_plan when it is in the
+ *             sources' send layout (after the second all-to-all).
+ *   y_sfd     fp32 [T*min(k,Nd), d];  y_shared fp32 [T, d] nullable;  y out fp32 [T, d].
+ */
+int occult_combine_sfd(const occult_desc_t* desc, const void* y_sfd, const int32_t* row_map,
+                       const void* y_shared, void* y, occult_stream_t stream);
+
+/* Largest number of source shards of the sharded-source mode. */
+#define OCCULT_MAX_SOURCES 32
+
+/*
+ * occult_shard_plan -- sharded-source expert parallelism (App. A.1: Algorithm 2
+ * runs on every device; each source device builds BRIM0 over its own tokens with
+ * Algorithm 3, dispatches them with Algorithm 4, and all_to_all_single sends SFD
+ * segment d to device d with BRIM0 row d's non-zero counts as split sizes).  The
+ * T tokens are split into contiguous source shards that stand for the source
+ * devices.
+ *   n_src      1 <= n_src <= OCCULT_MAX_SOURCES source shards.
+ *   src_off    HOST int32 [n_src + 1]: shard s holds tokens [src_off[s],
+ *              src_off[s+1]); src_off[0] = 0, src_off[n_src] = T, non-decreasing
+ *              (empty shards allowed).  Copied at launch.
+ *   vmask      uint32 [T] from occult_route.
+ *   brim0      int32 [Nd, T] from occult_build_brim: the receive layout, which
+ *              for contiguous shards is device-major, then source, then token.
+ *   brim0_send out int32 [Nd, T]: each token's row in the send layout (the
+ *              sources' SFD tensors end to end: source-major, then device, then
+ *              token) -- Algorithm 3 over shard s, offset by the rows of shards
+ *              0..s-1; -1 where brim0 is -1.  occult_dispatch with it as brim0
+ *              fills the send buffers.
+ *   counts     out int32 [n_src, Nd]: rows shard s sends to device d (split sizes).
+ *   send_off   out int32 [n_src, Nd]: first row of block (s, d) in the send layout.
+ *   recv_off   out int32 [n_src, Nd]: first row of block (s, d) in the receive layout.
+ */
+int occult_shard_plan(const occult_desc_t* desc, int32_t n_src, const int32_t* src_off,
+                      const uint32_t* vmask, const int32_t* brim0, int32_t* brim0_send,
+                      int32_t* counts, int32_t* send_off, int32_t* recv_off,
+                      occult_stream_t stream);
+
+/*
+ * occult_all_to_all -- the exchange of the sharded-source mode as block copies
+ * between the two layouts of occult_shard_plan: block (s, d) moves counts[s, d]
+ * rows from send_off[s, d] to recv_off[s, d] (reverse = 0, the first all-to-all:
+ * sources' SFD tensors -> devices) or back (reverse = 1, the second all-to-all:
+ * stage-one sums -> their sources).
+ *   src, dst   row buffers of at least T*min(k,Nd) rows of row_bytes bytes, not
+ *              overlapping, 16-byte aligned; rows >= N_sfd of dst untouched.
+ *   row_bytes  bytes per row, a positive multiple of 16 (d*2 for bf16 x, d*4 for
+ *              the fp32 stage-one sums).
+ */
+int occult_all_to_all(const occult_desc_t* desc, int32_t n_src, const int32_t* counts,
+                      const int32_t* send_off, const int32_t* recv_off, const void* src,
+                      void* dst, int64_t row_bytes, int32_t reverse, occult_stream_t stream);
+
+/*
  * occult_expert_bwd -- backward of the expert computation (bf16 layers).  The
  * paper states that its sparse kernels serve the backward pass too (Sec. 1) but
  * gives no backward pseudo-code; these are the derivatives of Eq. 1 run through

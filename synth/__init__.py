@@ -62,6 +62,7 @@ class LayerConfig:
     shared_inter: int = 0      # intermediate size of each shared expert
     shared_gate: bool = False  # sigmoid(w_sg . x) gate on the shared output
     backward: bool = False     # the workload includes the backward pass
+    n_src: int = 1             # source shards (1: the whole batch is one source)
 
     @property
     def n_loc(self) -> int:
@@ -111,11 +112,23 @@ CONFIGS: Dict[str, LayerConfig] = {
                                                dtype="bf16", n_clusters=16,
                                                experts_per_cluster=10, prof_tokens=16384,
                                                route_mode="similarity_pruned"),
+    # the OLMoE-shaped forward with the batch split over 8 source devices: the
+    # first all-to-all is a real exchange of row blocks (and the second its reverse)
+    "olmoe_fwd_sharded": LayerConfig("olmoe_fwd_sharded", T=4096, d=2048, n_experts=64,
+                                     top_k=8, inter=1024, n_vdev=8, dtype="bf16",
+                                     n_clusters=16, experts_per_cluster=10, prof_tokens=16384,
+                                     n_src=8),
     # OLMoE-shaped training step (forward + backward)
     "olmoe_train": LayerConfig("olmoe_train", T=32768, d=2048, n_experts=64, top_k=8,
                                inter=1024, n_vdev=16, dtype="bf16", n_clusters=16,
                                experts_per_cluster=10, prof_tokens=16384, backward=True),
 }
+
+
+def source_offsets(cfg: LayerConfig, n_tokens: Optional[int] = None):
+    """Token offsets [n_src + 1] of ``cfg.n_src`` contiguous, near-equal source shards."""
+    T = cfg.T if n_tokens is None else n_tokens
+    return [s * T // cfg.n_src for s in range(cfg.n_src + 1)]
 
 
 def cluster_mask(cfg: LayerConfig, seed: int = SEED_CLUSTERS) -> torch.Tensor:

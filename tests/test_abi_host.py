@@ -106,6 +106,43 @@ def test_calls_reject_bad_arguments_before_launching(occ):
     assert L.occult_similarity_accumulate(ctypes.byref(good), v, -1, v, null) == -1
     assert L.occult_similarity_finish(ctypes.byref(good), null, v, null) == -1
     assert L.occult_router_grad(ctypes.byref(good), v, null, v, v, null) == -1
+    # stage-split merge and the sharded-source plan and exchange
+    assert L.occult_merge_sfd(ctypes.byref(good), v, v, v, v, v, null, null) == -1
+    assert L.occult_combine_sfd(ctypes.byref(good), v, null, null, v, null) == -1
+
+
+def test_shard_entry_points_check_their_arguments(occ):
+    L = occ.lib()
+    good = _desc(occ)
+    v = ctypes.c_void_p(256)
+    null = ctypes.c_void_p(0)
+    T = good.T
+
+    def plan(off, n_src=None):
+        host = (ctypes.c_int32 * len(off))(*off)
+        n = len(off) - 1 if n_src is None else n_src
+        return L.occult_shard_plan(ctypes.byref(good), n, ctypes.cast(host, ctypes.c_void_p),
+                                   v, v, v, v, v, v, null)
+
+    assert plan([0, T // 2, T // 4]) == -1            # not non-decreasing / does not end at T
+    assert plan([1, T]) == -1                         # does not start at 0
+    assert plan([0, T], n_src=0) == -1
+    assert plan(list(range(0, 34)) + [T]) == -1       # more than 32 sources
+    assert L.occult_shard_plan(ctypes.byref(good), 1, null, v, v, v, v, v, v, null) == -1
+
+    def a2a(src, dst, row_bytes, reverse=0, n_src=2):
+        return L.occult_all_to_all(ctypes.byref(good), n_src, v, v, v, ctypes.c_void_p(src),
+                                   ctypes.c_void_p(dst), ctypes.c_int64(row_bytes), reverse, null)
+
+    rows = T * min(good.top_k, good.n_vdev)
+    rb = good.d * 2
+    far = 1 << 40
+    assert a2a(256, far, rb - 8) == -1                # row not a multiple of 16 bytes
+    assert a2a(256, far, 0) == -1
+    assert a2a(264, far, rb) == -1                    # unaligned source
+    assert a2a(256, 256 + rows * rb - 16, rb) == -1   # overlapping buffers
+    assert a2a(256, far, rb, reverse=2) == -1
+    assert a2a(256, far, rb, n_src=33) == -1
 
 
 def test_host_placement_matches_oracle(occ, golden):
