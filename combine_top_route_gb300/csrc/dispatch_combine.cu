@@ -153,33 +153,53 @@ combine_fused_kernel(const float* __restrict__ y_epd, const int32_t* __restrict_
 }
 
 // Stage two from a materialised SFD tensor: y[t] = sum_d y_sfd[brim0[d, t]] (+ shared).
-__global__ void __launch_bounds__(kWarps * 32)
+// The token's rows are first listed in device order (ballot + popcount), then
+// loaded eight at a time so that their loads are in flight together.
+__global__ void __launch_bounds__(kWarps * 32, 3)
 combine_sfd_kernel(const float* __restrict__ y_sfd, const int32_t* __restrict__ brim0,
                    const float* __restrict__ y_shared, int ntok, int Nd, int D,
                    float* __restrict__ y) {
   constexpr int VN = 4;
+  constexpr int kChunk = 8;
+  __shared__ int s_rows[kWarps][OCCULT_MAX_VDEV];
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int nvec = D / VN;
-  for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < ntok; t += gridDim.x * kWarps) {
+  int* rows = s_rows[warp];
+  for (int t = blockIdx.x * kWarps + warp; t < ntok; t += gridDim.x * kWarps) {
     const int my_row = lane < Nd ? brim0[static_cast<size_t>(lane) * ntok + t] : -1;
+    const unsigned bal = __ballot_sync(0xffffffffu, my_row >= 0);
+    if (my_row >= 0) rows[__popc(bal & lanemask_lt())] = my_row;
+    const int n = __popc(bal);
+    __syncwarp();
     for (int v = lane; v < nvec; v += 32) {
-      float acc[VN], f[VN];
+      float acc[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
-      for (int d = 0; d < Nd; ++d) {
-        const int row = __shfl_sync(0xffffffffu, my_row, d);
-        if (row < 0) continue;
-        unpack16(ld_nc_v4(reinterpret_cast<const float4*>(y_sfd + static_cast<size_t>(row) * D) + v), f, float());
+      for (int j0 = 0; j0 < n; j0 += kChunk) {
+        uint4 buf[kChunk];
 #pragma unroll
-        for (int i = 0; i < VN; ++i) acc[i] += f[i];
+        for (int j = 0; j < kChunk; ++j)
+          if (j0 + j < n)
+            buf[j] = ld_nc_v4(reinterpret_cast<const float4*>(y_sfd + static_cast<size_t>(rows[j0 + j]) * D) + v);
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          if (j0 + j < n) {
+            float f[VN];
+            unpack16(buf[j], f, float());
+#pragma unroll
+            for (int i = 0; i < VN; ++i) acc[i] += f[i];
+          }
       }
       if (y_shared) {
+        float f[VN];
         unpack16(ld_nc_v4(reinterpret_cast<const float4*>(y_shared + static_cast<size_t>(t) * D) + v), f, float());
 #pragma unroll
         for (int i = 0; i < VN; ++i) acc[i] += f[i];
       }
       st_v4(reinterpret_cast<float4*>(y + static_cast<size_t>(t) * D) + v, pack16(acc, float()));
     }
+    __syncwarp();
   }
 }
 

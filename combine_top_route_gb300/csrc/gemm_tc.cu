@@ -13,20 +13,21 @@
 // (or, for weight gradients, the 64-row K blocks of that segment), scheduled by a
 // persistent kernel.
 //
-// GEMMs whose A is a plain matrix (the second linear layer, the dgrad through
-// [W_g; W_u], the shared experts) run on CTA pairs (2-CTA clusters, one CTA per
-// SM): tcgen05.mma.cta_group::2 computes a 256 x 256 tile, rows 0..127 in the
-// even CTA, 128..255 (the segment's next M tile) in the odd one; each CTA stages
-// its own 128 A rows and half of the 256 B rows, so a 64-deep k block moves
-// 32 KB into each SM instead of 48 KB and six stages fit.  GEMMs with gathered
-// rows run one 128 x 256 tile per CTA with four 48 KB stages.
+// The forward and dgrad GEMMs (A K-major, gathered or plain; B a plain matrix)
+// run on CTA pairs (2-CTA clusters, one CTA per SM): tcgen05.mma.cta_group::2
+// computes a 256 x 256 tile, rows 0..127 in the even CTA, 128..255 (the
+// segment's next M tile) in the odd one; each CTA stages its own 128 A rows and
+// half of the 256 B rows, so a 64-deep k block moves 32 KB into each SM instead
+// of 48 KB and six stages fit.  The weight gradients (gathered MN-major operands)
+// run one 128 x 256 tile per CTA with four 48 KB stages.
 //
 // CTA = 10 warps, plus 4 when an operand is gathered; warp-specialised:
 //   warp 0       TMA producer for every operand held as a plain 2-D matrix.
 //   warp 1       owns TMEM (512 columns = two 128x256 fp32 accumulators, double-
 //                buffered so one tile's epilogue overlaps the next main loop);
 //                lane 0 issues tcgen05.mma kind::f16 (bf16 in, fp32 accumulate)
-//                -- in a pair only the even CTA's, for both.
+//                -- in a pair only the even CTA's, for both; the odd CTA's lane 0
+//                forwards the completion of its gathered stages to the even one.
 //   warps 2..9   epilogue: tcgen05.ld of the accumulator, two warps per TMEM
 //                lane quarter (half of the columns each).
 //   warps 10..13 cp.async producers for a gathered operand (rows picked by the
@@ -80,6 +81,7 @@ struct SmemTail {
   uint32_t epi[kEpiWarps][32 * 32];  // per epilogue warp: 32 rows x 32 words, XOR-swizzled
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t gfull[kMaxStages];        // a pair's odd CTA: its own cp.async arrivals
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -225,8 +227,8 @@ template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
-  static_assert(!(PAIR && (WGRAD || AM != OP_TMA_K || op_gathered(BMODE))),
-                "CTA pairs run the forward / dgrad GEMMs whose A is a plain matrix");
+  static_assert(!(PAIR && (WGRAD || op_mn(AM) || op_gathered(BMODE))),
+                "CTA pairs run the forward / dgrad GEMMs, A K-major, B a plain matrix");
   constexpr int kStages = stages_for(PAIR);
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
@@ -253,9 +255,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // ---- prologue ------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // the TMA arrival, plus one per cp.async producer thread
-      mbar_init(&tail->full[s], kGather ? 1 + 128 : 1);
+      // the TMA arrival, plus one per cp.async producer thread (and, in a pair,
+      // one forwarded from the odd CTA for all of its producer threads)
+      mbar_init(&tail->full[s], kGather ? 1 + 128 + (PAIR ? 1 : 0) : 1);
       mbar_init(&tail->empty[s], 1);
+      mbar_init(&tail->gfull[s], 128);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
@@ -404,6 +408,27 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (ok) {
           if (PAIR) tc_commit_pair(&tail->tfull[a], 0x3);
           else tc_commit(&tail->tfull[a]);
+        }
+      }
+      if (!ok) {
+        latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    } else if (PAIR && kGather && lane == 0) {
+      // ---- odd CTA: forwards its gathered stages to the even CTA -------------
+      // Its cp.async copies complete on its own barrier; once a stage's have all
+      // landed, they are made visible to the async proxy (the even CTA's MMAs
+      // read them) and counted as one arrival on the even CTA's full barrier.
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tau = unit0; tau < total && ok; tau += n_units) {
+        const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          if (!mbar_wait(&tail->gfull[stage], phase, abort_flag)) { ok = false; break; }
+          fence_proxy_async_smem();
+          mbar_arrive_remote(full_lead + stage * 8);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
@@ -579,7 +604,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int i = 0; i < 8; ++i) {
           const int r = gw * 32 + rsub + 4 * i;
           dst_k[i] = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
-          const int rr = min(r, ti.rows - 1);
+          const int rr = max(0, min(r, ti.rows - 1));  // a pair's empty half reads row 0
           src_k[i] = p.g_ptr + static_cast<int64_t>(p.gather[ti.m0 + rr]) * p.g_ld + chunk * 8;
         }
       }
@@ -624,7 +649,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
         idx_cur = idx_next;
-        cp_async_arrive_noinc(&tail->full[stage]);
+        cp_async_arrive_noinc(PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
     }
@@ -724,13 +749,19 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
   if (!g.wgrad && g.K % BK != 0) return OCCULT_ERR_UNSUPPORTED;
   if (g.n_seg == 0 || (!g.wgrad && g.max_rows == 0)) return OCCULT_OK;
-  // Forward and dgrad GEMMs whose A is a plain matrix run on CTA pairs (one
-  // 256 x 256 tile per pair, each CTA holding 128 rows of B).  Gathered A rows
-  // stay on single CTAs: with cp.async producers beside them the pair's MMAs
-  // measured 2x slower, and TMA tile::gather4 (one instruction per four 128-byte
-  // rows) 2.6x slower than cp.async.
+  // Forward and dgrad GEMMs run on CTA pairs (one 256 x 256 tile per pair, each
+  // CTA holding 128 rows of B), gathered A rows included: each CTA gathers its
+  // own 128 rows with cp.async and the odd CTA forwards its stages' completion
+  // to the even CTA's barrier with a CTA-scope release (a cluster-scope release
+  // there cost ~1 us per stage and made the pair 2.5x slower than one CTA).  TMA
+  // tile::gather4 (one instruction per four 128-byte rows) measured 2.6x slower
+  // than cp.async on single CTAs.
+  // A pair works on two M tiles of one segment at a time: segments shorter than
+  // that (decode-sized batches, ~50 rows an expert) leave half of each pair idle
+  // and run faster on single CTAs.
   const int am = g.a_mode;
-  const bool pair = !g.wgrad && !op_gathered(am);
+  const int64_t avg_rows = g.seg_off ? g.max_rows / g.n_seg : g.max_rows;
+  const bool pair = !g.wgrad && !op_gathered(g.b_mode) && avg_rows >= 2 * BM;
   CUtensorMap ma, mb;
   int rc = operand_map(&ma, am, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
@@ -763,17 +794,17 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.dev_err = ctx.dev_err;
   const int bm = g.b_mode, ep = g.epi;
   // the instantiations the layer uses
+#define OCCULT_ROWS_GEMM(AM_, BM_, EP_)                                                 \
+  if (am == AM_ && bm == BM_ && ep == EP_)                                             \
+    return pair ? launch_tc<AM_, BM_, EP_, false, true>(ctx, ma, mb, p)                \
+                : launch_tc<AM_, BM_, EP_, false, false>(ctx, ma, mb, p);
   if (!g.wgrad) {
-    if (am == OP_GATHER_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
-      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false, false>(ctx, ma, mb, p);
-    if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_SWIGLU)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_SWIGLU, false, true>(ctx, ma, mb, p);
-    if (am == OP_TMA_K && bm == OP_TMA_K && ep == EPI_F32)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false, true>(ctx, ma, mb, p);
-    if (am == OP_GATHER_K && bm == OP_TMA_MN && ep == EPI_SWIGLU_BWD)
-      return launch_tc<OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD, false, false>(ctx, ma, mb, p);
-    if (am == OP_TMA_K && bm == OP_TMA_MN && ep == EPI_F32)
-      return launch_tc<OP_TMA_K, OP_TMA_MN, EPI_F32, false, true>(ctx, ma, mb, p);
+    OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_K, EPI_SWIGLU)     // up-projection
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_SWIGLU)        // shared experts' up-projection
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32)           // down-projections
+    OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD)  // dgrad through W_d
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32)          // dgrad through [W_g; W_u]
+#undef OCCULT_ROWS_GEMM
   } else if (ep == EPI_F32) {
     if (am == OP_GATHER_MN && bm == OP_TMA_MN)
       return launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, p);

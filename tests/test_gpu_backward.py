@@ -23,6 +23,8 @@ TRAIN = synth.CONFIGS["olmoe_train"]
 CASES = {
     "train_slice_1024": TRAIN.with_(name="train_slice_1024", T=1024),
     "ragged_i192": TRAIN.with_(name="ragged_i192", T=333, d=512, inter=192, n_vdev=8),
+    # >= 256 rows an expert: the dgrads run on CTA pairs
+    "pair_ragged": TRAIN.with_(name="pair_ragged", T=2600, d=512, inter=192, n_vdev=8),
 }
 
 

@@ -34,6 +34,9 @@ EDGE = {
     "nloc1": CFG["tiny_f32"].with_(name="nloc1", T=77, n_vdev=8),
     "k1_bf16": CFG["olmoe_fwd"].with_(name="k1_bf16", T=300, top_k=1, d=256, inter=128),
     "k_eq_nd": CFG["olmoe_fwd"].with_(name="k_eq_nd", T=513, d=512, inter=192, n_vdev=8),
+    # >= 256 rows an expert on average: the GEMMs run on CTA pairs, with ragged
+    # segments (pair units whose second tile is partial or empty)
+    "pair_ragged": CFG["olmoe_fwd"].with_(name="pair_ragged", T=2500, d=512, inter=320),
 }
 
 
@@ -189,7 +192,8 @@ def epd_sample(b, n=256, seed=1):
     return np.unique(np.concatenate(rows)).astype(np.int64)
 
 
-@pytest.mark.parametrize("name", ALL + ["ragged_1000", "k1_bf16", "k_eq_nd", "nloc1"])
+@pytest.mark.parametrize("name", ALL + ["ragged_1000", "k1_bf16", "k_eq_nd", "nloc1",
+                                  "pair_ragged"])
 def test_expert_up(occ, name):
     cfg = CFG.get(name) or EDGE[name]
     case = make_case(cfg)
@@ -223,7 +227,7 @@ def test_expert_up(occ, name):
     assert np.isfinite(h.float().cpu().numpy()).all(), "an EPD row was left unwritten"
 
 
-@pytest.mark.parametrize("name", ALL + ["ragged_1000", "k1_bf16", "nloc1"])
+@pytest.mark.parametrize("name", ALL + ["ragged_1000", "k1_bf16", "nloc1", "pair_ragged"])
 def test_expert_down(occ, name):
     cfg = CFG.get(name) or EDGE[name]
     case = make_case(cfg)
