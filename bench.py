@@ -315,17 +315,27 @@ def run_ours(args, cfg, world, rank, local):
     else:
         calls.append(("dispatch", lambda: occ.occult_dispatch(ds, x, moe.brim0, moe.vmask,
                                                               moe.x_sfd, moe.sfd_tok, stream)))
-    calls += [
-        ("expert_up", lambda: occ.occult_expert_up(ds, moe.x_sfd, moe.epd_src, moe.epd_gate,
-                                                   moe.exp_off, moe.placement, moe.w["w1"],
-                                                   moe.h_epd, moe.gu_epd, stream=stream)),
-        ("expert_down", lambda: occ.occult_expert_down(ds, moe.h_epd, moe.exp_off, moe.placement,
-                                                       moe.w["w2"], moe.y_epd, stream)),
-    ]
-    if ds.n_shared:
-        calls.append(("shared_ffn", lambda: occ.occult_shared_ffn(
-            ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s, moe.s_gate, moe.y_s,
-            stream)))
+    calls.append(("expert_up", lambda: occ.occult_expert_up(
+        ds, moe.x_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement, moe.w["w1"],
+        moe.h_epd, moe.gu_epd, stream=stream)))
+    atomic = moe.merge == "atomic"
+    if atomic:
+        # shared experts write y; the down-projection adds every EPD row into its
+        # token's row of y (fp32 atomics): no separate merge kernel
+        if ds.n_shared:
+            calls.append(("shared_ffn", lambda: occ.occult_shared_ffn(
+                ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s, moe.s_gate, moe.y,
+                stream)))
+        calls.append(("expert_down_merge", lambda: occ.occult_expert_down_merge(
+            ds, moe.h_epd, moe.exp_off, moe.placement, moe.w["w2"], moe.epd_src, moe.sfd_tok,
+            moe.y, zero_y=not ds.n_shared, stream=stream)))
+    else:
+        calls.append(("expert_down", lambda: occ.occult_expert_down(
+            ds, moe.h_epd, moe.exp_off, moe.placement, moe.w["w2"], moe.y_epd, stream)))
+        if ds.n_shared:
+            calls.append(("shared_ffn", lambda: occ.occult_shared_ffn(
+                ds, x, moe.w["ws1"], moe.w["ws2"], moe.w.get("w_sg"), moe.h_s, moe.s_gate,
+                moe.y_s, stream)))
     if sharded:
         # stage one, the second all-to-all back to the sources, stage two there
         calls += [
@@ -338,7 +348,7 @@ def run_ours(args, cfg, world, rank, local):
             ("combine_sfd", lambda: occ.occult_combine_sfd(ds, moe.y_send, moe.brim0_send, moe.y,
                                                            y_shared=moe.y_s, stream=stream)),
         ]
-    else:
+    elif not atomic:
         calls.append(("combine", lambda: occ.occult_combine(ds, moe.y_epd, moe.brim0,
                                                             moe.seg_off, moe.brim1, moe.exp_off,
                                                             moe.y, y_shared=moe.y_s,
@@ -443,9 +453,15 @@ def run_ours(args, cfg, world, rank, local):
     work = {
         "expert_up": (4.0 * d * I * n_epd,
                       cfg.n_experts * 2 * I * d * b + n_sfd * d * b + n_epd * I * b),
-        "expert_down": (2.0 * d * I * n_epd,
-                        cfg.n_experts * I * d * b + n_epd * I * b + n_epd * d * 4),
     }
+    if atomic:
+        # weights, h, and y written once (read once more when it holds the shared
+        # output); the additions themselves stay in L2 (y is 4 bytes x T x d)
+        work["expert_down_merge"] = (2.0 * d * I * n_epd, cfg.n_experts * I * d * b
+                                     + n_epd * I * b + T * d * 4 * (2 if cfg.n_shared else 1))
+    else:
+        work["expert_down"] = (2.0 * d * I * n_epd,
+                               cfg.n_experts * I * d * b + n_epd * I * b + n_epd * d * 4)
     if S:
         work["shared_ffn"] = (6.0 * d * S * T, 3 * S * d * b + T * d * b + T * S * b + T * d * 4)
     if train:
@@ -470,7 +486,7 @@ def run_ours(args, cfg, world, rank, local):
         kernels["combine_sfd"]["GB/s"] = ((n_sfd * d * 4 + T * d * 4 + shared_bytes)
                                           / per_call["combine_sfd"] / 1e6)
         hbm_kernels += ["all_to_all_0", "all_to_all_1", "merge_sfd", "combine_sfd"]
-    else:
+    elif not atomic:
         kernels["combine"].update({"GB/s": (n_epd * d * 4 + T * d * 4 + shared_bytes)
                                            / per_call["combine"] / 1e6})
         hbm_kernels.append("combine")
@@ -497,6 +513,8 @@ def run_ours(args, cfg, world, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": workload_desc(cfg),
+                   "merge": ("fp32 atomic adds into the token rows (the paper's merging SMM)"
+                             if atomic else "fixed-order two-stage merge"),
                    "l2": f"inputs larger than L2 ({w_bytes / 1e6:.0f} MB of expert weights read "
                          "every step)",
                    "parallelism": f"{world} independent replica(s), Nd={cfg.n_vdev} virtual "

@@ -87,6 +87,7 @@ _SIGNATURES = {
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_down_merge": (ctypes.c_int, [_D] + [_VP] * 7 + [_I32, _VP]),
     "occult_expert_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                          _VP]),
     "occult_shared_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -318,6 +319,18 @@ def occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream=None):
           _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
           _dev(placement, torch.int32, Ne, "placement"), _dev(w2, dt, Ne * d * I, "w2"),
           _dev(y_epd, torch.float32, T * k * d, "y_epd"), _stream(stream))
+
+
+def occult_expert_down_merge(desc, h_epd, exp_off, placement, w2, epd_src, sfd_tok, y,
+                             zero_y=True, stream=None):
+    """The down-projection with the merge as fp32 atomic adds into y (see occult.h)."""
+    T, d, Ne, k, I, Nd = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter, desc.n_vdev
+    dt, i32 = desc.torch_dtype, torch.int32
+    _call("occult_expert_down_merge", ctypes.byref(desc), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(placement, i32, Ne, "placement"),
+          _dev(w2, dt, Ne * d * I, "w2"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(sfd_tok, i32, T * min(k, Nd), "sfd_tok"), _dev(y, torch.float32, T * d, "y"),
+          int(bool(zero_y)), _stream(stream))
 
 
 def occult_expert_ffn(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd, y_epd,

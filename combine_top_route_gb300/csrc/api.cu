@@ -251,7 +251,8 @@ static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void
 
 static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* h_epd,
                        const int32_t* exp_off, const int32_t* placement, const void* w2,
-                       void* y_epd) {
+                       void* y_epd, const int32_t* out_src = nullptr,
+                       const int32_t* out_tok = nullptr) {
   GroupedGemm g;
   g.a_mode = OP_TMA_K;
   g.b_mode = OP_TMA_K;
@@ -274,6 +275,8 @@ static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const vo
   g.ldo = desc->d;
   g.N_out = desc->d;
   g.K = desc->inter;
+  g.out_src = out_src;
+  g.out_tok = out_tok;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g)
                                     : launch_grouped_gemm_f32(ctx, g);
 }
@@ -301,6 +304,24 @@ int occult_expert_down(const occult_desc_t* desc, const void* h_epd, const int32
   OCCULT_CTX(stream);
   if (desc->T == 0) return OCCULT_OK;
   return expert_down(ctx, desc, h_epd, exp_off, placement, w2, y_epd);
+}
+
+int occult_expert_down_merge(const occult_desc_t* desc, const void* h_epd, const int32_t* exp_off,
+                             const int32_t* placement, const void* w2, const int32_t* epd_src,
+                             const int32_t* sfd_tok, void* y, int32_t zero_y,
+                             occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  OCCULT_REQUIRE(exp_off && placement && w2);
+  OCCULT_REQUIRE(zero_y == 0 || zero_y == 1);
+  OCCULT_REQUIRE(desc->T == 0 || (h_epd && epd_src && sfd_tok && y));
+  OCCULT_CTX(stream);
+  if (desc->T == 0) return OCCULT_OK;
+  if (zero_y &&
+      cudaMemsetAsync(y, 0, static_cast<size_t>(desc->T) * desc->d * sizeof(float), ctx.stream) !=
+          cudaSuccess)
+    return OCCULT_ERR_CUDA;
+  return expert_down(ctx, desc, h_epd, exp_off, placement, w2, y, epd_src, sfd_tok);
 }
 
 int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,

@@ -29,6 +29,8 @@ struct SimtParams {
   int64_t ldo;
   int N_out;
   int K;
+  const int32_t* out_src;  // nullable: rows added into out[out_tok[out_src[r]]]
+  const int32_t* out_tok;
 };
 
 template <bool SWIGLU>
@@ -108,7 +110,8 @@ grouped_gemm_f32_kernel(const SimtParams p) {
       const float g = p.row_gate ? p.row_gate[orow] : 1.0f;
       v = g * (v / (1.0f + expf(-v))) * accu[i];
     }
-    p.out[orow * p.ldo + n] = v;
+    if (p.out_tok) atomicAdd(&p.out[static_cast<int64_t>(p.out_tok[p.out_src[orow]]) * p.ldo + n], v);
+    else p.out[orow * p.ldo + n] = v;
   }
 }
 
@@ -144,6 +147,8 @@ int launch_grouped_gemm_f32(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.ldo = g.ldo;
   p.N_out = g.N_out;
   p.K = g.K;
+  p.out_src = g.out_src;
+  p.out_tok = g.out_tok;
   const int64_t m_tiles = (g.max_rows + TM - 1) / TM + g.n_seg;
   dim3 grid(static_cast<unsigned>(m_tiles), (g.N_out + TN - 1) / TN);
   if (g.epi == EPI_SWIGLU) grouped_gemm_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(p);

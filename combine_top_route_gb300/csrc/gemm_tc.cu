@@ -118,6 +118,8 @@ struct Params {
   __nv_bfloat16* gu_out;       // SwiGLU: optional copy of G|U for the backward
   const __nv_bfloat16* gu_in;  // SwiGLU bwd: G|U saved by the forward
   float* dg_part;              // SwiGLU bwd: [rows, 2 * n_tiles_n] partial gate gradients
+  const int32_t* out_src;      // fp32 reduce: SFD row of every output row
+  const int32_t* out_tok;      // fp32 reduce: token (output row) of every SFD row
   int* dev_err;
 };
 
@@ -201,6 +203,33 @@ __device__ __forceinline__ void store_rows(uint32_t* buf, const uint32_t* v, cha
     if (r < valid)
       st_v4(out + r * row_bytes + c4 * 16,
             *reinterpret_cast<const uint4*>(buf + r * 32 + 4 * (c4 ^ (r & 7))));
+  }
+  __syncwarp();
+}
+
+// Like store_rows<32> (32 rows x 32 fp32 through shared memory, 8 lanes a row),
+// but each 16-byte chunk is added to row dst_row(r) of `out` with a vector
+// reduction; lane r of the warp holds dst_row(r) in `my_dst`.
+__device__ __forceinline__ void red_rows32(uint32_t* buf, const uint32_t* v, float* out,
+                                           int64_t ldo, int64_t my_dst, int valid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 32 + 4 * (j ^ (lane & 7))) =
+        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + lane / 8;
+    const int c4 = lane % 8;
+    const int64_t dst = __shfl_sync(0xffffffffu, my_dst, r);
+    if (r < valid) {
+      const uint4 u = *reinterpret_cast<const uint4*>(buf + r * 32 + 4 * (c4 ^ (r & 7)));
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                   :: "l"(out + dst * ldo + c4 * 4), "f"(__uint_as_float(u.x)),
+                      "f"(__uint_as_float(u.y)), "f"(__uint_as_float(u.z)),
+                      "f"(__uint_as_float(u.w)) : "memory");
+    }
   }
   __syncwarp();
 }
@@ -550,6 +579,17 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         // one partial per (row, N tile, column half)
         if (valid) p.dg_part[grow * (2 * p.n_tiles_n) + 2 * ti.nt + half] = dg;
+      } else if (EPI == EPI_F32_RED) {
+        // fp32 rows added into their tokens' output rows (the merge)
+        const int col0 = ti.nt * BN;
+        const int64_t my_dst = valid ? p.out_tok[p.out_src[grow]] : 0;
+#pragma unroll 1
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+          tmem_ld32(t_row + c, v0);
+          tmem_ld_wait();
+          if (col0 + c < p.N_out)
+            red_rows32(ebuf, v0, static_cast<float*>(p.out) + col0 + c, p.ldo, my_dst, wrows);
+        }
       } else {
         // plain fp32 tile; a weight-gradient tile without rows is zero
         const int col0 = ti.nt * BN;
@@ -791,8 +831,10 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.gu_out = static_cast<__nv_bfloat16*>(g.gu_out);
   p.gu_in = static_cast<const __nv_bfloat16*>(g.gu_in);
   p.dg_part = g.dg_part;
+  p.out_src = g.out_src;
+  p.out_tok = g.out_tok;
   p.dev_err = ctx.dev_err;
-  const int bm = g.b_mode, ep = g.epi;
+  const int bm = g.b_mode, ep = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED : g.epi;
   // the instantiations the layer uses
 #define OCCULT_ROWS_GEMM(AM_, BM_, EP_)                                                 \
   if (am == AM_ && bm == BM_ && ep == EP_)                                             \
@@ -802,6 +844,7 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_K, EPI_SWIGLU)     // up-projection
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_SWIGLU)        // shared experts' up-projection
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32)           // down-projections
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32_RED)       // down-projection + merge
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD)  // dgrad through W_d
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32)          // dgrad through [W_g; W_u]
 #undef OCCULT_ROWS_GEMM

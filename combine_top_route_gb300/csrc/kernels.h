@@ -61,7 +61,9 @@ int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t*
 enum : int { OP_TMA_K = 0, OP_GATHER_K = 1, OP_TMA_MN = 2, OP_GATHER_MN = 3 };
 // Epilogues: SwiGLU + gate -> layer dtype (optionally also G|U); plain fp32;
 // SwiGLU backward -> dG|dU in the layer dtype plus partial gate gradients.
-enum : int { EPI_SWIGLU = 0, EPI_F32 = 1, EPI_SWIGLU_BWD = 2 };
+// EPI_F32_RED: fp32 rows added (red.global.add) into out[out_tok[out_src[r]]]
+// instead of stored at row r (the merge of Algorithm 8 as fp32 atomic adds).
+enum : int { EPI_SWIGLU = 0, EPI_F32 = 1, EPI_SWIGLU_BWD = 2, EPI_F32_RED = 3 };
 
 // Grouped GEMM over segments.
 //  rows mode (wgrad = false): output rows [seg_off[s], seg_off[s+1]) use weight
@@ -98,6 +100,8 @@ struct GroupedGemm {
   void* gu_out = nullptr;             // EPI_SWIGLU: optional G|U [rows, 2*N_out]
   const void* gu_in = nullptr;        // EPI_SWIGLU_BWD: G|U [rows, 2*N_out]
   float* dg_part = nullptr;           // EPI_SWIGLU_BWD: [rows, 2 * ceil(N_out/256)]
+  const int32_t* out_src = nullptr;   // EPI_F32_RED: SFD row of every output row
+  const int32_t* out_tok = nullptr;   // EPI_F32_RED: token of every SFD row
 };
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g);

@@ -4,8 +4,12 @@
 of the pipeline, sized for the worst case so that no step waits on the host:
 
     route -> build BRIMs -> dispatch (ORI -> SFD, first all-to-all's send buffer)
-    -> expert_up (SFD -> EPD, SwiGLU, modulation) -> expert_down
-    -> [shared experts] -> combine (EPD -> SFD -> ORI)
+    -> expert_up (SFD -> EPD, SwiGLU, modulation) -> [shared experts]
+    -> expert_down_merge (the second linear layer; its rows added into the
+       token rows with fp32 atomics, the paper's merging SMM)
+
+or, with ``merge="ordered"`` (bit-reproducible), the down-projection writes the
+fp32 EPD rows and ``combine`` sums them in a fixed order (EPD -> SFD -> ORI).
 
 With ``src_off`` (contiguous source shards standing for the source devices of
 App. A.1) the two all-to-alls are real exchanges of row blocks:
@@ -28,6 +32,7 @@ from . import (MAX_SOURCES, OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE
                ROUTE_SCORE_PRUNED, ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD,
                occult_all_to_all, occult_build_brim, occult_combine, occult_combine_sfd,
                occult_desc_t, occult_dispatch, occult_expert_bwd, occult_expert_down,
+               occult_expert_down_merge,
                occult_expert_up, occult_gate_grad, occult_merge_sfd, occult_route,
                occult_route_similarity, occult_router_grad, occult_shard_plan,
                occult_shared_ffn, workspace_size)
@@ -60,8 +65,18 @@ class OccultMoE:
     def __init__(self, desc: occult_desc_t, weights: Dict[str, torch.Tensor],
                  placement: torch.Tensor, device="cuda", materialize_sfd: bool = False,
                  train: bool = False, sim_table: Optional[torch.Tensor] = None,
-                 src_off: Optional[Sequence[int]] = None):
+                 src_off: Optional[Sequence[int]] = None, merge: Optional[str] = None):
+        """``merge``: "atomic" (default; fp32 atomic adds into the token rows) or
+        "ordered" (fixed order, bit-reproducible; the only one with a
+        materialised SFD stage or source shards, and their default)."""
         self.desc = desc
+        staged = materialize_sfd or src_off is not None
+        if merge is None:
+            merge = "ordered" if staged else "atomic"
+        if merge not in ("atomic", "ordered") or (merge == "atomic" and staged):
+            raise ValueError("merge must be 'ordered' or 'atomic'; the atomic merge has no "
+                             "materialised SFD stage and no source shards")
+        self.merge = merge
         if desc.route_mode == ROUTE_SIMILARITY_PRUNED and sim_table is None:
             raise ValueError("similarity-based pruning needs sim_table [Ne, Ne] (fp32)")
         dev = torch.device(device)
@@ -91,7 +106,8 @@ class OccultMoE:
         self.brim_ws = e(max(1, workspace_size(desc, WS_BUILD_BRIM)), dtype=torch.uint8)
         self.x_sfd, self.sfd_tok = e(n_sfd_max, d, dtype=dt), e(n_sfd_max)
         # after the second linear layer everything is fp32
-        self.h_epd, self.y_epd = e(T * k, I, dtype=dt), e(T * k, d, dtype=f32)
+        self.h_epd = e(T * k, I, dtype=dt)
+        self.y_epd = e(T * k, d, dtype=f32) if merge == "ordered" else None
         self.y = e(T, d, dtype=f32)
         self.y_sfd = e(n_sfd_max, d, dtype=f32) if materialize_sfd else None
         self.train = train
@@ -134,6 +150,8 @@ class OccultMoE:
     def launches_per_forward(self) -> int:
         """Kernels this object launches per forward call."""
         n = 8  # route, 3 BRIM kernels, dispatch, up, down, combine
+        if self.merge == "atomic":
+            n -= 1  # the down-projection merges
         if self.src_off is not None:
             n += 4  # 2 plan kernels, 2 exchanges; combine runs as stage one + stage two
         if self.y_sfd is not None:
@@ -189,6 +207,15 @@ class OccultMoE:
         self._scatter(x, self.x_sfd, self.sfd_tok, stream)
         occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
                          self.placement, self.w["w1"], self.h_epd, self.gu_epd, stream)
+        if self.merge == "atomic":
+            # the shared experts write y, the routed experts' rows are added to it
+            if ds.n_shared:
+                occult_shared_ffn(ds, x, self.w["ws1"], self.w["ws2"], self.w.get("w_sg"),
+                                  self.h_s, self.s_gate, self.y, stream)
+            occult_expert_down_merge(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
+                                     self.epd_src, self.sfd_tok, self.y,
+                                     zero_y=not ds.n_shared, stream=stream)
+            return self.y
         occult_expert_down(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
                            self.y_epd, stream)
         if ds.n_shared:

@@ -303,6 +303,26 @@ int occult_expert_down(const occult_desc_t* desc, const void* h_epd, const int32
                        const int32_t* placement, const void* w2, void* y_epd,
                        occult_stream_t stream);
 
+/*
+ * occult_expert_down_merge -- occult_expert_down with the merge folded into it
+ * as fp32 atomic additions, which is how the paper's merging SMM aggregates
+ * (Algorithm 8; Sec. 3.1 footnote 3: fp32 atomic adds, cast afterwards).  On one
+ * GPU the second all-to-all is the identity and both merge stages are plain sums,
+ * so every EPD row is added straight into its token's output row:
+ *   y[sfd_tok[epd_src[r]]] += h_epd[r, :] . W_d[e]^T   for every EPD row r.
+ *   epd_src  int32 [T*k] from occult_build_brim.
+ *   sfd_tok  int32 [T*min(k,Nd)] from occult_dispatch (token of every SFD row).
+ *   y        in/out fp32 [T, d].  zero_y = 1: the call zeroes y first; zero_y = 0:
+ *            the rows are added to what y holds (e.g. the shared experts' output).
+ * The additions land in no fixed order: y equals occult_combine's ordered merge
+ * up to fp32 rounding of the k terms of each element, but is not bit-reproducible
+ * from run to run (use occult_expert_down + occult_combine for that).
+ */
+int occult_expert_down_merge(const occult_desc_t* desc, const void* h_epd, const int32_t* exp_off,
+                             const int32_t* placement, const void* w2, const int32_t* epd_src,
+                             const int32_t* sfd_tok, void* y, int32_t zero_y,
+                             occult_stream_t stream);
+
 /* occult_expert_ffn -- occult_expert_up followed by occult_expert_down. */
 int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
                       const float* epd_gate, const int32_t* exp_off, const int32_t* placement,

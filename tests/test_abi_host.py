@@ -39,6 +39,26 @@ def test_exports_every_declared_symbol(occ):
     assert set(names) == set(occ.EXPORTED)
 
 
+def declared_arity():
+    """Number of parameters of every entry point declared in occult.h."""
+    with open(os.path.join(ROOT, "include", "occult.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:int|const char\*)\s+(occult_\w+)\s*\(([^;]*?)\)\s*;", text,
+                         re.M | re.S):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        out[m.group(1)] = len(params)
+    return out
+
+
+def test_binding_signatures_match_the_header(occ):
+    """Every ctypes prototype has as many arguments as its C declaration."""
+    arity = declared_arity()
+    assert set(arity) == set(occ.EXPORTED)
+    for name, (_, args) in occ._SIGNATURES.items():
+        assert len(args) == arity[name], f"{name}: binding {len(args)} args, header {arity[name]}"
+
+
 def test_strerror(occ):
     assert occ.strerror(0) == "success"
     assert "timeout" in occ.strerror(occ.ERR_DEVICE_TIMEOUT) or "expired" in occ.strerror(occ.ERR_DEVICE_TIMEOUT)

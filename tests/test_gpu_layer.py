@@ -272,10 +272,11 @@ def test_shared_ffn(occ, name):
 
 
 # --------------------------------------------------------------------------- whole layer
-def run_layer(occ, case, materialize=False):
+def run_layer(occ, case, materialize=False, merge=None):
     from combine_top_route_gb300 import OccultMoE
     ds = occ.desc_for(case.cfg)
-    moe = OccultMoE(ds, case.weights, torch.as_tensor(case.placement), materialize_sfd=materialize)
+    moe = OccultMoE(ds, case.weights, torch.as_tensor(case.placement), materialize_sfd=materialize,
+                    merge=merge)
     y = moe.forward(case.logits.cuda(), case.x)
     torch.cuda.synchronize()
     return moe, y
@@ -283,10 +284,12 @@ def run_layer(occ, case, materialize=False):
 
 @pytest.mark.parametrize("name", ALL + list(EDGE))
 def test_layer_matches_eq1(occ, name):
-    """Occult without pruning reaches the standard top-k MoE output (Eq. 1)."""
+    """Occult without pruning reaches the standard top-k MoE output (Eq. 1); the
+    merge adds each token's rows with fp32 atomics (the default)."""
     cfg = CFG.get(name) or EDGE[name]
     case = make_case(cfg)
     moe, y = run_layer(occ, case)
+    assert moe.merge == "atomic"
     ids_o, gates_o, margin = case.oracle_route()
     toks = sample_tokens(cfg.T, 64 if cfg.T > 4096 else 128)
     toks = toks[margin[toks] > 1e-5]
@@ -333,11 +336,40 @@ def test_placement_leaves_output_unchanged(occ):
 
 
 def test_deterministic_bitwise(occ):
+    """The ordered merge is bit-reproducible."""
     case = make_case(CFG["olmoe_fwd"].with_(T=2048))
-    _, y1 = run_layer(occ, case)
+    _, y1 = run_layer(occ, case, merge="ordered")
     y1 = y1.clone()
-    _, y2 = run_layer(occ, case)
+    _, y2 = run_layer(occ, case, merge="ordered")
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "olmoe_fwd", "qwen_prefill", "deepseek_decode",
+                                  "pair_ragged", "one_token"])
+def test_atomic_merge_equals_ordered_merge(occ, name):
+    """Both merges sum the same fp32 rows (and the shared output); they differ only
+    by the order of the additions: |diff| <= 2 (k + 2) 2^-24 sum|terms| per element.
+    The ordered merge also meets Eq. 1 on its own."""
+    cfg = CFG.get(name) or EDGE[name]
+    case = make_case(cfg)
+    moe_o, y_o = run_layer(occ, case, merge="ordered")
+    y_o = y_o.clone()
+    moe_a, y_a = run_layer(occ, case, merge="atomic")
+    ids_o, gates_o, margin = case.oracle_route()
+    b = oracle_brims(case, ids_o, gates_o)
+    # sum of |rows| of every token, from the ordered run's fp32 EPD rows
+    y_epd = moe_o.y_epd[:b.n_epd].cpu().numpy().astype(np.float64)
+    S = np.zeros((cfg.T, cfg.d))
+    np.add.at(S, b.epd_tok, np.abs(y_epd))
+    if cfg.n_shared:
+        S += np.abs(moe_o.y_s.cpu().numpy())
+    bound = 2 * (cfg.top_k + 2) * 2.0 ** -24 * S + 1e-30
+    err = np.abs(y_a.cpu().numpy().astype(np.float64) - y_o.cpu().numpy())
+    assert (err <= bound).all(), f"worst excess {float(np.max(err - bound)):.3e}"
+    toks = sample_tokens(cfg.T, 64)
+    toks = toks[margin[toks] > 1e-5]
+    assert_close_layer(y_o.cpu().numpy()[toks], reference_output(case, toks, ids_o, gates_o),
+                       cfg.dtype)
 
 
 def test_empty_batch(occ):
