@@ -359,13 +359,23 @@ def run_ours(args, cfg, world, rank, local):
         calls += [
             ("dispatch_dy", lambda: occ.occult_dispatch(ds, dy, moe.brim0, moe.vmask, moe.dy_sfd,
                                                         None, stream)),
-            ("expert_bwd", lambda: occ.occult_expert_bwd(
+        ]
+        if atomic:
+            calls.append(("expert_bwd", lambda: occ.occult_expert_bwd_merge(
                 ds, moe.x_sfd, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
-                moe.w["w1"], moe.w["w2"], moe.h_epd, moe.gu_epd, moe.dgu_epd, moe.dx_epd, moe.dw1,
-                moe.dw2, moe.dg_epd, moe.bwd_ws, stream)),
-            ("combine_dx", lambda: occ.occult_combine(ds, moe.dx_epd, moe.brim0, moe.seg_off,
-                                                      moe.brim1, moe.exp_off, moe.dx,
-                                                      stream=stream)),
+                moe.w["w1"], moe.w["w2"], moe.h_epd, moe.gu_epd, moe.dgu_epd, moe.sfd_tok, moe.dx,
+                moe.dw1, moe.dw2, moe.dg_epd, moe.bwd_ws, stream)))
+        else:
+            calls += [
+                ("expert_bwd", lambda: occ.occult_expert_bwd(
+                    ds, moe.x_sfd, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
+                    moe.placement, moe.w["w1"], moe.w["w2"], moe.h_epd, moe.gu_epd, moe.dgu_epd,
+                    moe.dx_epd, moe.dw1, moe.dw2, moe.dg_epd, moe.bwd_ws, stream)),
+                ("combine_dx", lambda: occ.occult_combine(ds, moe.dx_epd, moe.brim0, moe.seg_off,
+                                                          moe.brim1, moe.exp_off, moe.dx,
+                                                          stream=stream)),
+            ]
+        calls += [
             ("gate_grad", lambda: occ.occult_gate_grad(ds, moe.ids, moe.placement, moe.brim0,
                                                        moe.seg_off, moe.brim1, moe.exp_off,
                                                        moe.dg_epd, moe.dgates, stream)),
@@ -468,10 +478,10 @@ def run_ours(args, cfg, world, rank, local):
         # dgrad through W_d and [W_g; W_u], wgrad of both: twice the forward FLOPs.
         # Bytes: dy_sfd (twice) and x_sfd gathered rows, the weights read and their
         # fp32 gradients written, G|U read, dG|dU written and read twice, h read,
-        # fp32 dx_epd written
+        # fp32 dx_epd written (with the atomic merge: dx written once)
         work["expert_bwd"] = (2 * 6.0 * d * I * n_epd,
                               3 * n_sfd * d * b + 3 * cfg.n_experts * I * d * (b + 4)
-                              + 9 * n_epd * I * b + n_epd * d * 4)
+                              + 9 * n_epd * I * b + (T * d * 4 if atomic else n_epd * d * 4))
     ridge = tflops * 1e12 / (hbm * 1e9)  # flop per byte where the two roofs meet
     kernels = {c: {"ms": per_call[c]} for c in names}
     kernels["dispatch"].update({"GB/s": (T * d * b + n_sfd * d * b) / per_call["dispatch"] / 1e6})

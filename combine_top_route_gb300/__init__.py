@@ -98,6 +98,7 @@ _SIGNATURES = {
     "occult_all_to_all": (ctypes.c_int, [_D, _I32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int64,
                                          _I32, _VP]),
     "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 16 + [ctypes.c_size_t, _VP]),
+    "occult_expert_bwd_merge": (ctypes.c_int, [_D] + [_VP] * 17 + [ctypes.c_size_t, _VP]),
     "occult_gate_grad": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_size_t, _VP]),
@@ -297,6 +298,27 @@ def occult_expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement
           _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
           _dev(dx_epd, f32, T * k * d, "dx_epd"), _dev(dw1, f32, Ne * 2 * I * d, "dw1"),
           _dev(dw2, f32, Ne * d * I, "dw2"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
+          _stream(stream))
+
+
+def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2,
+                            h_epd, gu_epd, dgu_epd, sfd_tok, dx, dw1, dw2, dg_epd, ws,
+                            stream=None):
+    """occult_expert_bwd with dx merged by fp32 atomics into the token rows (occult.h)."""
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
+    n_sfd_max = T * min(k, desc.n_vdev)
+    need = workspace_size(desc, WS_EXPERT_BWD)
+    _call("occult_expert_bwd_merge", ctypes.byref(desc), _dev(x_sfd, dt, n_sfd_max * d, "x_sfd"),
+          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
+          _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
+          _dev(sfd_tok, i32, n_sfd_max, "sfd_tok"), _dev(dx, f32, T * d, "dx"),
+          _dev(dw1, f32, Ne * 2 * I * d, "dw1"), _dev(dw2, f32, Ne * d * I, "dw2"),
+          _dev(dg_epd, f32, T * k, "dg_epd"),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
 

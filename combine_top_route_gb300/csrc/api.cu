@@ -390,21 +390,27 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g) : launch_grouped_gemm_f32(ctx, g);
 }
 
-int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+// The expert backward; with sfd_tok given, the dgrad through [W_g; W_u] adds its
+// rows into dx[token] (fp32 atomics) instead of writing the EPD rows to dx_out.
+static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w1, const void* w2,
-                      const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
-                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
-                      occult_stream_t stream) {
+                      const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_out,
+                      const int32_t* sfd_tok, float* dw1, float* dw2, float* dg_epd, void* ws,
+                      size_t ws_bytes, occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && w1 && w2 && dw1 && dw2);
   OCCULT_REQUIRE(desc->T == 0 || (x_sfd && dy_sfd && epd_src && epd_gate && h_epd && gu_epd &&
-                                  dgu_epd && dx_epd && dg_epd));
+                                  dgu_epd && dx_out && dg_epd));
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
+  if (sfd_tok && desc->T > 0 &&
+      cudaMemsetAsync(dx_out, 0, static_cast<size_t>(desc->T) * desc->d * sizeof(float),
+                      ctx.stream) != cudaSuccess)
+    return OCCULT_ERR_CUDA;
   if (desc->T == 0) {
     // no rows: every weight gradient is zero
     const size_t n1 = static_cast<size_t>(desc->n_experts) * 2 * desc->inter * desc->d;
@@ -449,7 +455,11 @@ int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
     h.n_groups = Ne;
     h.seg_off = exp_off; h.seg_group = placement; h.n_seg = Ne; h.max_rows = rows;
     h.K = 2 * I; h.N_out = d;
-    h.out = dx_epd; h.ldo = d;
+    h.out = dx_out; h.ldo = d;
+    if (sfd_tok) {
+      h.out_src = epd_src;
+      h.out_tok = sfd_tok;
+    }
     rc = launch_grouped_gemm_bf16(ctx, h);
     if (rc) return rc;
   }
@@ -480,6 +490,27 @@ int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
   v.M_total = 2 * I; v.N_out = d;
   v.out = dw1; v.ldo = d; v.out_group_stride = 2ll * I * d;
   return launch_grouped_gemm_bf16(ctx, v);
+}
+
+int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                      const int32_t* placement, const void* w1, const void* w2,
+                      const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
+                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
+                      occult_stream_t stream) {
+  return expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
+                    gu_epd, dgu_epd, dx_epd, nullptr, dw1, dw2, dg_epd, ws, ws_bytes, stream);
+}
+
+int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+                            const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                            const int32_t* placement, const void* w1, const void* w2,
+                            const void* h_epd, const void* gu_epd, void* dgu_epd,
+                            const int32_t* sfd_tok, float* dx, float* dw1, float* dw2,
+                            float* dg_epd, void* ws, size_t ws_bytes, occult_stream_t stream) {
+  if (desc && desc->T > 0 && !sfd_tok) return OCCULT_ERR_INVALID_ARG;
+  return expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
+                    gu_epd, dgu_epd, dx, sfd_tok, dw1, dw2, dg_epd, ws, ws_bytes, stream);
 }
 
 int occult_gate_grad(const occult_desc_t* desc, const int32_t* ids, const int32_t* placement,

@@ -847,6 +847,7 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32_RED)       // down-projection + merge
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD)  // dgrad through W_d
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32)          // dgrad through [W_g; W_u]
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32_RED)      // the same + merge of dx
 #undef OCCULT_ROWS_GEMM
   } else if (ep == EPI_F32) {
     if (am == OP_GATHER_MN && bm == OP_TMA_MN)

@@ -32,7 +32,7 @@ from . import (MAX_SOURCES, OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE
                ROUTE_SCORE_PRUNED, ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD,
                occult_all_to_all, occult_build_brim, occult_combine, occult_combine_sfd,
                occult_desc_t, occult_dispatch, occult_expert_bwd, occult_expert_down,
-               occult_expert_down_merge,
+               occult_expert_down_merge, occult_expert_bwd_merge,
                occult_expert_up, occult_gate_grad, occult_merge_sfd, occult_route,
                occult_route_similarity, occult_router_grad, occult_shard_plan,
                occult_shared_ffn, workspace_size)
@@ -116,7 +116,8 @@ class OccultMoE:
             self.gu_epd = e(T * k, 2 * I, dtype=dt)
             self.dy_sfd = e(n_sfd_max, d, dtype=dt)
             self.dgu_epd = e(T * k, 2 * I, dtype=dt)
-            self.dx_epd = e(T * k, d, dtype=f32)
+            # fp32 EPD rows of dx only for the ordered merge
+            self.dx_epd = e(T * k, d, dtype=f32) if merge == "ordered" else None
             self.dw1 = e(Ne, 2 * I, d, dtype=f32)
             self.dw2 = e(Ne, d, I, dtype=f32)
             self.dg_epd = e(T * k, dtype=f32)
@@ -230,6 +231,8 @@ class OccultMoE:
         # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad,
         # router grad (+ 2 exchanges and the split merge when sharded)
         n = 9 + (1 if self.y_sfd is not None else 0)
+        if self.merge == "atomic":
+            n -= 1  # the dgrad through [W_g; W_u] merges dx
         return n + (2 if self.src_off is not None else 0)
 
     def backward(self, dy: torch.Tensor, stream=None):
@@ -248,12 +251,22 @@ class OccultMoE:
         if ds.n_shared:
             raise NotImplementedError("backward of shared experts is not provided")
         self._scatter(dy, self.dy_sfd, None, stream)
+        if self.merge == "atomic":
+            occult_expert_bwd_merge(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate,
+                                    self.exp_off, self.placement, self.w["w1"], self.w["w2"],
+                                    self.h_epd, self.gu_epd, self.dgu_epd, self.sfd_tok, self.dx,
+                                    self.dw1, self.dw2, self.dg_epd, self.bwd_ws, stream)
+        else:
+            self._expert_bwd_ordered(stream)
+        occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
+                         self.exp_off, self.dg_epd, self.dgates, stream)
+        occult_router_grad(ds, self.logits, self.routed, self.dgates, self.dlogits, stream)
+        return self.dx, self.dw1, self.dw2, self.dgates
+
+    def _expert_bwd_ordered(self, stream) -> None:
+        ds = self.desc
         occult_expert_bwd(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate, self.exp_off,
                           self.placement, self.w["w1"], self.w["w2"], self.h_epd, self.gu_epd,
                           self.dgu_epd, self.dx_epd, self.dw1, self.dw2, self.dg_epd, self.bwd_ws,
                           stream)
         self._merge(self.dx_epd, self.dx, None, stream)
-        occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
-                         self.exp_off, self.dg_epd, self.dgates, stream)
-        occult_router_grad(ds, self.logits, self.routed, self.dgates, self.dlogits, stream)
-        return self.dx, self.dw1, self.dw2, self.dgates

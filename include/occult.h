@@ -452,6 +452,22 @@ int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
                       occult_stream_t stream);
 
 /*
+ * occult_expert_bwd_merge -- occult_expert_bwd with the merge of dx folded into
+ * the dgrad through [W_g; W_u] as fp32 atomic additions (as occult_expert_down_merge
+ * does for y): dx[sfd_tok[epd_src[r]]] += [dG | dU]_r . [W_g; W_u] for every EPD
+ * row r, so dx_epd is never written.  Same arguments as occult_expert_bwd except
+ *   sfd_tok  int32 [T*min(k,Nd)] from occult_dispatch (token of every SFD row);
+ *   dx       out fp32 [T, d] (zeroed by the call, then accumulated; no fixed
+ *            order of the additions, so not bit-reproducible).
+ */
+int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
+                            const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                            const int32_t* placement, const void* w1, const void* w2,
+                            const void* h_epd, const void* gu_epd, void* dgu_epd,
+                            const int32_t* sfd_tok, float* dx, float* dw1, float* dw2,
+                            float* dg_epd, void* ws, size_t ws_bytes, occult_stream_t stream);
+
+/*
  * occult_gate_grad -- gate gradients back in token order: dgates[t, j] =
  * dg_epd[EPD row of (t, ids[t, j])], the row found as in the combine (BRIM0 gives
  * the token's received row on the expert's device, BRIM1 its EPD row).

@@ -39,9 +39,9 @@ def occ():
     return occ
 
 
-def train_step(occ, case, dy):
+def train_step(occ, case, dy, merge=None):
     moe = occ.OccultMoE(occ.desc_for(case.cfg), case.weights, torch.as_tensor(case.placement),
-                        train=True)
+                        train=True, merge=merge)
     moe.forward(case.logits.cuda(), case.x)
     out = moe.backward(dy)
     torch.cuda.synchronize()
@@ -154,3 +154,24 @@ def test_backward_full_size_sampled(occ):
         b = expert_backward_bounds(x[te], dy_h[te], w1[e], w2[e], gates[te, se])
         check(f"dW1[{e}]", dw1[e], ref["dw1"][e], b["dW1_b"] + 1e-30)
         check(f"dW2[{e}]", dw2[e], ref["dw2"][e], b["dW2_b"] + 1e-30)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_atomic_and_ordered_merges_agree(occ, name):
+    """The merge only changes the order of dx's fp32 additions: the weight and gate
+    gradients are bit for bit the same, dx within 2 k 2^-24 sum|rows| (the sum of
+    |rows| taken from the ordered run's fp32 EPD rows)."""
+    cfg = CASES[name]
+    case = make_case(cfg)
+    dy = synth.upstream_grad(cfg, device="cuda")
+    moe_o, out_o = train_step(occ, case, dy, merge="ordered")
+    dx_abs = np.zeros((cfg.T, cfg.d))
+    tok = moe_o.sfd_tok.cpu().numpy()[moe_o.epd_src.cpu().numpy()]
+    np.add.at(dx_abs, tok, np.abs(moe_o.dx_epd.cpu().numpy().astype(np.float64)))
+    moe_a, out_a = train_step(occ, case, dy, merge="atomic")
+    assert moe_a.merge == "atomic" and moe_a.dx_epd is None
+    for a, b, nm in zip(out_a[1:], out_o[1:], ("dw1", "dw2", "dgates")):
+        assert (a == b).all(), nm
+    assert (moe_a.dlogits.cpu().numpy() == moe_o.dlogits.cpu().numpy()).all()
+    err = np.abs(out_a[0].astype(np.float64) - out_o[0])
+    assert (err <= 2 * cfg.top_k * F32_EPS * dx_abs + 1e-30).all()
