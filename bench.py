@@ -47,6 +47,11 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="olmoe_fwd")
+    p.add_argument("--merge", choices=["atomic", "ordered"], default=None,
+                   help="merge of the expert outputs (default: atomic; ordered with source "
+                        "shards)")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override the workload's token count (smaller profiling cases)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="CPU time of the oracle sample in the baseline leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -280,7 +285,8 @@ def run_ours(args, cfg, world, rank, local):
         occ.occult_similarity_finish(ds, G, table)
     sharded = cfg.n_src > 1
     src_off = synth.source_offsets(cfg) if sharded else None
-    moe = occ.OccultMoE(ds, w, L, device=dev, train=train, sim_table=table, src_off=src_off)
+    moe = occ.OccultMoE(ds, w, L, device=dev, train=train, sim_table=table, src_off=src_off,
+                        merge=args.merge)
     dy = synth.upstream_grad(cfg, device=dev) if train else None
     stream = torch.cuda.current_stream(dev)
     T, k, d, I = cfg.T, cfg.top_k, cfg.d, cfg.inter
@@ -512,7 +518,9 @@ def run_ours(args, cfg, world, rank, local):
         src = f"{peak_src} HBM copy bandwidth"
     roofline = {"bound": kernels[dom]["bound"], "kernel": dom, "achieved": achieved,
                 "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": recorded_traffic(cfg.name, dom), "peak_source": src}
+                "traffic": (recorded_traffic(cfg.name + ("" if atomic else ":ordered"), dom)
+                            if cfg.T == synth.CONFIGS[cfg.name].T else None),
+                "peak_source": src}
     for c in hbm_kernels:
         kernels[c]["hbm_frac"] = kernels[c]["GB/s"] / hbm
 
@@ -553,6 +561,8 @@ def main():
     args = parse()
     world, rank, local = dist_setup(args.gpus)
     cfg = synth.CONFIGS[args.config]
+    if args.tokens is not None:
+        cfg = cfg.with_(T=args.tokens)
     if args.impl == "reference":
         run_reference(args, cfg, world, rank)
     else:

@@ -146,12 +146,14 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
                                                 int rank) {
   TileInfo ti;
   if (WGRAD) {
-    const int per = p.n_tiles_m * p.n_tiles_n;
+    // a pair's unit is two consecutive M tiles of the output matrix
+    const int units_m = PAIR ? p.n_tiles_m / 2 : p.n_tiles_m;
+    const int per = units_m * p.n_tiles_n;
     ti.seg = tau / per;
     const int rem = tau - ti.seg * per;
     const int mt = rem / p.n_tiles_n;
     ti.nt = rem - mt * p.n_tiles_n;
-    ti.m0 = mt * BM;
+    ti.m0 = (PAIR ? 2 * mt + rank : mt) * BM;
     ti.rows = min(BM, p.M_total - ti.m0);
     ti.k0 = seg_at(p, ti.seg);
     ti.k1 = seg_at(p, ti.seg + 1);
@@ -256,8 +258,9 @@ template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
-  static_assert(!(PAIR && (WGRAD || op_mn(AM) || op_gathered(BMODE))),
-                "CTA pairs run the forward / dgrad GEMMs, A K-major, B a plain matrix");
+  static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
+                "paired forward / dgrad GEMMs take A K-major and B a plain matrix");
+  static_assert(!(WGRAD && (!op_mn(AM) || !op_mn(BMODE))), "weight gradients are MN-major");
   constexpr int kStages = stages_for(PAIR);
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
@@ -321,7 +324,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (PAIR) cluster_sync(); else __syncthreads();
   tc_fence_after();
 
-  const int total = WGRAD ? p.n_seg * p.n_tiles_m * p.n_tiles_n
+  const int total = WGRAD ? p.n_seg * (PAIR ? p.n_tiles_m / 2 : p.n_tiles_m) * p.n_tiles_n
                           : tail->mt_off[p.n_seg] * p.n_tiles_n;
   const uint32_t tbase = tail->tmem_base;
   volatile int* abort_flag = &tail->abort_flag;
@@ -352,11 +355,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (leader) mbar_arrive_expect_tx(bar, kTmaBytes);
             const uint32_t lbar = full_lead + stage * 8;
             if (AM == OP_TMA_K) tma_load_2d_pair(sa, &tmA, kb * BK, ti.m0, lbar);
+            if (AM == OP_TMA_MN)
+              for (int a = 0; a < BM / 64; ++a)
+                tma_load_2d_pair(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, lbar);
             if (BMODE == OP_TMA_K) {
               const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0 +
                                rank * (EPI == EPI_SWIGLU ? p.half_n : BN / 2);
               tma_load_2d_pair(sb, &tmB, kb * BK, brow, lbar);
-            } else {
+            } else if (BMODE == OP_TMA_MN) {
               for (int a = 0; a < 2; ++a)
                 tma_load_2d_pair(sb + a * kMnAtomBytes, &tmB, n0 + rank * (BN / 2) + 64 * a, krow, lbar);
             }
@@ -649,9 +655,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
       // MN-major gathers: a warp touches 16 K rows of a stage; lane j < 16 holds
-      // the source row of the warp's j-th one, loaded one stage ahead (-1 past the
-      // segment's end) and handed to the copying lanes by shuffle
-      constexpr int CPR = (AM == OP_GATHER_MN ? BM : BN) / 8;   // chunks per K row
+      // the source row of the warp's j-th one, loaded four stages ahead (-1 past
+      // the segment's end) and handed to the copying lanes by shuffle
+      // chunks per K row: the A tile's 128 columns, or B's 256 (a pair: this CTA's 128)
+      constexpr int CPR = (AM == OP_GATHER_MN ? BM : (PAIR ? BN / 2 : BN)) / 8;
       const int gw = warp - kGatherWarp0;
       const int jrow = CPR == 32 ? gw + 4 * (lane & 15) : 2 * gw + (lane & 1) + 8 * ((lane & 15) >> 1);
       auto load_idx = [&](int kb) -> int {
@@ -659,8 +666,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         return r < ti.k1 ? p.gather[r] : -1;
       };
       int idx_cur = (WGRAD && ti.kb > 0) ? load_idx(0) : -1;
+      int idx_1 = (WGRAD && ti.kb > 1) ? load_idx(1) : -1;
+      int idx_2 = (WGRAD && ti.kb > 2) ? load_idx(2) : -1;
+      int idx_3 = (WGRAD && ti.kb > 3) ? load_idx(3) : -1;
       for (int kb = 0; kb < ti.kb; ++kb) {
-        const int idx_next = (WGRAD && kb + 1 < ti.kb) ? load_idx(kb + 1) : -1;
+        const int idx_4 = (WGRAD && kb + 4 < ti.kb) ? load_idx(kb + 4) : -1;
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
         if (AM == OP_GATHER_K) {
@@ -672,7 +682,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           // past the segment's end and columns past the matrix are zero-filled
           constexpr bool kOnA = (AM == OP_GATHER_MN);
           uint8_t* base = kOnA ? sa : sa + kATileBytes;
-          const int mn0 = kOnA ? ti.m0 : ti.nt * BN;
+          const int mn0 = kOnA ? ti.m0 : ti.nt * BN + (PAIR ? rank * (BN / 2) : 0);
           const int mn_total = kOnA ? p.M_total : p.N_out;
 #pragma unroll
           for (int i = 0; i < CPR / 2; ++i) {
@@ -688,7 +698,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             cp_async_16_zfill(base + off, src, in ? 16u : 0u);
           }
         }
-        idx_cur = idx_next;
+        idx_cur = idx_1;
+        idx_1 = idx_2;
+        idx_2 = idx_3;
+        idx_3 = idx_4;
         cp_async_arrive_noinc(PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
@@ -801,7 +814,8 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // and run faster on single CTAs.
   const int am = g.a_mode;
   const int64_t avg_rows = g.seg_off ? g.max_rows / g.n_seg : g.max_rows;
-  const bool pair = !g.wgrad && !op_gathered(g.b_mode) && avg_rows >= 2 * BM;
+  const bool pair = g.wgrad ? g.M_total % (2 * BM) == 0
+                            : !op_gathered(g.b_mode) && avg_rows >= 2 * BM;
   CUtensorMap ma, mb;
   int rc = operand_map(&ma, am, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
@@ -851,9 +865,11 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
 #undef OCCULT_ROWS_GEMM
   } else if (ep == EPI_F32) {
     if (am == OP_GATHER_MN && bm == OP_TMA_MN)
-      return launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, p);
+      return pair ? launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, true>(ctx, ma, mb, p)
+                  : launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, p);
     if (am == OP_TMA_MN && bm == OP_GATHER_MN)
-      return launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, p);
+      return pair ? launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, true>(ctx, ma, mb, p)
+                  : launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, p);
   }
   return OCCULT_ERR_UNSUPPORTED;
 }
