@@ -9,12 +9,14 @@
 // and the BRIM0 entry of (d, t) is seg_off[d] + #{tokens t' < t using device d}.
 // So both are exclusive prefix counts over tokens, one column per device and one
 // per expert slot, computed with warp ballots and popcounts:
-//   1. count  -- every CTA counts its 64-token tile per column;
-//   2. scan   -- one CTA (a warp scan per column) turns the tile counts into per-tile
-//                column offsets, and
-//                the column totals into seg_off / exp_off;
-//   3. fill   -- every CTA re-counts per warp, adds the warp prefix to its tile
-//                offsets and writes BRIM0, BRIM1, epd_src and epd_gate.
+//   1. count  -- one warp per 32-token tile counts the tile per column;
+//   2. scan   -- one warp per column turns the tile counts into inclusive prefixes
+//                over tiles (in place; the last tile's is the column total);
+//   3. fill   -- every CTA derives seg_off / exp_off from the column totals, re-counts
+//                per warp (the ballots give each tile's own count, so its exclusive
+//                offset is the inclusive prefix minus that count) and writes BRIM0,
+//                BRIM1, epd_src and epd_gate; CTA 0 also writes seg_off, exp_off and
+//                the counts.
 // Integer and deterministic; the workspace holds the [tiles, columns] counts.
 #include "common.cuh"
 #include "kernels.h"
@@ -87,52 +89,82 @@ brim_count_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ 
   if (lane == 0) cnt[static_cast<size_t>(kDevCols + Ne) * n_tiles + tile] = ct;
 }
 
-// 2. scan: one CTA, one warp per column: exclusive prefix over tiles (32 tiles
-//    per step, coalesced), then seg_off / exp_off from the column totals.
-__global__ void __launch_bounds__(1024)
-brim_scan_kernel(int n_tiles, int Ne, int Nd, int32_t* __restrict__ cnt,
-                 int32_t* __restrict__ seg_off, int32_t* __restrict__ exp_off,
-                 int32_t* __restrict__ counts) {
-  __shared__ int s_tot[kDevCols + OCCULT_MAX_EXPERTS + 1];
+// 2. scan: one warp per column: inclusive prefix over tiles, eight 32-tile chunks
+//    loaded at a time so that their loads overlap; the last column (the tiles'
+//    max C_T) is reduced to its maximum, left in its last tile's entry.
+constexpr int kScanWarps = 4;
+__global__ void __launch_bounds__(kScanWarps * 32)
+brim_scan_kernel(int n_tiles, int Ne, int32_t* __restrict__ cnt) {
   const int nc = ncols(Ne);
   const int lane = threadIdx.x & 31;
-  for (int c = threadIdx.x >> 5; c < nc; c += blockDim.x >> 5) {
-    int32_t* col = cnt + static_cast<size_t>(c) * n_tiles;
-    int run = 0;
-    for (int b0 = 0; b0 < n_tiles; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = b < n_tiles ? col[b] : 0;
-      if (c == nc - 1) {
-        int m = v;
+  const int c = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
+  if (c >= nc) return;
+  int32_t* col = cnt + static_cast<size_t>(c) * n_tiles;
+  const bool is_max = c == nc - 1;
+  int run = 0;
+  for (int b0 = 0; b0 < n_tiles; b0 += 8 * 32) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int b = b0 + 32 * u + lane;
+      v[u] = b < n_tiles ? col[b] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int b = b0 + 32 * u + lane;
+      if (is_max) {
+        int m = v[u];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
         run = max(run, m);
       } else {
-        int inc = v;
+        int inc = v[u];
 #pragma unroll
         for (int sh = 1; sh < 32; sh <<= 1) {
-          const int u = __shfl_up_sync(0xffffffffu, inc, sh);
-          if (lane >= sh) inc += u;
+          const int w = __shfl_up_sync(0xffffffffu, inc, sh);
+          if (lane >= sh) inc += w;
         }
-        if (b < n_tiles) col[b] = run + inc - v;
+        if (b < n_tiles) col[b] = run + inc;
         run += __shfl_sync(0xffffffffu, inc, 31);
       }
     }
-    if (lane == 0) s_tot[c] = run;
   }
+  if (is_max && lane == 0) col[n_tiles - 1] = run;
+}
+
+// Exclusive prefix of the column totals (the inclusive prefixes' last entries):
+// out[i] = sum of the totals of columns first .. first+i-1 for i <= n (n <= 256).
+// Every thread of the CTA must call it.
+__device__ void column_offsets(const int32_t* __restrict__ cnt, int n_tiles, int first, int n,
+                               int* out) {
+  __shared__ int s_part[kWarpsPerCta];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int run = 0;  // each warp scans 64 consecutive columns, 32 at a time
+  for (int h = 0; h < 2; ++h) {
+    const int i = warp * 64 + h * 32 + lane;
+    const int v = i < n ? cnt[static_cast<size_t>(first + i) * n_tiles + n_tiles - 1] : 0;
+    int inc = v;
+#pragma unroll
+    for (int sh = 1; sh < 32; sh <<= 1) {
+      const int w = __shfl_up_sync(0xffffffffu, inc, sh);
+      if (lane >= sh) inc += w;
+    }
+    if (i < n) out[i] = run + inc - v;
+    run += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  if (lane == 0) s_part[warp] = run;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int a = 0;
-    for (int d = 0; d < Nd; ++d) seg_off[d] = a, a += s_tot[d];
-    seg_off[Nd] = a;
-    counts[0] = a;
-    int e = 0;
-    for (int s = 0; s < Ne; ++s) exp_off[s] = e, e += s_tot[kDevCols + s];
-    exp_off[Ne] = e;
-    counts[1] = e;
-    counts[2] = s_tot[nc - 1];
-    counts[3] = 0;
+  int base = 0, tot = 0;
+  for (int w = 0; w < kWarpsPerCta; ++w) {
+    if (w < warp) base += s_part[w];
+    tot += s_part[w];
   }
+  for (int h = 0; h < 2; ++h) {
+    const int i = warp * 64 + h * 32 + lane;
+    if (i < n) out[i] += base;
+  }
+  if (threadIdx.x == 0) out[n] = tot;
+  __syncthreads();
 }
 
 // 3. fill: one warp per (tile, device): BRIM0 of device d for the tile's tokens,
@@ -143,18 +175,32 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
 brim_fill_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gates,
                  const uint32_t* __restrict__ vmask, const int32_t* __restrict__ placement,
                  int T, int k, int Ne, int Nd, int n_loc, int n_tiles,
-                 const int32_t* __restrict__ pre, const int32_t* __restrict__ seg_off,
-                 const int32_t* __restrict__ exp_off, int32_t* __restrict__ brim0,
-                 int32_t* __restrict__ brim1, int32_t* __restrict__ epd_src,
-                 float* __restrict__ epd_gate) {
+                 const int32_t* __restrict__ pre, int32_t* __restrict__ seg_off,
+                 int32_t* __restrict__ exp_off, int32_t* __restrict__ counts,
+                 int32_t* __restrict__ brim0, int32_t* __restrict__ brim1,
+                 int32_t* __restrict__ epd_src, float* __restrict__ epd_gate) {
   constexpr int NS = 64 * W64;
   __shared__ int s_slot_of[NS];
   __shared__ int s_expert[NS];
+  __shared__ int s_seg[OCCULT_MAX_VDEV + 1];
+  __shared__ int s_exp[OCCULT_MAX_EXPERTS + 1];
   for (int s = threadIdx.x; s < Ne; s += blockDim.x) {
     s_slot_of[placement[s]] = s;
     s_expert[s] = placement[s];
   }
-  __syncthreads();
+  // segment offsets of the devices and of the expert slots from the column totals
+  column_offsets(pre, n_tiles, 0, Nd, s_seg);
+  column_offsets(pre, n_tiles, kDevCols, Ne, s_exp);
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i <= Nd; i += blockDim.x) seg_off[i] = s_seg[i];
+    for (int i = threadIdx.x; i <= Ne; i += blockDim.x) exp_off[i] = s_exp[i];
+    if (threadIdx.x == 0) {
+      counts[0] = s_seg[Nd];
+      counts[1] = s_exp[Ne];
+      counts[2] = pre[static_cast<size_t>(kDevCols + Ne) * n_tiles + n_tiles - 1];
+      counts[3] = 0;
+    }
+  }
   const int lane = threadIdx.x & 31;
   const int w = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (w >= n_tiles * Nd) return;
@@ -166,7 +212,8 @@ brim_fill_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gate
   const uint32_t vm = valid ? vmask[t] : 0u;
   const unsigned bit = (vm >> d) & 1u;
   const unsigned bal = __ballot_sync(0xffffffffu, bit);
-  const int dbase = pre[static_cast<size_t>(d) * n_tiles + tile] + seg_off[d];
+  // the tile's exclusive offset: its inclusive prefix less its own count
+  const int dbase = pre[static_cast<size_t>(d) * n_tiles + tile] - __popc(bal) + s_seg[d];
   const int sfd = bit ? dbase + __popc(bal & lt) : -1;
   if (valid) brim0[static_cast<size_t>(d) * T + t] = sfd;
   if (bal == 0) return;
@@ -180,19 +227,19 @@ brim_fill_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gate
     my_ids[j] = (bit && j < k) ? ids[static_cast<size_t>(t) * k + j] : -1;
     my_g[j] = (bit && j < k) ? gates[static_cast<size_t>(t) * k + j] : 0.f;
   }
-  const int r_local = sfd - seg_off[d];
-  const int ebase = exp_off[d * n_loc];
+  const int r_local = sfd - s_seg[d];
+  const int ebase = s_exp[d * n_loc];
   for (int j0 = 0; j0 < n_loc; j0 += 32) {
     // lane i holds the row base of slot d*n_loc + j0 + i
     const int sl = d * n_loc + j0 + lane;
     const int sbase_l = (j0 + lane < n_loc)
-        ? pre[static_cast<size_t>(kDevCols + sl) * n_tiles + tile] + exp_off[sl] : 0;
+        ? pre[static_cast<size_t>(kDevCols + sl) * n_tiles + tile] + s_exp[sl] : 0;
     const int jn = min(32, n_loc - j0);
     for (int j = 0; j < jn; ++j) {
       const int s = d * n_loc + j0 + j;
       const unsigned sbit = mask_bit<W64>(m, s);
       const unsigned sbal = __ballot_sync(0xffffffffu, sbit);
-      const int sbase = __shfl_sync(0xffffffffu, sbase_l, j);
+      const int sbase = __shfl_sync(0xffffffffu, sbase_l, j) - __popc(sbal);
       if (bit) {
         int val = -1;
         if (sbit) {
@@ -234,19 +281,24 @@ int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32
                                                                     Ne, Nd, tiles, cnt)
 #define OCCULT_BRIM_FILL(W)                                                                    \
   brim_fill_kernel<W><<<fgrid, kWarpsPerCta * 32, 0, ctx.stream>>>(                            \
-      ids, gates, vmask, placement, T, k, Ne, Nd, n_loc, tiles, cnt, seg_off, exp_off, brim0,  \
-      brim1, epd_src, epd_gate)
-  if (tiles > 0) {
-    if (Ne <= 64) OCCULT_BRIM_COUNT(1);
-    else if (Ne <= 128) OCCULT_BRIM_COUNT(2);
-    else OCCULT_BRIM_COUNT(4);
+      ids, gates, vmask, placement, T, k, Ne, Nd, n_loc, tiles, cnt, seg_off, exp_off, counts, \
+      brim0, brim1, epd_src, epd_gate)
+  if (tiles == 0) {
+    // no tokens: every offset and count is zero
+    if (cudaMemsetAsync(seg_off, 0, (Nd + 1) * sizeof(int32_t), ctx.stream) != cudaSuccess ||
+        cudaMemsetAsync(exp_off, 0, (Ne + 1) * sizeof(int32_t), ctx.stream) != cudaSuccess ||
+        cudaMemsetAsync(counts, 0, 4 * sizeof(int32_t), ctx.stream) != cudaSuccess)
+      return OCCULT_ERR_CUDA;
+    return OCCULT_OK;
   }
-  brim_scan_kernel<<<1, 1024, 0, ctx.stream>>>(tiles, Ne, Nd, cnt, seg_off, exp_off, counts);
-  if (tiles > 0) {
-    if (Ne <= 64) OCCULT_BRIM_FILL(1);
-    else if (Ne <= 128) OCCULT_BRIM_FILL(2);
-    else OCCULT_BRIM_FILL(4);
-  }
+  if (Ne <= 64) OCCULT_BRIM_COUNT(1);
+  else if (Ne <= 128) OCCULT_BRIM_COUNT(2);
+  else OCCULT_BRIM_COUNT(4);
+  brim_scan_kernel<<<(ncols(Ne) + kScanWarps - 1) / kScanWarps, kScanWarps * 32, 0, ctx.stream>>>(
+      tiles, Ne, cnt);
+  if (Ne <= 64) OCCULT_BRIM_FILL(1);
+  else if (Ne <= 128) OCCULT_BRIM_FILL(2);
+  else OCCULT_BRIM_FILL(4);
 #undef OCCULT_BRIM_COUNT
 #undef OCCULT_BRIM_FILL
   return cuda_status(cudaGetLastError());
