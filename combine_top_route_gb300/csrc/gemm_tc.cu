@@ -52,7 +52,7 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int kATileBytes = BM * BK * 2;   // 16 KB
 constexpr int kBTileBytes = BN * BK * 2;   // 32 KB
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 7;
 constexpr int kMnAtomBytes = BK * 128;     // one 64-element MN atom over the 64 K rows
 constexpr int kEpiWarp0 = 2;               // first epilogue warp
 constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, half the columns each
@@ -62,7 +62,12 @@ constexpr uint32_t kTmemCols = 512;
 
 // A CTA pair keeps half of the B tile per CTA: 32 KB stages, six of them, in the
 // shared memory that holds four 48 KB stages of a single CTA.
-__host__ __device__ constexpr int stages_for(bool pair) { return pair ? 6 : 4; }
+// The forward SwiGLU epilogue stores straight from registers and needs no
+// staging buffer: a pair running it takes that 32 KB as a seventh stage.
+__host__ __device__ constexpr bool epi_staged(int epi) { return epi != EPI_SWIGLU; }
+__host__ __device__ constexpr int stages_for(bool pair, int epi = EPI_F32) {
+  return pair ? (epi_staged(epi) ? 6 : 7) : 4;
+}
 __host__ __device__ constexpr int b_stage_bytes(bool pair) { return pair ? kBTileBytes / 2 : kBTileBytes; }
 __host__ __device__ constexpr int stage_bytes(bool pair) { return kATileBytes + b_stage_bytes(pair); }
 __host__ __device__ constexpr bool op_gathered(int m) { return m == OP_GATHER_K || m == OP_GATHER_MN; }
@@ -78,7 +83,6 @@ __host__ __device__ constexpr uint32_t idesc_for(int am, int bm, bool pair) {
 }
 
 struct SmemTail {
-  uint32_t epi[kEpiWarps][32 * 32];  // per epilogue warp: 32 rows x 32 words, XOR-swizzled
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t gfull[kMaxStages];        // a pair's odd CTA: its own cp.async arrivals
@@ -88,10 +92,17 @@ struct SmemTail {
   int abort_flag;
   int mt_off[kMaxSeg + 1];
 };
-__host__ __device__ constexpr int smem_bytes(bool pair) {
-  return 1024 /*alignment slack*/ + stages_for(pair) * stage_bytes(pair) + static_cast<int>(sizeof(SmemTail));
+// per epilogue warp: 32 rows x 32 words, XOR-swizzled; after the tail (rounded up
+// to 128 bytes so that the 16-byte accesses stay aligned), when staged
+constexpr int kTailBytes = (static_cast<int>(sizeof(SmemTail)) + 127) & ~127;
+constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
+__host__ __device__ constexpr int smem_bytes(bool pair, int epi) {
+  return 1024 /*alignment slack*/ + stages_for(pair, epi) * stage_bytes(pair) + kTailBytes +
+         (epi_staged(epi) ? kEpiBytes : 0);
 }
-static_assert(smem_bytes(false) <= 232448 && smem_bytes(true) <= 232448, "shared memory");
+static_assert(smem_bytes(false, EPI_F32) <= 232448 && smem_bytes(true, EPI_F32) <= 232448 &&
+              smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448,
+              "shared memory");
 
 struct Params {
   // schedule
@@ -261,7 +272,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
                 "paired forward / dgrad GEMMs take A K-major and B a plain matrix");
   static_assert(!(WGRAD && (!op_mn(AM) || !op_mn(BMODE))), "weight gradients are MN-major");
-  constexpr int kStages = stages_for(PAIR);
+  constexpr int kStages = stages_for(PAIR, EPI);
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
   constexpr bool kGather = op_gathered(AM) || op_gathered(BMODE);
@@ -490,7 +501,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const int64_t grow = ti.m0 + row;
       const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
       const int64_t wrow0 = ti.m0 + quarter * 32;
-      uint32_t* ebuf = tail->epi[warp - kEpiWarp0];
+      uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes) +
+                       (warp - kEpiWarp0) * 32 * 32;
       uint32_t v0[32], v1[32];
       if (EPI == EPI_SWIGLU) {
         const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
@@ -772,7 +784,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(threads_for(AM, BMODE));
-  cfg.dynamicSmemBytes = smem_bytes(PAIR);
+  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI);
   cfg.stream = ctx.stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
@@ -785,7 +797,8 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   static cudaError_t attr_err = cudaSuccess;
   static int n_pairs = 0;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(PAIR));
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_bytes(PAIR, EPI));
     if (PAIR && attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
       attr_err = cudaOccupancyMaxActiveClusters(&n_pairs, kern, &cfg);
