@@ -4,7 +4,7 @@
 //
 // Atomics-free: one warp per 32-token chunk turns the routing into per-expert
 // token bitsets (one ballot per expert), then C[i, j] is the popcount of the
-// AND of two bitsets, summed over chunks in a fixed order.
+// AND of two bitsets, summed by warp reductions (integers: exact in any order).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -53,30 +53,46 @@ bitset_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ vmas
   }
 }
 
-// C[i, j] for row i (one block), j over threads.
-__global__ void __launch_bounds__(256)
+// C[i, j]: block i keeps expert i's token bitset in shared memory; warp w takes
+// j = w, w + 8, ..., its lanes stride over the words and the popcounts are summed
+// with a warp reduction (integers: exact in any order).
+constexpr int kPairWarps = 8;
+constexpr int kMaxSharedWords = 8192;  // 256K tokens; longer batches read global memory
+__global__ void __launch_bounds__(kPairWarps * 32)
 pair_count_kernel(const uint32_t* __restrict__ bits, int Ne, int nwords, int64_t* __restrict__ C) {
+  __shared__ uint32_t s_bi[kMaxSharedWords];
   const int i = blockIdx.x;
   const uint32_t* bi = bits + static_cast<size_t>(i) * nwords;
-  for (int j = threadIdx.x; j < Ne; j += blockDim.x) {
+  const bool in_smem = nwords <= kMaxSharedWords;
+  if (in_smem)
+    for (int w = threadIdx.x; w < nwords; w += blockDim.x) s_bi[w] = bi[w];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j = warp; j < Ne; j += kPairWarps) {
     const uint32_t* bj = bits + static_cast<size_t>(j) * nwords;
     long long acc = 0;
-    for (int w = 0; w < nwords; ++w) acc += __popc(bi[w] & bj[w]);
-    C[static_cast<size_t>(i) * Ne + j] = acc;
+    for (int w = lane; w < nwords; w += 32) acc += __popc((in_smem ? s_bi[w] : bi[w]) & bj[w]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) C[static_cast<size_t>(i) * Ne + j] = acc;
   }
 }
 
-// P = C / max C and the C_T histogram (sum of the per-chunk counts).
+// P = C / max C and the C_T histogram (sum of the per-chunk counts): every thread
+// sums a strided share of the chunks for all C_T values, then warp and block
+// reductions (integers: exact in any order).
 __global__ void __launch_bounds__(1024)
 finish_kernel(const int64_t* __restrict__ C, int Ne, float* __restrict__ P,
               const int32_t* __restrict__ chunk_hist, int nchunks, int max_ct,
               int64_t* __restrict__ ct_hist) {
   __shared__ long long s_max[32];
+  __shared__ long long s_hist[32][OCCULT_MAX_TOPK + 1];  // per warp
+  const int lane = threadIdx.x & 31;
   long long mx = 0;
   for (int i = threadIdx.x; i < Ne * Ne; i += blockDim.x) mx = max(mx, (long long)C[i]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = mx;
+  if (lane == 0) s_max[threadIdx.x >> 5] = mx;
   __syncthreads();
   if (threadIdx.x < 32) {
     mx = threadIdx.x < (blockDim.x >> 5) ? s_max[threadIdx.x] : 0;
@@ -91,10 +107,27 @@ finish_kernel(const int64_t* __restrict__ C, int Ne, float* __restrict__ P,
       P[i] = mx > 0 ? static_cast<float>(static_cast<double>(C[i]) / static_cast<double>(mx)) : 0.f;
   }
   if (ct_hist) {
+    long long loc[OCCULT_MAX_TOPK + 1];
+#pragma unroll
+    for (int c = 0; c <= OCCULT_MAX_TOPK; ++c) loc[c] = 0;
+    for (int ch = threadIdx.x; ch < nchunks; ch += blockDim.x) {
+      const int32_t* row = chunk_hist + static_cast<size_t>(ch) * (max_ct + 1);
+#pragma unroll
+      for (int c = 0; c <= OCCULT_MAX_TOPK; ++c)
+        if (c <= max_ct) loc[c] += row[c];
+    }
+#pragma unroll
+    for (int c = 0; c <= OCCULT_MAX_TOPK; ++c) {
+      long long v = loc[c];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_hist[threadIdx.x >> 5][c] = v;
+    }
+    __syncthreads();
     for (int c = threadIdx.x; c <= max_ct; c += blockDim.x) {
-      long long s = 0;
-      for (int ch = 0; ch < nchunks; ++ch) s += chunk_hist[static_cast<size_t>(ch) * (max_ct + 1) + c];
-      ct_hist[c] = s;
+      long long v = 0;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) v += s_hist[w][c];
+      ct_hist[c] = v;
     }
   }
 }
@@ -131,7 +164,8 @@ int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t*
     else OCCULT_BITSET_LAUNCH(4);
 #undef OCCULT_BITSET_LAUNCH
   }
-  pair_count_kernel<<<ds.n_experts, 256, 0, ctx.stream>>>(bits, ds.n_experts, nwords, C);
+  pair_count_kernel<<<ds.n_experts, kPairWarps * 32, 0, ctx.stream>>>(bits, ds.n_experts, nwords,
+                                                                       C);
   finish_kernel<<<1, 1024, 0, ctx.stream>>>(C, ds.n_experts, P, chunk_hist, nwords, max_ct,
                                             chunk_hist ? ct_hist : nullptr);
   return cuda_status(cudaGetLastError());
