@@ -210,6 +210,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y), "r"(bar_cluster) : "memory");
 }
+// 5-D tiled TMA load into this CTA's shared memory, complete_tx to an mbarrier of
+// either CTA of the pair.
+__device__ __forceinline__ void tma_load_5d_pair(void* smem_dst, const CUtensorMap* map, int c0,
+                                                 int c1, int c2, int c3, int c4,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(smem_u32(smem_dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+         "r"(bar_cluster) : "memory");
+}
 // One arrival, with cluster-scope release, on an mbarrier of another CTA.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cluster)

@@ -13,13 +13,16 @@
 // (or, for weight gradients, the 64-row K blocks of that segment), scheduled by a
 // persistent kernel.
 //
-// The forward and dgrad GEMMs (A K-major, gathered or plain; B a plain matrix)
-// run on CTA pairs (2-CTA clusters, one CTA per SM): tcgen05.mma.cta_group::2
-// computes a 256 x 256 tile, rows 0..127 in the even CTA, 128..255 (the
-// segment's next M tile) in the odd one; each CTA stages its own 128 A rows and
-// half of the 256 B rows, so a 64-deep k block moves 32 KB into each SM instead
-// of 48 KB and six stages fit.  The weight gradients (gathered MN-major operands)
-// run one 128 x 256 tile per CTA with four 48 KB stages.
+// The forward, dgrad and weight-gradient GEMMs run on CTA pairs (2-CTA
+// clusters, one CTA per SM) when the segments are long enough:
+// tcgen05.mma.cta_group::2 computes a 256 x 256 tile, rows 0..127 in the even
+// CTA, 128..255 (the segment's next M tile) in the odd one; each CTA stages its
+// own 128 A rows and half of the 256 B rows, so a 64-deep k block moves 32 KB into
+// each SM instead of 48 KB and six stages fit.  The routed forward GEMMs swap the
+// operands (weights on the MMA's M, the segment's rows on its N, a runtime N of
+// the unit's rows rounded up to 16), so a segment's last unit carries at most 15
+// padding rows instead of up to 255.  Short segments (decode) run one 128 x 256
+// tile per CTA with four 48 KB stages.
 //
 // CTA = 10 warps, plus 4 when an operand is gathered; warp-specialised:
 //   warp 0       TMA producer for every operand held as a plain 2-D matrix.
@@ -64,9 +67,11 @@ constexpr uint32_t kTmemCols = 512;
 // shared memory that holds four 48 KB stages of a single CTA.
 // The forward SwiGLU epilogue stores straight from registers and needs no
 // staging buffer: a pair running it takes that 32 KB as a seventh stage.
-__host__ __device__ constexpr bool epi_staged(int epi) { return epi != EPI_SWIGLU; }
-__host__ __device__ constexpr int stages_for(bool pair, int epi = EPI_F32) {
-  return pair ? (epi_staged(epi) ? 6 : 7) : 4;
+__host__ __device__ constexpr bool epi_staged(int epi, bool swap = false) {
+  return swap || epi != EPI_SWIGLU;
+}
+__host__ __device__ constexpr int stages_for(bool pair, int epi = EPI_F32, bool swap = false) {
+  return pair ? (epi_staged(epi, swap) ? 6 : 7) : 4;
 }
 __host__ __device__ constexpr int b_stage_bytes(bool pair) { return pair ? kBTileBytes / 2 : kBTileBytes; }
 __host__ __device__ constexpr int stage_bytes(bool pair) { return kATileBytes + b_stage_bytes(pair); }
@@ -96,9 +101,9 @@ struct SmemTail {
 // to 128 bytes so that the 16-byte accesses stay aligned), when staged
 constexpr int kTailBytes = (static_cast<int>(sizeof(SmemTail)) + 127) & ~127;
 constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
-__host__ __device__ constexpr int smem_bytes(bool pair, int epi) {
-  return 1024 /*alignment slack*/ + stages_for(pair, epi) * stage_bytes(pair) + kTailBytes +
-         (epi_staged(epi) ? kEpiBytes : 0);
+__host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false) {
+  return 1024 /*alignment slack*/ + stages_for(pair, epi, swap) * stage_bytes(pair) + kTailBytes +
+         (epi_staged(epi, swap) ? kEpiBytes : 0);
 }
 static_assert(smem_bytes(false, EPI_F32) <= 232448 && smem_bytes(true, EPI_F32) <= 232448 &&
               smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448,
@@ -146,16 +151,26 @@ struct TileInfo {
   int nt;       // N tile
   int k0, k1;   // wgrad: EPD rows [k0, k1) reduced over
   int kb;       // k blocks
+  int t0;       // swapped: the unit's first EPD row (its tokens are the MMA's N)
+  int urows;    // swapped: the unit's rows (<= 256)
+  int nmma;     // swapped: the MMA's N, urows rounded up to 16 (each CTA holds half)
 };
 
 // Tile tau of the schedule.  For a CTA pair tau is a unit of
 // two consecutive M tiles of one segment and `rank` picks one; a segment with an
 // odd number of M tiles ends with a unit whose second tile has no rows (it
 // repeats the first tile's rows and stores nothing).
-template <bool WGRAD, bool PAIR>
+//
+// Swapped (SWAP) units put the weights on the MMA's M side (256 weight rows, 128
+// in each CTA) and the unit's EPD rows on its N side: N is the unit's row count
+// rounded up to 16 (each CTA holds half of the rows), so a segment's last unit
+// computes no more than 15 padding rows.  m0 / rows are then this CTA's half of
+// the rows (m0 = t0 when that half is empty), nt the weight block.
+template <bool WGRAD, bool PAIR, bool SWAP = false>
 __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const int* mt_off,
                                                 int rank) {
   TileInfo ti;
+  ti.t0 = ti.urows = ti.nmma = 0;
   if (WGRAD) {
     // a pair's unit is two consecutive M tiles of the output matrix
     const int units_m = PAIR ? p.n_tiles_m / 2 : p.n_tiles_m;
@@ -179,11 +194,20 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
       if (mt_off[mid] <= mt) lo = mid; else hi = mid;
     }
     ti.seg = lo;
-    ti.m0 = seg_at(p, lo) + (PAIR ? 2 * (mt - mt_off[lo]) + rank : mt - mt_off[lo]) * BM;
-    ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
-    if (PAIR && ti.rows <= 0) {
-      ti.m0 -= BM;
-      ti.rows = 0;
+    if (SWAP) {
+      ti.t0 = seg_at(p, lo) + (mt - mt_off[lo]) * (2 * BM);
+      ti.urows = min(2 * BM, seg_at(p, lo + 1) - ti.t0);
+      ti.nmma = (ti.urows + 15) & ~15;
+      const int half = ti.nmma / 2;
+      ti.rows = max(0, min(half, ti.urows - rank * half));
+      ti.m0 = ti.rows > 0 ? ti.t0 + rank * half : ti.t0;
+    } else {
+      ti.m0 = seg_at(p, lo) + (PAIR ? 2 * (mt - mt_off[lo]) + rank : mt - mt_off[lo]) * BM;
+      ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
+      if (PAIR && ti.rows <= 0) {
+        ti.m0 -= BM;
+        ti.rows = 0;
+      }
     }
     ti.k0 = ti.k1 = 0;
     ti.kb = p.K / BK;
@@ -265,14 +289,19 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 
 namespace {
 
-template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
+template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
   static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
                 "paired forward / dgrad GEMMs take A K-major and B a plain matrix");
   static_assert(!(WGRAD && (!op_mn(AM) || !op_mn(BMODE))), "weight gradients are MN-major");
-  constexpr int kStages = stages_for(PAIR, EPI);
+  static_assert(!SWAP || (PAIR && !WGRAD && !op_mn(AM) && BMODE == OP_TMA_K &&
+                          (EPI == EPI_SWIGLU || EPI == EPI_F32 || EPI == EPI_F32_RED)),
+                "swapped units: paired forward GEMMs with K-major rows and weights");
+  // Swapped: the stage's first 16 KB hold this CTA's 128 weight rows (the MMA's
+  // A), the next 16 KB its half of the unit's rows (the MMA's B).
+  constexpr int kStages = stages_for(PAIR, EPI, SWAP);
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
   constexpr bool kGather = op_gathered(AM) || op_gathered(BMODE);
@@ -349,7 +378,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int tau = unit0; tau < total && ok; tau += n_units) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       const int n0 = ti.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -359,7 +388,24 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
           // K row of an MN-major operand: weight rows (dgrad) or EPD rows (wgrad)
           const int krow = WGRAD ? ti.k0 + kb * BK : static_cast<int>(ti.grp * p.b_group_rows) + kb * BK;
-          if (PAIR) {
+          if (SWAP) {
+            // this CTA's 128 weight rows of the unit's 256 (SwiGLU: 64 gate rows
+            // and the 64 up rows of the same units) and 128 rows of its half of
+            // the unit's rows (only the first nmma/2 are read by the MMA)
+            if (leader) mbar_arrive_expect_tx(bar, kTmaBytes);
+            const uint32_t lbar = full_lead + stage * 8;
+            if (EPI == EPI_SWIGLU) {
+              // TMEM lane quarter q holds 16 gate rows and the 16 up rows of the
+              // same intermediate units, so that one warp's epilogue sees both:
+              // one 5-D box (K, 16 rows, gate/up, 4 groups of 16 units, expert)
+              tma_load_5d_pair(sa, &tmB, kb * BK, 0, 0, (ti.nt * (BN / 2) + rank * 64) / 16, ti.grp,
+                               lbar);
+            } else {
+              const int wrow = static_cast<int>(ti.grp * p.b_group_rows) + ti.nt * BN + rank * BM;
+              tma_load_2d_pair(sa, &tmB, kb * BK, wrow, lbar);
+            }
+            if (AM == OP_TMA_K) tma_load_2d_pair(sb, &tmA, kb * BK, ti.m0, lbar);
+          } else if (PAIR) {
             // this CTA's A rows and its half of the B tile (SwiGLU: the gate rows
             // in the even CTA, the up rows in the odd one), all counted on the
             // even CTA's barrier
@@ -421,13 +467,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       int it = 0;
       bool ok = true;
       for (int tau = unit0; tau < total && ok; tau += n_units, ++it) {
-        const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!(PAIR ? mbar_wait_cluster(&tail->tempty[a], aph ^ 1u, abort_flag)
                    : mbar_wait(&tail->tempty[a], aph ^ 1u, abort_flag))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tbase + a * BN;
+        const uint32_t idesc = SWAP ? idesc_bf16_f32(2 * BM, ti.nmma) : kIdesc;
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!(PAIR ? mbar_wait_cluster(&tail->full[stage], phase, abort_flag)
                      : mbar_wait(&tail->full[stage], phase, abort_flag))) { ok = false; break; }
@@ -441,7 +488,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           for (int kk = 0; kk < BK / 16; ++kk) {
             if (PAIR)
               tc_mma_f16_pair(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
-                              kIdesc, (kb | kk) != 0);
+                              idesc, (kb | kk) != 0);
             else
               tc_mma_f16(d_tmem, operand_desc<op_mn(AM)>(sa, kk), operand_desc<op_mn(BMODE)>(sb, kk),
                          kIdesc, (kb | kk) != 0);
@@ -469,7 +516,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t phase = 0;
       bool ok = true;
       for (int tau = unit0; tau < total && ok; tau += n_units) {
-        const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&tail->gfull[stage], phase, abort_flag)) { ok = false; break; }
           fence_proxy_async_smem();
@@ -491,7 +538,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int it = 0;
     bool ok = true;
     for (int tau = unit0; tau < total; tau += n_units, ++it) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!mbar_wait(&tail->tfull[a], aph, abort_flag)) { ok = false; break; }
@@ -504,7 +551,85 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes) +
                        (warp - kEpiWarp0) * 32 * 32;
       uint32_t v0[32], v1[32];
-      if (EPI == EPI_SWIGLU) {
+      if (SWAP) {
+        // TMEM columns are the unit's rows t0 + c (nmma of them), lanes this CTA's
+        // weight rows; each warp takes the 32-column chunks of its half
+        if (EPI == EPI_SWIGLU) {
+          // lanes 0..15: gate rows of intermediate units i0 .. i0+15, lanes 16..31:
+          // their up rows; after one exchange each lane holds G and U of one unit
+          // for 16 of the chunk's columns (lanes < 16 the first 16)
+          const int i0 = ti.nt * (BN / 2) + rank * 64 + quarter * 16;
+          const int li = lane & 15;
+          const bool hi = lane >= 16;
+          __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out);
+          uint16_t* hb = reinterpret_cast<uint16_t*>(ebuf);  // [32 columns][16 units]
+          // a last weight block past N_out (N_out % 128 != 0) leaves quarters idle
+#pragma unroll 1
+          for (int c = half * 32; c < (i0 < p.N_out ? ti.nmma : 0); c += 64) {
+            tmem_ld32(t_row + c, v0);
+            tmem_ld_wait();
+            const int col_l = c + lane;
+            const float gl = (col_l < ti.urows && p.row_gate) ? p.row_gate[ti.t0 + col_l] : 1.0f;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              const uint32_t send = hi ? v0[t] : v0[16 + t];
+              const float recv = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+              const int col = hi ? 16 + t : t;
+              const float G = hi ? recv : __uint_as_float(v0[t]);
+              const float U = hi ? __uint_as_float(v0[16 + t]) : recv;
+              const float gj = __shfl_sync(0xffffffffu, gl, col);
+              const float hv = gj * silu_f(G) * U;
+              hb[col * 16 + li] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+            }
+            __syncwarp();
+            // 32 rows of 32 bytes: two 16-byte chunks a row
+#pragma unroll
+            for (int it2 = 0; it2 < 2; ++it2) {
+              const int q = it2 * 32 + lane;
+              const int r = q >> 1, c2 = q & 1;
+              if (c + r < ti.urows)
+                st_v4(hout + (ti.t0 + c + r) * p.ldo + i0 + c2 * 8,
+                      *reinterpret_cast<const uint4*>(hb + r * 16 + c2 * 8));
+            }
+            __syncwarp();
+          }
+        } else {
+          // fp32 rows: lanes are 32 output columns, transposed through shared
+          // memory so that each row's 128 bytes leave as 16-byte vectors (8 lanes
+          // a row), stored at row t0 + c (plain) or added into the token's row
+          const int d0 = ti.nt * BN + rank * BM + quarter * 32;
+          float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+          for (int c = half * 32; c < (d0 < p.N_out ? ti.nmma : 0); c += 64) {
+            const int col_l = c + lane;
+            int64_t dst_l = 0;
+            if (col_l < ti.urows)
+              dst_l = EPI == EPI_F32_RED ? p.out_tok[p.out_src[ti.t0 + col_l]] : ti.t0 + col_l;
+            tmem_ld32(t_row + c, v0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              ebuf[j * 32 + ((((lane >> 2) ^ (j & 7)) << 2) | (lane & 3))] = v0[j];
+            __syncwarp();
+#pragma unroll
+            for (int it2 = 0; it2 < 8; ++it2) {
+              const int r = it2 * 4 + (lane >> 3), c4 = lane & 7;
+              const int64_t dst = __shfl_sync(0xffffffffu, dst_l, r);
+              if (c + r < ti.urows) {
+                const uint4 u = *reinterpret_cast<const uint4*>(ebuf + r * 32 + ((c4 ^ (r & 7)) << 2));
+                float* o = out + dst * p.ldo + d0 + c4 * 4;
+                if (EPI == EPI_F32_RED)
+                  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                               :: "l"(o), "f"(__uint_as_float(u.x)), "f"(__uint_as_float(u.y)),
+                                  "f"(__uint_as_float(u.z)), "f"(__uint_as_float(u.w)) : "memory");
+                else
+                  st_v4(o, u);
+              }
+            }
+            __syncwarp();
+          }
+        }
+      } else if (EPI == EPI_SWIGLU) {
         const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
         const int col0 = ti.nt * (BN / 2);
 #pragma unroll 1
@@ -650,7 +775,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int tau = unit0; tau < total && ok; tau += n_units) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
       // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
       // at r*128 + ((c ^ (r % 8)) * 16)
@@ -687,7 +812,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint8_t* sa = smem + stage * kStageBytes;
         if (AM == OP_GATHER_K) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cp_async_16(sa + dst_k[i], src_k[i] + kb * BK);
+          for (int i = 0; i < 8; ++i) cp_async_16((SWAP ? sa + kATileBytes : sa) + dst_k[i], src_k[i] + kb * BK);
         } else {
           // MN-major rows (weight gradients): K row k of the stage is EPD row
           // k0 + kb*64 + k; chunk c covers MN elements 8c..8c+7 of the tile; rows
@@ -768,6 +893,25 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint3
   return r == CUDA_SUCCESS ? OCCULT_OK : OCCULT_ERR_CUDA;
 }
 
+// SwiGLU weights [Ne, 2I, K] (gate rows then up rows of every expert) as a 5-D
+// tensor (K, 16 rows, gate/up, I/16 groups, expert); box (64, 16, 2, 4, 1):
+// 4 groups of 16 gate rows each followed by the same units' up rows.
+int make_map_swiglu5d(CUtensorMap* m, const void* base, int64_t n_exp, int64_t I, int64_t K) {
+  auto fn = encode_fn();
+  if (!fn || I % 64 != 0) return fn ? OCCULT_ERR_UNSUPPORTED : OCCULT_ERR_CUDA;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(K), 16, 2, static_cast<cuuint64_t>(I / 16),
+                              static_cast<cuuint64_t>(n_exp)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(I * K) * 2,
+                                 static_cast<cuuint64_t>(16 * K) * 2,
+                                 static_cast<cuuint64_t>(2 * I * K) * 2};
+  const cuuint32_t box[5] = {BK, 16, 2, 4, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? OCCULT_OK : OCCULT_ERR_CUDA;
+}
+
 // Tensor map of one operand: K-major tiles are 64 K columns x 128 or 256 rows;
 // MN-major tiles are loaded as 64 MN columns x 64 K rows.
 int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t cols,
@@ -778,13 +922,13 @@ int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t
   return make_map(m, ptr, rows, cols, BK, BK);
 }
 
-template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR>
+template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP = false>
 int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb, const Params& p) {
-  auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR>;
+  auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR, SWAP>;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(threads_for(AM, BMODE));
-  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI);
+  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP);
   cfg.stream = ctx.stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
@@ -798,7 +942,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   static int n_pairs = 0;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_bytes(PAIR, EPI));
+                                    smem_bytes(PAIR, EPI, SWAP));
     if (PAIR && attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
       attr_err = cudaOccupancyMaxActiveClusters(&n_pairs, kern, &cfg);
@@ -829,10 +973,25 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   const int64_t avg_rows = g.seg_off ? g.max_rows / g.n_seg : g.max_rows;
   const bool pair = g.wgrad ? g.M_total % (2 * BM) == 0
                             : !op_gathered(g.b_mode) && avg_rows >= 2 * BM;
+  // Paired routed forward GEMMs swap operands (weights on M, the segment's rows on
+  // N) so that a segment's last unit computes its rows rounded up to 16, not to
+  // 256 (decode-sized segments stay on single CTAs: a swapped pair measured
+  // slower there, 164 vs 135 us for the DeepSeek decode up-projection).
+  const int epi_eff = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED : g.epi;
+  const bool swap = pair && !g.wgrad && g.seg_off && g.b_mode == OP_TMA_K &&
+                    ((epi_eff == EPI_SWIGLU && g.a_mode == OP_GATHER_K && !g.gu_out) ||
+                     ((epi_eff == EPI_F32 || epi_eff == EPI_F32_RED) && g.a_mode == OP_TMA_K));
   CUtensorMap ma, mb;
   int rc = operand_map(&ma, am, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
-  rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols, (pair || g.epi == EPI_SWIGLU) ? BN / 2 : BN);
+  // B (weights) boxes: pairs and SwiGLU halves 128 rows, single CTAs 256;
+  // swapped SwiGLU a 5-D view of [Ne, 2, I/16, 16, d] taking 4 groups of 16 gate
+  // rows and their 16 up rows at once
+  if (swap && g.epi == EPI_SWIGLU)
+    rc = make_map_swiglu5d(&mb, g.B, g.n_groups, g.N_out, g.b_cols);
+  else
+    rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols,
+                     (pair || g.epi == EPI_SWIGLU) ? BN / 2 : BN);
   if (rc) return rc;
   Params p{};
   p.seg_off = g.seg_off;
@@ -861,12 +1020,20 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.out_src = g.out_src;
   p.out_tok = g.out_tok;
   p.dev_err = ctx.dev_err;
-  const int bm = g.b_mode, ep = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED : g.epi;
+  const int bm = g.b_mode, ep = epi_eff;
   // the instantiations the layer uses
 #define OCCULT_ROWS_GEMM(AM_, BM_, EP_)                                                 \
   if (am == AM_ && bm == BM_ && ep == EP_)                                             \
     return pair ? launch_tc<AM_, BM_, EP_, false, true>(ctx, ma, mb, p)                \
                 : launch_tc<AM_, BM_, EP_, false, false>(ctx, ma, mb, p);
+  if (swap) {
+    if (am == OP_GATHER_K && ep == EPI_SWIGLU)
+      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false, true, true>(ctx, ma, mb, p);
+    if (am == OP_TMA_K && ep == EPI_F32)
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false, true, true>(ctx, ma, mb, p);
+    if (am == OP_TMA_K && ep == EPI_F32_RED)
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32_RED, false, true, true>(ctx, ma, mb, p);
+  }
   if (!g.wgrad) {
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_K, EPI_SWIGLU)     // up-projection
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_SWIGLU)        // shared experts' up-projection
