@@ -429,33 +429,56 @@ def run_ours(args, cfg, world, rank, local):
     n_sfd = int(moe.counts[0].item())
 
     # ---- end to end through the public API with host buffers ----------------
+    # Every step copies its inputs from pinned host memory and reads its output
+    # back; the copies run on their own streams, double-buffered, so that step
+    # i+1's inputs arrive and step i-1's output leaves while step i computes.
     x_h = x.cpu().pin_memory()
     lg_h = logits.cpu().pin_memory()
     y_h = torch.empty(T, d, dtype=torch.float32).pin_memory()
-    x_d = torch.empty_like(x)
-    lg_d = torch.empty_like(logits)
-
     dy_h = dy.cpu().pin_memory() if train else None
-    dy_d = torch.empty_like(dy) if train else None
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    lg_d = [torch.empty_like(logits) for _ in range(2)]
+    y_d = [torch.empty(T, d, dtype=torch.float32, device=dev) for _ in range(2)]
+    dy_d = [torch.empty_like(dy) for _ in range(2)] if train else None
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        y = moe.forward(lg_d, x_d, stream)
-        y_h.copy_(y, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        s_in.wait_event(ev_done[b])          # buffer b's previous step has finished
+        with torch.cuda.stream(s_in):
+            x_d[b].copy_(x_h, non_blocking=True)
+            lg_d[b].copy_(lg_h, non_blocking=True)
+            if train:
+                dy_d[b].copy_(dy_h, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])         # y_d[b] has left for the host
+        moe.forward(lg_d[b], x_d[b], stream, out=y_d[b])
         if train:
-            dy_d.copy_(dy_h, non_blocking=True)
-            moe.backward(dy_d, stream)
+            moe.backward(dy_d[b], stream)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            y_h.copy_(y_d[b], non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(max(3, args.warmup // 4)):
-        e2e_step()
+    n_e2e_warm = max(3, args.warmup // 4)
+    for i in range(n_e2e_warm):
+        e2e_step(i)
     n_e2e = max(10, args.steps // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     e0.record(stream)
-    for _ in range(n_e2e):
-        e2e_step()
+    s_in.wait_stream(stream)                 # the first copy starts after the clock does
+    for i in range(n_e2e):
+        e2e_step(n_e2e_warm + i)
+    stream.wait_event(ev_out[(n_e2e_warm + n_e2e - 1) & 1])   # the last output is on the host
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)

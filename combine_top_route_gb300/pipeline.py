@@ -201,9 +201,18 @@ class OccultMoE:
         occult_combine_sfd(ds, self.y_send, self.brim0_send, out, y_shared=y_shared,
                            stream=stream)
 
-    def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
-        """y = MoE(x) (fp32 [T, d]) for router logits ``logits`` [T, Ne] (fp32) and x [T, d]."""
+    def forward(self, logits: torch.Tensor, x: torch.Tensor, stream=None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """y = MoE(x) (fp32 [T, d]) for router logits ``logits`` [T, Ne] (fp32) and x [T, d].
+
+        ``out``: an fp32 [T, d] CUDA tensor to write y into (default: the layer's own
+        buffer), e.g. one of two alternating outputs whose device-to-host copy
+        overlaps the next call."""
         ds = self.desc
+        y = self.y if out is None else out
+        if out is not None and (out.dtype != torch.float32 or out.numel() < ds.T * ds.d
+                                or not out.is_contiguous()):
+            raise ValueError("out must be a contiguous fp32 tensor of T * d elements")
         self.route_and_index(logits, stream)
         self._scatter(x, self.x_sfd, self.sfd_tok, stream)
         occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
@@ -212,18 +221,18 @@ class OccultMoE:
             # the shared experts write y, the routed experts' rows are added to it
             if ds.n_shared:
                 occult_shared_ffn(ds, x, self.w["ws1"], self.w["ws2"], self.w.get("w_sg"),
-                                  self.h_s, self.s_gate, self.y, stream)
+                                  self.h_s, self.s_gate, y, stream)
             occult_expert_down_merge(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
-                                     self.epd_src, self.sfd_tok, self.y,
+                                     self.epd_src, self.sfd_tok, y,
                                      zero_y=not ds.n_shared, stream=stream)
-            return self.y
+            return y
         occult_expert_down(ds, self.h_epd, self.exp_off, self.placement, self.w["w2"],
                            self.y_epd, stream)
         if ds.n_shared:
             occult_shared_ffn(ds, x, self.w["ws1"], self.w["ws2"], self.w.get("w_sg"), self.h_s,
                               self.s_gate, self.y_s, stream)
-        self._merge(self.y_epd, self.y, self.y_s, stream)
-        return self.y
+        self._merge(self.y_epd, y, self.y_s, stream)
+        return y
 
     @property
     def launches_per_backward(self) -> int:
