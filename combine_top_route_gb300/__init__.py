@@ -74,6 +74,7 @@ _SIGNATURES = {
     "occult_check_desc": (ctypes.c_int, [_D]),
     "occult_workspace_size": (ctypes.c_int, [_D, _I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
     "occult_device_error": (ctypes.c_int, [ctypes.POINTER(_I32)]),
+    "occult_selftest_wait": (ctypes.c_int, [_I32, ctypes.c_int64, _VP]),
     "occult_place": (ctypes.c_int, [_VP, _I32, _I32, _VP, _VP]),
     "occult_route": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_route_similarity": (ctypes.c_int, [_D] + [_VP] * 8),
@@ -173,6 +174,12 @@ def workspace_size(desc: occult_desc_t, op: int, n_tok: int = 0) -> int:
     n = ctypes.c_size_t(0)
     _call("occult_workspace_size", ctypes.byref(desc), op, n_tok, ctypes.byref(n))
     return n.value
+
+
+def occult_selftest_wait(complete: bool, limit_ns: int, stream=None) -> None:
+    """One bounded device wait that gives up (complete=False) or completes (see occult.h)."""
+    _call("occult_selftest_wait", int(bool(complete)), ctypes.c_int64(int(limit_ns)),
+          _stream(stream))
 
 
 def occult_place(C, n_vdev: int):

@@ -144,6 +144,13 @@ int occult_device_error(int32_t* code) {
   return OCCULT_OK;
 }
 
+int occult_selftest_wait(int32_t complete, int64_t limit_ns, occult_stream_t stream) {
+  OCCULT_REQUIRE(complete == 0 || complete == 1);
+  OCCULT_REQUIRE(limit_ns > 0 && limit_ns <= static_cast<int64_t>(kWaitLimitNs));
+  OCCULT_CTX(stream);
+  return launch_selftest_wait(ctx, complete, static_cast<uint64_t>(limit_ns));
+}
+
 int occult_route(const occult_desc_t* desc, const float* logits, const int32_t* expert_to_vdev,
                  int32_t* ids, float* gates, uint32_t* vmask, occult_stream_t stream) {
   int rc = check(desc);

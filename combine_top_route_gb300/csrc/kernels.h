@@ -114,6 +114,9 @@ int launch_gate_grad(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_
                      const int32_t* brim1, const int32_t* exp_off, const float* dg_epd,
                      float* dgates);
 
+// one bounded wait that nothing completes (complete = 0) or that completes
+int launch_selftest_wait(const LaunchCtx& ctx, int complete, uint64_t limit_ns);
+
 // s[t] = sigmoid(w . x_t) for the shared-expert gate
 int launch_shared_gate(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
                        const void* w_sg, float* s_gate);

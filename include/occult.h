@@ -114,6 +114,18 @@ int occult_workspace_size(const occult_desc_t* desc, int32_t op, int32_t n_tok, 
 int occult_device_error(int32_t* code);
 
 /*
+ * occult_selftest_wait -- exercises the library's failure detection; the paper
+ * has no counterpart.  Every pipelined kernel waits on its barriers with a time
+ * limit, after which it latches OCCULT_ERR_DEVICE_TIMEOUT (read with
+ * occult_device_error) and returns, leaving the context usable.  This launches
+ * one such wait on a barrier that nothing completes (complete = 0), which must
+ * give up after limit_ns nanoseconds (0 < limit_ns <= 2e9) and latch the error,
+ * or that the kernel completes itself (complete = 1), which must not.  It reads
+ * and writes no caller memory.
+ */
+int occult_selftest_wait(int32_t complete, int64_t limit_ns, occult_stream_t stream);
+
+/*
  * occult_place -- Algorithm 1 (Sec. 3.2), HOST function, run once offline.
  *   C               host int64 [Ne, Ne] co-activation counts (Eq. 3).
  *   placement       host int32 [Nd, Ne/Nd] out: device d's experts in the order
