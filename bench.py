@@ -1,13 +1,16 @@
 """Throughput of the Occult MoE layer (tokens/s) on GB300, with roofline and CPU baseline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+                    [--merge atomic|ordered] [--tokens T]
 
 One step = one forward of the whole layer path (route -> BRIM build -> dispatch
--> grouped SwiGLU expert GEMMs -> two-stage combine) over one batch of the
-OLMoE-shaped bf16 workload (T=4096, d=2048, Ne=64, k=8, I=1024, Nd=8 virtual
+-> grouped SwiGLU expert GEMMs -> merge of the expert outputs) over one batch of
+the OLMoE-shaped bf16 workload (T=4096, d=2048, Ne=64, k=8, I=1024, Nd=8 virtual
 devices, Algorithm 1 placement from a 16384-token profiling batch).  Inputs are
 resident in HBM when the timed region starts; they are larger than L2 (the
-expert weights alone are 805 MB), so no L2 flush is needed between steps.
+expert weights alone are 805 MB), so no L2 flush is needed between steps.  The
+end-to-end figure runs the same steps through OccultMoE.forward with the inputs
+copied from pinned host memory and the output read back every step.
 
 Under torchrun (N > 1) every rank runs its own replica of the layer on its own
 batch (the layer's batches are independent problems; no data-path collective),
