@@ -324,10 +324,10 @@ int occult_expert_down_merge(const occult_desc_t* desc, const void* h_epd, const
   OCCULT_REQUIRE(desc->T == 0 || (h_epd && epd_src && sfd_tok && y));
   OCCULT_CTX(stream);
   if (desc->T == 0) return OCCULT_OK;
-  if (zero_y &&
-      cudaMemsetAsync(y, 0, static_cast<size_t>(desc->T) * desc->d * sizeof(float), ctx.stream) !=
-          cudaSuccess)
-    return OCCULT_ERR_CUDA;
+  if (zero_y) {
+    rc = launch_zero_f32(ctx, static_cast<float*>(y), static_cast<size_t>(desc->T) * desc->d);
+    if (rc) return rc;
+  }
   return expert_down(ctx, desc, h_epd, exp_off, placement, w2, y, epd_src, sfd_tok);
 }
 
@@ -414,10 +414,10 @@ static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
-  if (sfd_tok && desc->T > 0 &&
-      cudaMemsetAsync(dx_out, 0, static_cast<size_t>(desc->T) * desc->d * sizeof(float),
-                      ctx.stream) != cudaSuccess)
-    return OCCULT_ERR_CUDA;
+  if (sfd_tok && desc->T > 0) {
+    rc = launch_zero_f32(ctx, dx_out, static_cast<size_t>(desc->T) * desc->d);
+    if (rc) return rc;
+  }
   if (desc->T == 0) {
     // no rows: every weight gradient is zero
     const size_t n1 = static_cast<size_t>(desc->n_experts) * 2 * desc->inter * desc->d;

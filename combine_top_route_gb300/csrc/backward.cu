@@ -11,6 +11,8 @@ namespace {
 
 __global__ void __launch_bounds__(256)
 dg_reduce_kernel(const float* __restrict__ part, int rows, int n_part, float* __restrict__ dg) {
+  pdl_wait();
+  pdl_trigger();
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
     float s = 0.f;
     for (int i = 0; i < n_part; ++i) s += part[static_cast<size_t>(r) * n_part + i];
@@ -26,6 +28,8 @@ gate_grad_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ pl
                  const int32_t* __restrict__ brim1, const int32_t* __restrict__ exp_off,
                  const float* __restrict__ dg_epd, int T, int k, int Ne, int n_loc,
                  float* __restrict__ dgates) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_slot_of[OCCULT_MAX_EXPERTS];
   for (int s = threadIdx.x; s < Ne; s += blockDim.x) s_slot_of[placement[s]] = s;
   __syncthreads();
@@ -56,7 +60,7 @@ size_t expert_bwd_ws_bytes(const occult_desc_t& ds) {
 
 int launch_dg_reduce(const LaunchCtx& ctx, const float* part, int rows, int n_part, float* dg) {
   if (rows == 0) return OCCULT_OK;
-  dg_reduce_kernel<<<blocks_for(ctx, rows), 256, 0, ctx.stream>>>(part, rows, n_part, dg);
+  launch_pdl(dg_reduce_kernel, blocks_for(ctx, rows), 256, 0, ctx.stream, part, rows, n_part, dg);
   return cuda_status(cudaGetLastError());
 }
 
@@ -66,7 +70,7 @@ int launch_gate_grad(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_
                      float* dgates) {
   const int64_t n = static_cast<int64_t>(ds.T) * ds.top_k;
   if (n == 0) return OCCULT_OK;
-  gate_grad_kernel<<<blocks_for(ctx, n), 256, 0, ctx.stream>>>(
+  launch_pdl(gate_grad_kernel, blocks_for(ctx, n), 256, 0, ctx.stream,
       ids, placement, brim0, seg_off, brim1, exp_off, dg_epd, ds.T, ds.top_k, ds.n_experts,
       ds.n_experts / ds.n_vdev, dgates);
   return cuda_status(cudaGetLastError());
@@ -85,6 +89,8 @@ __global__ void __launch_bounds__(256)
 router_grad_kernel(const float* __restrict__ logits, const int32_t* __restrict__ gate_ids,
                    const float* __restrict__ dgates, int T, int Ne, int k, int renorm,
                    float* __restrict__ dlogits) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const float NEG = -__int_as_float(0x7f800000);
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
@@ -155,7 +161,7 @@ int launch_router_grad(const LaunchCtx& ctx, const occult_desc_t& ds, const floa
   int blocks = (ds.T + 7) / 8;
   if (blocks > ctx.num_sms * 16) blocks = ctx.num_sms * 16;
 #define OCCULT_RGRAD_LAUNCH(PL)                                                            \
-  router_grad_kernel<PL><<<blocks, 256, 0, ctx.stream>>>(logits, gate_ids, dgates, ds.T,   \
+  launch_pdl(router_grad_kernel<PL>, blocks, 256, 0, ctx.stream, logits, gate_ids, dgates, ds.T,   \
                                                           ds.n_experts, ds.top_k, ds.renorm, \
                                                           dlogits)
   if (ds.n_experts <= 32) OCCULT_RGRAD_LAUNCH(1);

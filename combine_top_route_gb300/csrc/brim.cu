@@ -65,6 +65,8 @@ brim_count_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ 
                   int n_tiles, int32_t* __restrict__ cnt) {
   constexpr int NS = 64 * W64;
   __shared__ int s_slot_of[NS];
+  pdl_wait();
+  pdl_trigger();
   for (int s = threadIdx.x; s < Ne; s += blockDim.x) s_slot_of[placement[s]] = s;
   __syncthreads();
   const int lane = threadIdx.x & 31;
@@ -98,6 +100,8 @@ brim_scan_kernel(int n_tiles, int Ne, int32_t* __restrict__ cnt) {
   const int nc = ncols(Ne);
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x * kScanWarps + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (c >= nc) return;
   int32_t* col = cnt + static_cast<size_t>(c) * n_tiles;
   const bool is_max = c == nc - 1;
@@ -184,6 +188,8 @@ brim_fill_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gate
   __shared__ int s_expert[NS];
   __shared__ int s_seg[OCCULT_MAX_VDEV + 1];
   __shared__ int s_exp[OCCULT_MAX_EXPERTS + 1];
+  pdl_wait();
+  pdl_trigger();
   for (int s = threadIdx.x; s < Ne; s += blockDim.x) {
     s_slot_of[placement[s]] = s;
     s_expert[s] = placement[s];
@@ -277,12 +283,12 @@ int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32
   const int cgrid = (tiles + kWarpsPerCta - 1) / kWarpsPerCta;
   const int fgrid = (tiles * Nd + kWarpsPerCta - 1) / kWarpsPerCta;
 #define OCCULT_BRIM_COUNT(W)                                                                   \
-  brim_count_kernel<W><<<cgrid, kWarpsPerCta * 32, 0, ctx.stream>>>(ids, vmask, placement, T, k, \
-                                                                    Ne, Nd, tiles, cnt)
+  launch_pdl(brim_count_kernel<W>, cgrid, kWarpsPerCta * 32, 0, ctx.stream, ids, vmask,         \
+             placement, T, k, Ne, Nd, tiles, cnt)
 #define OCCULT_BRIM_FILL(W)                                                                    \
-  brim_fill_kernel<W><<<fgrid, kWarpsPerCta * 32, 0, ctx.stream>>>(                            \
-      ids, gates, vmask, placement, T, k, Ne, Nd, n_loc, tiles, cnt, seg_off, exp_off, counts, \
-      brim0, brim1, epd_src, epd_gate)
+  launch_pdl(brim_fill_kernel<W>, fgrid, kWarpsPerCta * 32, 0, ctx.stream, ids, gates, vmask,  \
+             placement, T, k, Ne, Nd, n_loc, tiles, cnt, seg_off, exp_off, counts, brim0,      \
+             brim1, epd_src, epd_gate)
   if (tiles == 0) {
     // no tokens: every offset and count is zero
     if (cudaMemsetAsync(seg_off, 0, (Nd + 1) * sizeof(int32_t), ctx.stream) != cudaSuccess ||
@@ -294,8 +300,8 @@ int launch_build_brim(const LaunchCtx& ctx, const occult_desc_t& ds, const int32
   if (Ne <= 64) OCCULT_BRIM_COUNT(1);
   else if (Ne <= 128) OCCULT_BRIM_COUNT(2);
   else OCCULT_BRIM_COUNT(4);
-  brim_scan_kernel<<<(ncols(Ne) + kScanWarps - 1) / kScanWarps, kScanWarps * 32, 0, ctx.stream>>>(
-      tiles, Ne, cnt);
+  launch_pdl(brim_scan_kernel, (ncols(Ne) + kScanWarps - 1) / kScanWarps, kScanWarps * 32, 0,
+             ctx.stream, tiles, Ne, cnt);
   if (Ne <= 64) OCCULT_BRIM_FILL(1);
   else if (Ne <= 128) OCCULT_BRIM_FILL(2);
   else OCCULT_BRIM_FILL(4);

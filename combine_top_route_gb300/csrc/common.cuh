@@ -26,6 +26,31 @@ static inline int cuda_status(cudaError_t e) {
   return e == cudaSuccess ? OCCULT_OK : OCCULT_ERR_CUDA;
 }
 
+// Programmatic dependent launch: a kernel launched this way may be scheduled
+// while the previous kernel of the stream finishes; it waits in pdl_wait() (the
+// first thing it does) until that kernel has completed and its writes are
+// visible, so only the launch latency overlaps.  pdl_trigger() lets the next
+// kernel be scheduled once every CTA of this one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ----------------------------------------------------------------------------
 // element access for the two layer dtypes
 // ----------------------------------------------------------------------------

@@ -27,6 +27,8 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ brim0,
                 T* __restrict__ x_sfd, int32_t* __restrict__ sfd_tok) {
   const int lane = threadIdx.x & 31;
   const int nvec = D / Vec16<T>::N;
+  pdl_wait();
+  pdl_trigger();
   for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < ntok; t += gridDim.x * kWarps) {
     const uint32_t vm = vmask[t];
     // SFD rows of this token, one per device it uses (at most 32)
@@ -63,6 +65,8 @@ combine_fused_kernel(const float* __restrict__ y_epd, const int32_t* __restrict_
                      const int32_t* __restrict__ exp_off, const float* __restrict__ y_shared,
                      int ntok, int Nd, int n_loc, int D, float* __restrict__ y_sfd,
                      float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VN = 4;
   constexpr int kChunk = 8;  // EPD rows loaded per pass (all of them for k <= 8)
   __shared__ int s_rows[kWarps][OCCULT_MAX_TOPK];
@@ -159,6 +163,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 combine_sfd_kernel(const float* __restrict__ y_sfd, const int32_t* __restrict__ brim0,
                    const float* __restrict__ y_shared, int ntok, int Nd, int D,
                    float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VN = 4;
   constexpr int kChunk = 8;
   __shared__ int s_rows[kWarps][OCCULT_MAX_VDEV];
@@ -203,6 +209,18 @@ combine_sfd_kernel(const float* __restrict__ y_sfd, const int32_t* __restrict__ 
   }
 }
 
+// y = 0 before a merge by atomic additions (a kernel rather than a memset, so
+// that it joins the stream's chain of dependent launches).
+__global__ void __launch_bounds__(256)
+zero_f32_kernel(float4* __restrict__ p, size_t n4) {
+  pdl_wait();
+  pdl_trigger();
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = z;
+}
+
 int grid_for(const LaunchCtx& ctx, int ntok) {
   int blocks = (ntok + kWarps - 1) / kWarps;
   const int cap = ctx.num_sms * 16;
@@ -216,14 +234,27 @@ int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x
   if (ds.T == 0) return OCCULT_OK;
   const int g = grid_for(ctx, ds.T);
   if (ds.dtype == OCCULT_BF16)
-    dispatch_kernel<__nv_bfloat16><<<g, kWarps * 32, 0, ctx.stream>>>(
-        static_cast<const __nv_bfloat16*>(x), brim0, vmask, ds.T, ds.n_vdev, ds.d,
-        static_cast<__nv_bfloat16*>(x_sfd), sfd_tok);
+    launch_pdl(dispatch_kernel<__nv_bfloat16>, g, kWarps * 32, 0, ctx.stream,
+               static_cast<const __nv_bfloat16*>(x), brim0, vmask, ds.T, ds.n_vdev, ds.d,
+               static_cast<__nv_bfloat16*>(x_sfd), sfd_tok);
   else
-    dispatch_kernel<float><<<g, kWarps * 32, 0, ctx.stream>>>(
-        static_cast<const float*>(x), brim0, vmask, ds.T, ds.n_vdev, ds.d,
-        static_cast<float*>(x_sfd), sfd_tok);
+    launch_pdl(dispatch_kernel<float>, g, kWarps * 32, 0, ctx.stream, static_cast<const float*>(x),
+               brim0, vmask, ds.T, ds.n_vdev, ds.d, static_cast<float*>(x_sfd), sfd_tok);
   return cuda_status(cudaGetLastError());
+}
+
+int launch_zero_f32(const LaunchCtx& ctx, float* p, size_t n) {
+  if (n == 0) return OCCULT_OK;
+  if (n % 4 != 0 || reinterpret_cast<uintptr_t>(p) % 16 != 0) {
+    // not a whole number of aligned vectors: the plain memset
+    return cuda_status(cudaMemsetAsync(p, 0, n * sizeof(float), ctx.stream));
+  }
+  const size_t n4 = n / 4;
+  size_t blocks = (n4 + 255) / 256;
+  const size_t cap = static_cast<size_t>(ctx.num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  return cuda_status(launch_pdl(zero_f32_kernel, static_cast<unsigned>(blocks), 256, 0, ctx.stream,
+                                reinterpret_cast<float4*>(p), n4));
 }
 
 int launch_merge_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
@@ -231,7 +262,7 @@ int launch_merge_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float*
                      const int32_t* exp_off, float* y_sfd) {
   if (ds.T == 0) return OCCULT_OK;
   const int g = grid_for(ctx, ds.T);
-  combine_fused_kernel<true><<<g, kWarps * 32, 0, ctx.stream>>>(
+  launch_pdl(combine_fused_kernel<true>, g, kWarps * 32, 0, ctx.stream,
       y_epd, brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev, ds.n_experts / ds.n_vdev,
       ds.d, y_sfd, nullptr);
   return cuda_status(cudaGetLastError());
@@ -241,7 +272,7 @@ int launch_combine_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const floa
                        const int32_t* brim0, const float* y_shared, float* y) {
   if (ds.T == 0) return OCCULT_OK;
   const int g = grid_for(ctx, ds.T);
-  combine_sfd_kernel<<<g, kWarps * 32, 0, ctx.stream>>>(y_sfd, brim0, y_shared, ds.T, ds.n_vdev,
+  launch_pdl(combine_sfd_kernel, g, kWarps * 32, 0, ctx.stream, y_sfd, brim0, y_shared, ds.T, ds.n_vdev,
                                                         ds.d, y);
   return cuda_status(cudaGetLastError());
 }
@@ -253,13 +284,13 @@ int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y
   const int g = grid_for(ctx, ds.T);
   const int n_loc = ds.n_experts / ds.n_vdev;
   if (y_sfd) {
-    combine_fused_kernel<true><<<g, kWarps * 32, 0, ctx.stream>>>(
+    launch_pdl(combine_fused_kernel<true>, g, kWarps * 32, 0, ctx.stream,
         y_epd, brim0, seg_off, brim1, exp_off, nullptr, ds.T, ds.n_vdev, n_loc, ds.d, y_sfd,
         nullptr);
-    combine_sfd_kernel<<<g, kWarps * 32, 0, ctx.stream>>>(y_sfd, brim0, y_shared, ds.T,
+    launch_pdl(combine_sfd_kernel, g, kWarps * 32, 0, ctx.stream, y_sfd, brim0, y_shared, ds.T,
                                                           ds.n_vdev, ds.d, y);
   } else {
-    combine_fused_kernel<false><<<g, kWarps * 32, 0, ctx.stream>>>(
+    launch_pdl(combine_fused_kernel<false>, g, kWarps * 32, 0, ctx.stream,
         y_epd, brim0, seg_off, brim1, exp_off, y_shared, ds.T, ds.n_vdev, n_loc, ds.d, nullptr,
         y);
   }

@@ -36,6 +36,8 @@ struct SimtParams {
 template <bool SWIGLU>
 __global__ void __launch_bounds__(256)
 grouped_gemm_f32_kernel(const SimtParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sa[TM][TK + 1];
   __shared__ float sg[TN][TK + 1];
   __shared__ float su[TN][TK + 1];
@@ -119,6 +121,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 shared_gate_kernel(const T* __restrict__ x, const T* __restrict__ w, int ntok, int D,
                    float* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < ntok; t += gridDim.x * 8) {
     float acc = 0.f;
@@ -151,8 +155,8 @@ int launch_grouped_gemm_f32(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.out_tok = g.out_tok;
   const int64_t m_tiles = (g.max_rows + TM - 1) / TM + g.n_seg;
   dim3 grid(static_cast<unsigned>(m_tiles), (g.N_out + TN - 1) / TN);
-  if (g.epi == EPI_SWIGLU) grouped_gemm_f32_kernel<true><<<grid, 256, 0, ctx.stream>>>(p);
-  else grouped_gemm_f32_kernel<false><<<grid, 256, 0, ctx.stream>>>(p);
+  if (g.epi == EPI_SWIGLU) launch_pdl(grouped_gemm_f32_kernel<true>, grid, 256, 0, ctx.stream, p);
+  else launch_pdl(grouped_gemm_f32_kernel<false>, grid, 256, 0, ctx.stream, p);
   return cuda_status(cudaGetLastError());
 }
 
@@ -162,11 +166,11 @@ int launch_shared_gate(const LaunchCtx& ctx, const occult_desc_t& ds, const void
   int blocks = (ds.T + 7) / 8;
   if (blocks > ctx.num_sms * 8) blocks = ctx.num_sms * 8;
   if (ds.dtype == OCCULT_BF16)
-    shared_gate_kernel<__nv_bfloat16><<<blocks, 256, 0, ctx.stream>>>(
+    launch_pdl(shared_gate_kernel<__nv_bfloat16>, blocks, 256, 0, ctx.stream,
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_sg), ds.T,
         ds.d, s_gate);
   else
-    shared_gate_kernel<float><<<blocks, 256, 0, ctx.stream>>>(
+    launch_pdl(shared_gate_kernel<float>, blocks, 256, 0, ctx.stream,
         static_cast<const float*>(x), static_cast<const float*>(w_sg), ds.T, ds.d, s_gate);
   return cuda_status(cudaGetLastError());
 }

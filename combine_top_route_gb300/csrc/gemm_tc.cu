@@ -293,6 +293,8 @@ template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+  pdl_wait();
+  pdl_trigger();
   static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
                 "paired forward / dgrad GEMMs take A K-major and B a plain matrix");
   static_assert(!(WGRAD && (!op_mn(AM) || !op_mn(BMODE))), "weight gradients are MN-major");
@@ -926,7 +928,7 @@ template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP = false>
 int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb, const Params& p) {
   auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR, SWAP>;
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(threads_for(AM, BMODE));
   cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP);
   cfg.stream = ctx.stream;
@@ -934,8 +936,10 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = PAIR ? attr : attr + 1;
+  cfg.numAttrs = PAIR ? 2 : 1;
   // persistent grid: one CTA per SM, or as many co-resident CTA pairs as fit
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

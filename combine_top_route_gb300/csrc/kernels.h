@@ -28,6 +28,9 @@ int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
                    const int32_t* exp_off, const float* y_shared, float* y_sfd, float* y);
 
+// p[0, n) = 0 (fp32)
+int launch_zero_f32(const LaunchCtx& ctx, float* p, size_t n);
+
 // stage one only (EPD -> SFD, y_sfd written) / stage two only (SFD -> ORI)
 int launch_merge_sfd(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                      const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,

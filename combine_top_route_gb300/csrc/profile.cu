@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256)
 bitset_kernel(const int32_t* __restrict__ ids, const uint32_t* __restrict__ vmask, int n_tok,
               int k, int Ne, int max_ct, int nwords, uint32_t* __restrict__ bits,
               int32_t* __restrict__ chunk_hist) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int nchunks = (n_tok + 31) / 32;
   for (int ch = blockIdx.x * 8 + (threadIdx.x >> 5); ch < nchunks; ch += gridDim.x * 8) {
@@ -60,6 +62,8 @@ constexpr int kPairWarps = 8;
 constexpr int kMaxSharedWords = 8192;  // 256K tokens; longer batches read global memory
 __global__ void __launch_bounds__(kPairWarps * 32)
 pair_count_kernel(const uint32_t* __restrict__ bits, int Ne, int nwords, int64_t* __restrict__ C) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t s_bi[kMaxSharedWords];
   const int i = blockIdx.x;
   const uint32_t* bi = bits + static_cast<size_t>(i) * nwords;
@@ -85,6 +89,8 @@ __global__ void __launch_bounds__(1024)
 finish_kernel(const int64_t* __restrict__ C, int Ne, float* __restrict__ P,
               const int32_t* __restrict__ chunk_hist, int nchunks, int max_ct,
               int64_t* __restrict__ ct_hist) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ long long s_max[32];
   __shared__ long long s_hist[32][OCCULT_MAX_TOPK + 1];  // per warp
   const int lane = threadIdx.x & 31;
@@ -156,7 +162,7 @@ int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t*
     int blocks = (nwords + 7) / 8;
     if (blocks > ctx.num_sms * 8) blocks = ctx.num_sms * 8;
 #define OCCULT_BITSET_LAUNCH(W)                                                              \
-    bitset_kernel<W><<<blocks, 256, 0, ctx.stream>>>(ids, vmask, n_tok, ds.top_k,            \
+    launch_pdl(bitset_kernel<W>, blocks, 256, 0, ctx.stream, ids, vmask, n_tok, ds.top_k,            \
                                                      ds.n_experts, max_ct, nwords, bits,     \
                                                      chunk_hist)
     if (ds.n_experts <= 64) OCCULT_BITSET_LAUNCH(1);
@@ -164,9 +170,9 @@ int launch_profile(const LaunchCtx& ctx, const occult_desc_t& ds, const int32_t*
     else OCCULT_BITSET_LAUNCH(4);
 #undef OCCULT_BITSET_LAUNCH
   }
-  pair_count_kernel<<<ds.n_experts, kPairWarps * 32, 0, ctx.stream>>>(bits, ds.n_experts, nwords,
+  launch_pdl(pair_count_kernel, ds.n_experts, kPairWarps * 32, 0, ctx.stream, bits, ds.n_experts, nwords,
                                                                        C);
-  finish_kernel<<<1, 1024, 0, ctx.stream>>>(C, ds.n_experts, P, chunk_hist, nwords, max_ct,
+  launch_pdl(finish_kernel, 1, 1024, 0, ctx.stream, C, ds.n_experts, P, chunk_hist, nwords, max_ct,
                                             chunk_hist ? ct_hist : nullptr);
   return cuda_status(cudaGetLastError());
 }

@@ -100,6 +100,8 @@ route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v,
              int32_t* __restrict__ routed, uint32_t* __restrict__ vmask) {
   __shared__ float s_ex[kWarpsPerBlock][PER_LANE * 32];
   __shared__ int s_dev[PER_LANE * 32];
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e < PER_LANE * 32; e += blockDim.x) s_dev[e] = e < Ne ? e2v[e] : -1;
   __syncthreads();
   const int warp = threadIdx.x >> 5;
@@ -220,9 +222,9 @@ int launch_route(const LaunchCtx& ctx, const occult_desc_t& ds, const float* log
   int blocks = (ds.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > ctx.num_sms * 16) blocks = ctx.num_sms * 16;
 #define OCCULT_ROUTE_LAUNCH(PL)                                                              \
-  route_kernel<PL><<<blocks, kWarpsPerBlock * 32, 0, ctx.stream>>>(                          \
-      logits, e2v, table, ds.T, ds.n_experts, ds.top_k, ds.n_vdev, ds.renorm, ds.route_mode, \
-      ds.limit_devices, ids, gates, routed, vmask)
+  launch_pdl(route_kernel<PL>, blocks, kWarpsPerBlock * 32, 0, ctx.stream, logits, e2v, table,   \
+             ds.T, ds.n_experts, ds.top_k, ds.n_vdev, ds.renorm, ds.route_mode,                  \
+             ds.limit_devices, ids, gates, routed, vmask)
   if (ds.n_experts <= 32) OCCULT_ROUTE_LAUNCH(1);
   else if (ds.n_experts <= 64) OCCULT_ROUTE_LAUNCH(2);
   else if (ds.n_experts <= 128) OCCULT_ROUTE_LAUNCH(4);

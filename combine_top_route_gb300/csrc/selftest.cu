@@ -13,6 +13,8 @@ namespace {
 
 __global__ void __launch_bounds__(32)
 selftest_wait_kernel(int complete, uint64_t limit_ns, int* dev_err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -30,7 +32,7 @@ selftest_wait_kernel(int complete, uint64_t limit_ns, int* dev_err) {
 }  // namespace
 
 int launch_selftest_wait(const LaunchCtx& ctx, int complete, uint64_t limit_ns) {
-  selftest_wait_kernel<<<1, 32, 0, ctx.stream>>>(complete, limit_ns, ctx.dev_err);
+  launch_pdl(selftest_wait_kernel, 1, 32, 0, ctx.stream, complete, limit_ns, ctx.dev_err);
   return cuda_status(cudaGetLastError());
 }
 

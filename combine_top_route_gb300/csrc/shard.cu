@@ -39,6 +39,8 @@ constexpr int kMaxBlocks = OCCULT_MAX_SOURCES * OCCULT_MAX_VDEV;
 __global__ void __launch_bounds__(kCountThreads)
 shard_count_kernel(const uint32_t* __restrict__ vmask, ShardSplit split, int Nd,
                    int32_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_cnt[kCountThreads / 32][OCCULT_MAX_VDEV];
   const int s = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,6 +102,8 @@ __global__ void __launch_bounds__(kMapThreads)
 shard_map_kernel(const int32_t* __restrict__ brim0, ShardSplit split, int T, int Nd,
                  const int32_t* __restrict__ counts, int32_t* __restrict__ send_off,
                  int32_t* __restrict__ recv_off, int32_t* __restrict__ brim0_send) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_cnt[kMaxBlocks], s_send[kMaxBlocks], s_recv[kMaxBlocks];
   const int n_src = split.n;
   block_offsets(counts, n_src, Nd, s_cnt, s_send, s_recv);
@@ -131,6 +135,8 @@ all_to_all_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, in
                   int64_t max_rows, const int32_t* __restrict__ counts,
                   const int32_t* __restrict__ send_off, const int32_t* __restrict__ recv_off,
                   int n_src, int Nd, int reverse) {
+  pdl_wait();
+  pdl_trigger();
   // blocks listed in destination order: dst offset, src offset
   __shared__ int s_dst[kMaxBlocks + 1], s_src[kMaxBlocks];
   const int nb = n_src * Nd;
@@ -178,10 +184,10 @@ int launch_shard_plan(const LaunchCtx& ctx, const occult_desc_t& ds, const Shard
                       const uint32_t* vmask, const int32_t* brim0, int32_t* brim0_send,
                       int32_t* counts, int32_t* send_off, int32_t* recv_off) {
   const int Nd = ds.n_vdev;
-  shard_count_kernel<<<split.n, kCountThreads, 0, ctx.stream>>>(vmask, split, Nd, counts);
+  launch_pdl(shard_count_kernel, split.n, kCountThreads, 0, ctx.stream, vmask, split, Nd, counts);
   const int gx = ds.T > 0 ? (ds.T + kMapThreads - 1) / kMapThreads : 1;
   const dim3 grid(gx < 4 * ctx.num_sms ? gx : 4 * ctx.num_sms, Nd);
-  shard_map_kernel<<<grid, kMapThreads, 0, ctx.stream>>>(brim0, split, ds.T, Nd, counts, send_off,
+  launch_pdl(shard_map_kernel, grid, kMapThreads, 0, ctx.stream, brim0, split, ds.T, Nd, counts, send_off,
                                                          recv_off, brim0_send);
   return cuda_status(cudaGetLastError());
 }
@@ -194,7 +200,7 @@ int launch_all_to_all(const LaunchCtx& ctx, const occult_desc_t& ds, int n_src, 
   int64_t blocks = (max_rows + kA2aWarps - 1) / kA2aWarps;
   const int64_t cap = static_cast<int64_t>(ctx.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  all_to_all_kernel<<<static_cast<int>(blocks), kA2aWarps * 32, 0, ctx.stream>>>(
+  launch_pdl(all_to_all_kernel, static_cast<int>(blocks), kA2aWarps * 32, 0, ctx.stream,
       static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), row_bytes, max_rows, counts,
       send_off, recv_off, n_src, ds.n_vdev, reverse);
   return cuda_status(cudaGetLastError());

@@ -16,6 +16,8 @@ namespace {
 
 __global__ void __launch_bounds__(256)
 similarity_accumulate_kernel(const float* __restrict__ H, int n_tok, int Ne, double* __restrict__ G) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= Ne * Ne) return;
   const int i = e / Ne, j = e - i * Ne;
@@ -29,6 +31,8 @@ similarity_accumulate_kernel(const float* __restrict__ H, int n_tok, int Ne, dou
 
 __global__ void __launch_bounds__(256)
 similarity_finish_kernel(const double* __restrict__ G, int Ne, float* __restrict__ table) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= Ne * Ne) return;
   const int i = e / Ne, j = e - i * Ne;
@@ -43,13 +47,13 @@ int launch_similarity_accumulate(const LaunchCtx& ctx, int Ne, const float* logi
                                  double* G) {
   if (n_tok == 0) return OCCULT_OK;
   const int n = Ne * Ne;
-  similarity_accumulate_kernel<<<(n + 255) / 256, 256, 0, ctx.stream>>>(logits, n_tok, Ne, G);
+  launch_pdl(similarity_accumulate_kernel, (n + 255) / 256, 256, 0, ctx.stream, logits, n_tok, Ne, G);
   return cuda_status(cudaGetLastError());
 }
 
 int launch_similarity_finish(const LaunchCtx& ctx, int Ne, const double* G, float* table) {
   const int n = Ne * Ne;
-  similarity_finish_kernel<<<(n + 255) / 256, 256, 0, ctx.stream>>>(G, Ne, table);
+  launch_pdl(similarity_finish_kernel, (n + 255) / 256, 256, 0, ctx.stream, G, Ne, table);
   return cuda_status(cudaGetLastError());
 }
 
