@@ -213,12 +213,114 @@ route_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v,
   }
 }
 
+// ---- plain top-k for up to 64 experts and k <= 8: eight lanes per token --------
+// Lane s of a token's eight holds experts 8s .. 8s+7 and sorts them (a 19-step
+// network on (logit, id) with the same order as above); three exchange rounds
+// with the lanes 1, 2 and 4 apart each keep the best eight of two sorted lists
+// (elementwise best of one list and the other reversed, then a bitonic clean), so
+// every lane ends with the token's top eight in order.  Four tokens per warp.
+__device__ __forceinline__ void cas8(float* v, int* id, int a, int b) {
+  if (before(v[b], id[b], v[a], id[a])) {
+    const float tv = v[a]; v[a] = v[b]; v[b] = tv;
+    const int ti = id[a]; id[a] = id[b]; id[b] = ti;
+  }
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+route_top8_kernel(const float* __restrict__ logits, const int32_t* __restrict__ e2v, int T,
+                  int Ne, int k, int renorm, int32_t* __restrict__ ids, float* __restrict__ gates,
+                  uint32_t* __restrict__ vmask) {
+  __shared__ int s_dev[64];
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < 64; e += blockDim.x) s_dev[e] = e < Ne ? e2v[e] : 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const float NEG = -__int_as_float(0x7f800000);  // -inf
+  for (int base = (blockIdx.x * kWarpsPerBlock + warp) * 4; base < T;
+       base += gridDim.x * kWarpsPerBlock * 4) {
+    const int t = base + (lane >> 3);
+    const bool valid = t < T;
+    const float* row = logits + static_cast<size_t>(valid ? t : 0) * Ne;
+    float v[8];
+    int id[8];
+    float mx = NEG;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      id[i] = sub * 8 + i;
+      v[i] = (valid && id[i] < Ne) ? row[id[i]] : NEG;
+      mx = fmaxf(mx, v[i]);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float part = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part += (valid && id[i] < Ne) ? expf(v[i] - mx) : 0.f;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    const float Z = part;
+    // sort the lane's eight, best first
+    cas8(v, id, 0, 1); cas8(v, id, 2, 3); cas8(v, id, 4, 5); cas8(v, id, 6, 7);
+    cas8(v, id, 0, 2); cas8(v, id, 1, 3); cas8(v, id, 4, 6); cas8(v, id, 5, 7);
+    cas8(v, id, 1, 2); cas8(v, id, 5, 6); cas8(v, id, 0, 4); cas8(v, id, 3, 7);
+    cas8(v, id, 1, 5); cas8(v, id, 2, 6); cas8(v, id, 1, 4); cas8(v, id, 3, 6);
+    cas8(v, id, 2, 4); cas8(v, id, 3, 5); cas8(v, id, 3, 4);
+    // merge with the lanes 1, 2, 4 apart: best eight of the two lists
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      float pv[8];
+      int pid[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        pv[i] = __shfl_xor_sync(0xffffffffu, v[7 - i], o);
+        pid[i] = __shfl_xor_sync(0xffffffffu, id[7 - i], o);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (before(pv[i], pid[i], v[i], id[i])) { v[i] = pv[i]; id[i] = pid[i]; }
+#pragma unroll
+      for (int dd = 4; dd > 0; dd >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i & dd) == 0) cas8(v, id, i, i + dd);
+    }
+    // every lane holds the token's top eight; lane j < k writes slot j
+    uint32_t vm = 0;
+    float gsum = 0.f, my_g = 0.f;
+    int my_id = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const float g = expf(v[j] - mx) / Z;
+        vm |= 1u << s_dev[id[j]];
+        gsum += g;
+        if (j == sub) { my_g = g; my_id = id[j]; }
+      }
+    }
+    if (renorm) my_g = my_g / gsum;
+    if (valid && sub < k) {
+      ids[static_cast<size_t>(t) * k + sub] = my_id;
+      gates[static_cast<size_t>(t) * k + sub] = my_g;
+    }
+    if (valid && sub == 0) vmask[t] = vm;
+  }
+}
+
 }  // namespace
 
 int launch_route(const LaunchCtx& ctx, const occult_desc_t& ds, const float* logits,
                  const int32_t* e2v, const float* table, int32_t* ids, float* gates,
                  int32_t* routed, uint32_t* vmask) {
   if (ds.T == 0) return OCCULT_OK;
+  if (ds.route_mode == OCCULT_ROUTE_EXACT && ds.n_experts <= 64 && ds.top_k <= 8) {
+    int blocks = (ds.T + 4 * kWarpsPerBlock - 1) / (4 * kWarpsPerBlock);
+    if (blocks > ctx.num_sms * 16) blocks = ctx.num_sms * 16;
+    return cuda_status(launch_pdl(route_top8_kernel, blocks, kWarpsPerBlock * 32, 0, ctx.stream,
+                                  logits, e2v, ds.T, ds.n_experts, ds.top_k, ds.renorm, ids,
+                                  gates, vmask));
+  }
   int blocks = (ds.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   if (blocks > ctx.num_sms * 16) blocks = ctx.num_sms * 16;
 #define OCCULT_ROUTE_LAUNCH(PL)                                                              \
