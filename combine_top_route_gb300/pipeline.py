@@ -151,8 +151,9 @@ class OccultMoE:
     def launches_per_forward(self) -> int:
         """Kernels this object launches per forward call."""
         n = 8  # route, 3 BRIM kernels, dispatch, up, down, combine
-        if self.merge == "atomic":
-            n -= 1  # the down-projection merges
+        if self.merge == "atomic" and self.desc.n_shared:
+            n -= 1  # the down-projection merges into the shared experts' output
+        # (without shared experts the combine's place is taken by the zeroing of y)
         if self.src_off is not None:
             n += 4  # 2 plan kernels, 2 exchanges; combine runs as stage one + stage two
         if self.y_sfd is not None:
@@ -239,9 +240,9 @@ class OccultMoE:
         """Kernels one backward call launches."""
         # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad,
         # router grad (+ 2 exchanges and the split merge when sharded)
+        # (atomic merge: the dgrad through [W_g; W_u] merges dx, and the zeroing of
+        # dx takes the combine's place)
         n = 9 + (1 if self.y_sfd is not None else 0)
-        if self.merge == "atomic":
-            n -= 1  # the dgrad through [W_g; W_u] merges dx
         return n + (2 if self.src_off is not None else 0)
 
     def backward(self, dy: torch.Tensor, stream=None):

@@ -99,3 +99,57 @@ def test_forward_and_backward_replay_from_a_cuda_graph(occ, merge):
             scale = float(b.abs().max())
             assert float((a - b).abs().max()) <= 1e-5 * scale, name
     assert occ.device_error() == 0
+
+
+def kernel_nodes(fn):
+    """Kernel launches of fn, counted as the kernel nodes of a CUDA graph capturing
+    it (fn launches only this library's kernels)."""
+    import ctypes
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        pytest.skip("this PyTorch cannot keep a captured graph")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(g):
+        fn()
+    cu = ctypes.CDLL("libcuda.so.1")
+    graph = ctypes.c_void_p(g.raw_cuda_graph())
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) == 0
+    kinds = []
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kinds.append(t.value)
+    return sum(1 for t in kinds if t == 0)   # CU_GRAPH_NODE_TYPE_KERNEL
+
+
+@pytest.mark.parametrize("merge,shared,train", [("atomic", False, True), ("ordered", False, True),
+                                                ("atomic", True, False)])
+def test_launch_counts_match_the_kernels_that_run(occ, merge, shared, train):
+    """launches_per_forward / launches_per_backward (the bench's gpu_launches) equal
+    the kernels a captured graph of the calls holds."""
+    if shared:
+        cfg = synth.CONFIGS["qwen_prefill"].with_(name="runtime_shared", T=600, d=256,
+                                                   n_experts=16, top_k=4, inter=128, n_vdev=4,
+                                                   shared_inter=256, prof_tokens=2048)
+        case = make_case(cfg)
+    else:
+        case = small_case()
+    moe = occ.OccultMoE(occ.desc_for(case.cfg), case.weights, torch.as_tensor(case.placement),
+                        train=train, merge=merge)
+    logits = case.logits.cuda()
+    dy = synth.upstream_grad(case.cfg, device="cuda") if train else None
+    moe.forward(logits, case.x)
+    if train:
+        moe.backward(dy)
+    torch.cuda.synchronize()
+    assert kernel_nodes(lambda: moe.forward(logits, case.x)) == moe.launches_per_forward
+    if train:
+        assert kernel_nodes(lambda: moe.backward(dy)) == moe.launches_per_backward
