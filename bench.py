@@ -193,6 +193,9 @@ class OracleSample:
         self.x = synth.hidden_states(cfg, device=dev).float().cpu().numpy()
         self.w = {k: v.float().cpu().numpy()
                   for k, v in synth.expert_weights(cfg, device=dev).items()}
+        # a training workload's step is forward + backward on both sides
+        self.dy = (synth.upstream_grad(cfg, device=dev).float().cpu().numpy()
+                   if cfg.backward else None)
         try:
             import threadpoolctl
             self.cores = max(i["num_threads"] for i in threadpoolctl.threadpool_info()) or 1
@@ -200,7 +203,10 @@ class OracleSample:
             self.cores = len(os.sched_getaffinity(0))
 
     def run(self, n_tok: int) -> float:
-        """Seconds for routing, BRIMs (Alg. 3, 5) and the Eq. 1 output of n_tok tokens."""
+        """Seconds for routing, BRIMs (Alg. 3, 5) and the Eq. 1 output of n_tok tokens
+        (and, for a training workload, the gradients of x, the weights, the gates and
+        the router logits)."""
+        from oracle import backward as obackward
         from oracle import brim as obrim
         from oracle import expert as oexpert
         from oracle import routing as orouting
@@ -210,6 +216,10 @@ class OracleSample:
                                          renorm=self.cfg.renorm)
         obrim.Brims(ids, gates, self.L)
         oexpert.layer_output(self.x[:n_tok], ids, gates, self.w)
+        if self.dy is not None:
+            g = obackward.moe_backward(self.x[:n_tok], ids, gates, self.w["w1"], self.w["w2"],
+                                       self.dy[:n_tok])
+            obackward.router_grad(self.logits[:n_tok], ids, g["dgates"], renorm=self.cfg.renorm)
         return time.perf_counter() - t0
 
     def tokens_for(self, seconds: float) -> int:
@@ -226,7 +236,9 @@ class OracleSample:
     def describe(self, n_tok: int, dt: float, runs: int = 1) -> dict:
         return {"value": n_tok * runs / dt, "unit": UNIT, "cores": self.cores, "kind": "oracle",
                 "sample": f"first {n_tok} tokens of the {self.cfg.T}-token batch, {runs} run(s): "
-                          f"routing, BRIMs (Alg. 3, 5) and the Eq. 1 output in fp64, {dt:.1f} s"}
+                          f"routing, BRIMs (Alg. 3, 5) and the Eq. 1 output"
+                          + (" and its backward" if self.dy is not None else "")
+                          + f" in fp64, {dt:.1f} s"}
 
 
 def cpu_baseline(cfg, seconds: float = 15.0):
