@@ -37,6 +37,14 @@ EDGE = {
     # >= 256 rows an expert on average: the GEMMs run on CTA pairs, with ragged
     # segments (pair units whose second tile is partial or empty)
     "pair_ragged": CFG["olmoe_fwd"].with_(name="pair_ragged", T=2500, d=512, inter=320),
+    # the largest layers the ABI takes: 256 experts, 32 virtual devices, k = 16; and
+    # 128 experts on 16 devices with k = 12
+    "ne256_nd32_k16": CFG["olmoe_fwd"].with_(name="ne256_nd32_k16", T=700, d=256, inter=128,
+                                             n_experts=256, top_k=16, n_vdev=32, n_clusters=16,
+                                             experts_per_cluster=24, prof_tokens=4096),
+    "ne128_nd16_k12": CFG["olmoe_fwd"].with_(name="ne128_nd16_k12", T=513, d=512, inter=192,
+                                             n_experts=128, top_k=12, n_vdev=16, n_clusters=16,
+                                             experts_per_cluster=16, prof_tokens=4096),
 }
 
 
@@ -389,9 +397,10 @@ def test_empty_batch(occ):
 
 
 # --------------------------------------------------------------------------- profiling
-@pytest.mark.parametrize("name", ["tiny_f32", "olmoe_fwd", "qwen_prefill", "olmoe_train"])
+@pytest.mark.parametrize("name", ["tiny_f32", "olmoe_fwd", "qwen_prefill", "olmoe_train",
+                                  "ne256_nd32_k16", "ne128_nd16_k12"])
 def test_profile_coact_bit_exact(occ, name):
-    cfg = CFG[name]
+    cfg = CFG.get(name) or EDGE[name]
     lg = synth.profiling_logits(cfg).numpy()
     ids, _ = orouting.route_topk(lg, cfg.top_k)
     L = alg1_placement(cfg)
