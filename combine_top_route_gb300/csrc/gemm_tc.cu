@@ -143,6 +143,16 @@ __device__ __forceinline__ int seg_at(const Params& p, int s) {
   return p.seg_off ? p.seg_off[s] : (s ? p.single_rows : 0);
 }
 
+// The i-th unit a CTA (pair) takes.  Forward and dgrad units cost the same
+// (K is fixed), so they go round-robin.  Weight-gradient units reduce over their
+// expert's rows, which vary several-fold between experts: they are ordered by
+// decreasing rows and dealt out in a snake (even rounds left to right, odd
+// rounds right to left), so that every CTA ends with about the same sum of K.
+template <bool WGRAD>
+__device__ __forceinline__ int unit_at(int i, int unit0, int n_units) {
+  return i * n_units + ((WGRAD && (i & 1)) ? n_units - 1 - unit0 : unit0);
+}
+
 struct TileInfo {
   int seg;      // segment
   int grp;      // weight group / output matrix
@@ -175,8 +185,9 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
     // a pair's unit is two consecutive M tiles of the output matrix
     const int units_m = PAIR ? p.n_tiles_m / 2 : p.n_tiles_m;
     const int per = units_m * p.n_tiles_n;
-    ti.seg = tau / per;
-    const int rem = tau - ti.seg * per;
+    const int r = tau / per;   // rank of the segment by decreasing rows
+    ti.seg = mt_off[r];
+    const int rem = tau - r * per;
     const int mt = rem / p.n_tiles_n;
     ti.nt = rem - mt * p.n_tiles_n;
     ti.m0 = (PAIR ? 2 * mt + rank : mt) * BM;
@@ -222,14 +233,25 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
 // row r is kept at chunk c ^ (r % 8) of its 128-byte row (no bank conflicts on
 // either side).  Rows >= valid are not written.  `out` is the address of the
 // warp's first row at this column.
+// The two halves are also callable alone: stage_v4 puts 16-byte chunk j of the
+// lane's row in place, flush_rows stores the staged rows.
+__device__ __forceinline__ void stage_v4(uint32_t* buf, int j, const uint4& v) {
+  const int lane = threadIdx.x & 31;
+  *reinterpret_cast<uint4*>(buf + lane * 32 + 4 * (j ^ (lane & 7))) = v;
+}
+template <int W>
+__device__ __forceinline__ void flush_rows(uint32_t* buf, char* out, int64_t row_bytes, int valid);
 template <int W>
 __device__ __forceinline__ void store_rows(uint32_t* buf, const uint32_t* v, char* out,
                                            int64_t row_bytes, int valid) {
-  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < W / 4; ++j)
-    *reinterpret_cast<uint4*>(buf + lane * 32 + 4 * (j ^ (lane & 7))) =
-        make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    stage_v4(buf, j, make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+  flush_rows<W>(buf, out, row_bytes, valid);
+}
+template <int W>
+__device__ __forceinline__ void flush_rows(uint32_t* buf, char* out, int64_t row_bytes, int valid) {
+  const int lane = threadIdx.x & 31;
   __syncwarp();
   constexpr int LPR = W / 4;     // lanes per row
   constexpr int RPI = 32 / LPR;  // rows per instruction
@@ -274,6 +296,25 @@ __device__ __forceinline__ void red_rows32(uint32_t* buf, const uint32_t* v, flo
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 __device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
+// This thread's G and U segments of a SwiGLU-backward tile (BN / 2 columns of
+// one row, fewer at the matrix's edge) fetched into L2.
+__device__ __forceinline__ void gu_prefetch_l2(const __nv_bfloat16* g, int I, int cols) {
+  const int n = min(BN / 2, cols);
+  for (int c = 0; c < n; c += 64) {   // 128-byte lines
+    prefetch_l2(g + c);
+    prefetch_l2(g + I + c);
+  }
+}
+
+// G and U of 16 columns of one row for the SwiGLU backward: rows of the
+// forward's save are [G | U], 2*I bf16; r[0..1] get G, r[2..3] U.
+__device__ __forceinline__ void load_gu16(const __nv_bfloat16* g, int I, uint4 (&r)[4]) {
+  r[0] = __ldg(reinterpret_cast<const uint4*>(g));
+  r[1] = __ldg(reinterpret_cast<const uint4*>(g + 8));
+  r[2] = __ldg(reinterpret_cast<const uint4*>(g + I));
+  r[3] = __ldg(reinterpret_cast<const uint4*>(g + I + 8));
+}
+
 // Shared-memory descriptor of one K=16 slice of an operand tile.
 //  K-major: rows along M/N at 128 B, 8-row groups every 1024 B; slice kk starts
 //           32 bytes further inside the swizzle atom.
@@ -298,6 +339,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
                 "paired forward / dgrad GEMMs take A K-major and B a plain matrix");
   static_assert(!(WGRAD && (!op_mn(AM) || !op_mn(BMODE))), "weight gradients are MN-major");
+  static_assert(!WGRAD || (epi_staged(EPI, SWAP) && kEpiBytes >= 4 * kMaxSeg),
+                "weight gradients sort the segments in the epilogue buffers");
   static_assert(!SWAP || (PAIR && !WGRAD && !op_mn(AM) && BMODE == OP_TMA_K &&
                           (EPI == EPI_SWIGLU || EPI == EPI_F32 || EPI == EPI_F32_RED)),
                 "swapped units: paired forward GEMMs with K-major rows and weights");
@@ -342,6 +385,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     tail->abort_flag = 0;
     mbar_fence_init();
   }
+  if (WGRAD) {
+    // the segments in order of decreasing rows (ties by index) into mt_off, the
+    // rows staged in the epilogue buffers, which nothing else uses yet
+    int* len = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes);
+    for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) len[s] = seg_at(p, s + 1) - seg_at(p, s);
+    __syncthreads();
+    for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
+      const int ls = len[s];
+      int r = 0;
+      for (int t = 0; t < p.n_seg; ++t) r += (len[t] > ls) || (len[t] == ls && t < s);
+      tail->mt_off[r] = s;
+    }
+  }
   if (warp == 0) {
     if (lane == 0) {
       if (!WGRAD) {
@@ -379,7 +435,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tau = unit0; tau < total && ok; tau += n_units) {
+    for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
       const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       const int n0 = ti.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
@@ -468,7 +524,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tau = unit0; tau < total && ok; tau += n_units, ++it) {
+      for (int tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++it, unit0, n_units)) {
         const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
@@ -517,7 +573,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tau = unit0; tau < total && ok; tau += n_units) {
+      for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
         const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&tail->gfull[stage], phase, abort_flag)) { ok = false; break; }
@@ -539,15 +595,56 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int row = quarter * 32 + lane;
     int it = 0;
     bool ok = true;
-    for (int tau = unit0; tau < total; tau += n_units, ++it) {
+    for (int tau = unit0; tau < total; tau = unit_at<WGRAD>(++it, unit0, n_units)) {
       const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
+      const bool valid = row < ti.rows;
+      const int64_t grow = ti.m0 + row;
+      // Loads that do not depend on the accumulator are issued before waiting
+      // for it, so that their latency hides behind the tile's MMAs: the SwiGLU
+      // backward's first G|U chunk, the merge's destination rows, the swapped
+      // SwiGLU's row gates.
+      // SwiGLU backward: the next tile's G|U rows are fetched into L2 while
+      // this one is processed (the first tile's too)
+      const __nv_bfloat16* gu_row = nullptr;
+      if (EPI == EPI_SWIGLU_BWD && !SWAP) {
+        const int64_t ld_gu = 2 * static_cast<int64_t>(p.half_n);
+        const int c0 = ti.nt * BN + half * (BN / 2);
+        gu_row = p.gu_in + (valid ? grow : ti.m0) * ld_gu + c0;
+        if (it == 0 && valid && c0 < p.N_out) gu_prefetch_l2(gu_row, p.half_n, p.N_out - c0);
+        const int tau_n = unit_at<WGRAD>(it + 1, unit0, n_units);
+        if (tau_n < total) {
+          const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP>(tau_n, p, tail->mt_off, rank);
+          const int cn = tn.nt * BN + half * (BN / 2);
+          if (row < tn.rows && cn < p.N_out)
+            gu_prefetch_l2(p.gu_in + (tn.m0 + row) * ld_gu + cn, p.half_n, p.N_out - cn);
+        }
+      }
+      float g_pre = 0.f;
+      if (EPI == EPI_SWIGLU_BWD && !SWAP && valid) g_pre = p.row_gate[grow];
+      if (EPI == EPI_SWIGLU && !SWAP) g_pre = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
+      int64_t dst_pre = 0;
+      if (EPI == EPI_F32_RED && !SWAP && valid) dst_pre = p.out_tok[p.out_src[grow]];
+      constexpr int kSwapChunks = 4;  // a swapped unit's columns: at most 4 chunks a warp
+      int64_t dst_sw[kSwapChunks];
+      float gate_sw[kSwapChunks];
+      if (SWAP) {
+#pragma unroll
+        for (int j = 0; j < kSwapChunks; ++j) {
+          const int col_l = half * 32 + 64 * j + lane;
+          dst_sw[j] = 0;
+          gate_sw[j] = 1.0f;
+          if (col_l < ti.urows) {
+            if (EPI == EPI_F32_RED) dst_sw[j] = p.out_tok[p.out_src[ti.t0 + col_l]];
+            if (EPI == EPI_F32) dst_sw[j] = ti.t0 + col_l;
+            if (EPI == EPI_SWIGLU && p.row_gate) gate_sw[j] = p.row_gate[ti.t0 + col_l];
+          }
+        }
+      }
       if (!mbar_wait(&tail->tfull[a], aph, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_row = tbase + a * BN + (static_cast<uint32_t>(quarter * 32) << 16);
-      const bool valid = row < ti.rows;
-      const int64_t grow = ti.m0 + row;
       const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
       const int64_t wrow0 = ti.m0 + quarter * 32;
       uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes) +
@@ -566,12 +663,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out);
           uint16_t* hb = reinterpret_cast<uint16_t*>(ebuf);  // [32 columns][16 units]
           // a last weight block past N_out (N_out % 128 != 0) leaves quarters idle
-#pragma unroll 1
-          for (int c = half * 32; c < (i0 < p.N_out ? ti.nmma : 0); c += 64) {
+          const int c_end = i0 < p.N_out ? ti.nmma : 0;
+#pragma unroll
+          for (int j = 0; j < kSwapChunks; ++j) {
+            const int c = half * 32 + 64 * j;
+            if (c >= c_end) break;
             tmem_ld32(t_row + c, v0);
             tmem_ld_wait();
-            const int col_l = c + lane;
-            const float gl = (col_l < ti.urows && p.row_gate) ? p.row_gate[ti.t0 + col_l] : 1.0f;
+            const float gl = gate_sw[j];
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
               const uint32_t send = hi ? v0[t] : v0[16 + t];
@@ -601,12 +700,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           // a row), stored at row t0 + c (plain) or added into the token's row
           const int d0 = ti.nt * BN + rank * BM + quarter * 32;
           float* out = static_cast<float*>(p.out);
-#pragma unroll 1
-          for (int c = half * 32; c < (d0 < p.N_out ? ti.nmma : 0); c += 64) {
-            const int col_l = c + lane;
-            int64_t dst_l = 0;
-            if (col_l < ti.urows)
-              dst_l = EPI == EPI_F32_RED ? p.out_tok[p.out_src[ti.t0 + col_l]] : ti.t0 + col_l;
+          const int c_end = d0 < p.N_out ? ti.nmma : 0;
+#pragma unroll
+          for (int j = 0; j < kSwapChunks; ++j) {
+            const int c = half * 32 + 64 * j;
+            if (c >= c_end) break;
+            const int64_t dst_l = dst_sw[j];
             tmem_ld32(t_row + c, v0);
             tmem_ld_wait();
 #pragma unroll
@@ -632,7 +731,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       } else if (EPI == EPI_SWIGLU) {
-        const float g = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
+        const float g = g_pre;
         const int col0 = ti.nt * (BN / 2);
 #pragma unroll 1
         for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
@@ -678,56 +777,57 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       } else if (EPI == EPI_SWIGLU_BWD) {
         // accumulator = dh' (gradient of the modulated intermediate) for the
-        // tile's 256 columns of I; G and U come from the forward
-        const float g = valid ? p.row_gate[grow] : 0.f;
+        // tile's 256 columns of I; G and U come from the forward (fetched into
+        // L2 a tile ahead)
+        const float g = g_pre;
         const int col0 = ti.nt * BN;
         const int I = p.half_n;
         float dg = 0.f;
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+          if (col0 + c >= p.N_out) break;
           tmem_ld32(t_row + c, v0);
-          tmem_ld_wait();
-          if (col0 + c < p.N_out) {
-            const int64_t grow_c = valid ? grow : ti.m0;  // rows past the tile read its first row
-            const uint4* gp = reinterpret_cast<const uint4*>(p.gu_in + grow_c * (2 * static_cast<int64_t>(I)) + col0 + c);
-            const uint4* up = reinterpret_cast<const uint4*>(p.gu_in + grow_c * (2 * static_cast<int64_t>(I)) + I + col0 + c);
-            uint32_t pg[16], pu[16];
+          uint32_t pg[16], pu[16];
+          const __nv_bfloat16* gsrc = gu_row + (c - half * (BN / 2));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 x = gp[i], y = up[i];
-              pg[4 * i] = x.x; pg[4 * i + 1] = x.y; pg[4 * i + 2] = x.z; pg[4 * i + 3] = x.w;
-              pu[4 * i] = y.x; pu[4 * i + 1] = y.y; pu[4 * i + 2] = y.z; pu[4 * i + 3] = y.w;
-            }
-            uint32_t og[16], ou[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float dG[2], dU[2];
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const float G = __uint_as_float(h ? (pg[i] & 0xffff0000u) : (pg[i] << 16));
-                const float U = __uint_as_float(h ? (pu[i] & 0xffff0000u) : (pu[i] << 16));
-                const float dhp = __uint_as_float(v0[2 * i + h]);
-                const float sg = sigmoid_f(G);
-                const float s = G * sg;
-                dg = fmaf(dhp, s * U, dg);
-                const float dh = g * dhp;
-                dG[h] = dh * U * sg * (1.0f + G * (1.0f - sg));
-                dU[h] = dh * s;
-              }
-              og[i] = pack_bf16x2(dG[0], dG[1]);
-              ou[i] = pack_bf16x2(dU[0], dU[1]);
-            }
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0 + c;
-            store_rows<16>(ebuf, og, reinterpret_cast<char*>(o), p.ldo * 2, wrows);
-            store_rows<16>(ebuf, ou, reinterpret_cast<char*>(o + I), p.ldo * 2, wrows);
+          for (int i = 0; i < 2; ++i) {
+            uint4 r[4];
+            load_gu16(gsrc + 16 * i, I, r);
+            pg[8 * i] = r[0].x; pg[8 * i + 1] = r[0].y; pg[8 * i + 2] = r[0].z; pg[8 * i + 3] = r[0].w;
+            pg[8 * i + 4] = r[1].x; pg[8 * i + 5] = r[1].y; pg[8 * i + 6] = r[1].z; pg[8 * i + 7] = r[1].w;
+            pu[8 * i] = r[2].x; pu[8 * i + 1] = r[2].y; pu[8 * i + 2] = r[2].z; pu[8 * i + 3] = r[2].w;
+            pu[8 * i + 4] = r[3].x; pu[8 * i + 5] = r[3].y; pu[8 * i + 6] = r[3].z; pu[8 * i + 7] = r[3].w;
           }
+          tmem_ld_wait();
+          uint32_t og[16], ou[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float dG[2], dU[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float G = __uint_as_float(h ? (pg[i] & 0xffff0000u) : (pg[i] << 16));
+              const float U = __uint_as_float(h ? (pu[i] & 0xffff0000u) : (pu[i] << 16));
+              const float dhp = __uint_as_float(v0[2 * i + h]);
+              const float sg = sigmoid_f(G);
+              const float s = G * sg;
+              dg = fmaf(dhp, s * U, dg);
+              const float dh = g * dhp;
+              dG[h] = dh * U * sg * (1.0f + G * (1.0f - sg));
+              dU[h] = dh * s;
+            }
+            og[i] = pack_bf16x2(dG[0], dG[1]);
+            ou[i] = pack_bf16x2(dU[0], dU[1]);
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0 + c;
+          store_rows<16>(ebuf, og, reinterpret_cast<char*>(o), p.ldo * 2, wrows);
+          store_rows<16>(ebuf, ou, reinterpret_cast<char*>(o + I), p.ldo * 2, wrows);
         }
         // one partial per (row, N tile, column half)
         if (valid) p.dg_part[grow * (2 * p.n_tiles_n) + 2 * ti.nt + half] = dg;
       } else if (EPI == EPI_F32_RED) {
         // fp32 rows added into their tokens' output rows (the merge)
         const int col0 = ti.nt * BN;
-        const int64_t my_dst = valid ? p.out_tok[p.out_src[grow]] : 0;
+        const int64_t my_dst = dst_pre;
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           tmem_ld32(t_row + c, v0);
@@ -776,7 +876,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tau = unit0; tau < total && ok; tau += n_units) {
+    for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
       const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
       // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
       // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
