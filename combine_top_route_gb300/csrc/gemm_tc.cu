@@ -602,11 +602,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const bool valid = row < ti.rows;
       const int64_t grow = ti.m0 + row;
       // Loads that do not depend on the accumulator are issued before waiting
-      // for it, so that their latency hides behind the tile's MMAs: the SwiGLU
-      // backward's first G|U chunk, the merge's destination rows, the swapped
-      // SwiGLU's row gates.
-      // SwiGLU backward: the next tile's G|U rows are fetched into L2 while
-      // this one is processed (the first tile's too)
+      // for it, so that their latency hides behind the tile's MMAs: the row
+      // gates, the merge's destination rows.  The SwiGLU backward also fetches
+      // the next tile's G|U rows into L2 while this one is processed (the first
+      // tile's too).
       const __nv_bfloat16* gu_row = nullptr;
       if (EPI == EPI_SWIGLU_BWD && !SWAP) {
         const int64_t ld_gu = 2 * static_cast<int64_t>(p.half_n);
@@ -709,8 +708,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             tmem_ld32(t_row + c, v0);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              ebuf[j * 32 + ((((lane >> 2) ^ (j & 7)) << 2) | (lane & 3))] = v0[j];
+            for (int r = 0; r < 32; ++r)
+              ebuf[r * 32 + ((((lane >> 2) ^ (r & 7)) << 2) | (lane & 3))] = v0[r];
             __syncwarp();
 #pragma unroll
             for (int it2 = 0; it2 < 8; ++it2) {
@@ -1062,6 +1061,8 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
   if (!g.wgrad && g.K % BK != 0) return OCCULT_ERR_UNSUPPORTED;
+  // the epilogues write (or add) 16-byte vectors along output rows
+  if (reinterpret_cast<uintptr_t>(g.out) % 16 != 0 || g.ldo % 8 != 0) return OCCULT_ERR_UNSUPPORTED;
   if (g.n_seg == 0 || (!g.wgrad && g.max_rows == 0)) return OCCULT_OK;
   // Forward and dgrad GEMMs run on CTA pairs (one 256 x 256 tile per pair, each
   // CTA holding 128 rows of B), gathered A rows included: each CTA gathers its
