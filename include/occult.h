@@ -18,7 +18,10 @@
  * Memory:    every pointer is a DEVICE pointer unless the comment says "host".
  *            All buffers belong to the caller; the library never allocates,
  *            frees or synchronises (except occult_device_error, which reads back
- *            one word).  Row-major, densely packed unless stated.
+ *            one word).  Row-major, densely packed unless stated.  Buffers start
+ *            on a 16-byte boundary (the kernels move 16-byte vectors); a bf16
+ *            layer's expert-GEMM output that does not is refused with
+ *            OCCULT_ERR_UNSUPPORTED.
  * Execution: calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
  *            default stream) and capture into CUDA graphs.
  * Sizing:    data-dependent sizes are bounded by their worst case so that no

@@ -257,6 +257,27 @@ def test_expert_down(occ, name):
     assert np.isfinite(y.float().cpu().numpy()).all(), "an EPD row was left unwritten"
 
 
+def test_unaligned_output_is_refused(occ):
+    """A bf16 layer's GEMM output must start on a 16-byte boundary (its epilogues
+    store 16-byte vectors): one that does not is refused before any launch and
+    the buffer is left as it was."""
+    cfg = CFG["olmoe_fwd"].with_(name="unaligned", T=64)
+    case = make_case(cfg)
+    ids_o, gates_o, _ = case.oracle_route()
+    b = oracle_brims(case, ids_o, gates_o)
+    ds = occ.desc_for(cfg)
+    h = torch.zeros(cfg.T * cfg.top_k, cfg.inter, dtype=cfg.torch_dtype, device="cuda")
+    buf = torch.full((cfg.T * cfg.top_k * cfg.d + 1,), 7.0, dtype=torch.float32, device="cuda")
+    y = buf[1:].view(cfg.T * cfg.top_k, cfg.d)          # 4 bytes past a 16-byte boundary
+    with pytest.raises(occ.OccultError) as e:
+        occ.occult_expert_down(ds, h, i32(b.exp_off), i32(case.placement.reshape(-1)),
+                               case.weights["w2"], y)
+    assert e.value.code == occ.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (buf == 7.0).all()
+    assert occ.device_error() == 0
+
+
 # --------------------------------------------------------------------------- shared experts
 @pytest.mark.parametrize("name", ["qwen_prefill", "deepseek_decode"])
 def test_shared_ffn(occ, name):
