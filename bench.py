@@ -196,11 +196,15 @@ class OracleSample:
         # a training workload's step is forward + backward on both sides
         self.dy = (synth.upstream_grad(cfg, device=dev).float().cpu().numpy()
                    if cfg.backward else None)
-        try:
-            import threadpoolctl
-            self.cores = max(i["num_threads"] for i in threadpoolctl.threadpool_info()) or 1
-        except Exception:
-            self.cores = len(os.sched_getaffinity(0))
+        capped = [int(os.environ[k]) for k in THREAD_ENV if os.environ.get(k, "").isdigit()]
+        if capped:
+            self.cores = min(capped)
+        else:
+            try:
+                import threadpoolctl
+                self.cores = max(i["num_threads"] for i in threadpoolctl.threadpool_info()) or 1
+            except Exception:
+                self.cores = len(os.sched_getaffinity(0))
 
     def run(self, n_tok: int) -> float:
         """Seconds for routing, BRIMs (Alg. 3, 5) and the Eq. 1 output of n_tok tokens
@@ -239,6 +243,24 @@ class OracleSample:
                           f"routing, BRIMs (Alg. 3, 5) and the Eq. 1 output"
                           + (" and its backward" if self.dy is not None else "")
                           + f" in fp64, {dt:.1f} s"}
+
+
+THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def cpu_baseline_one_thread(cfg, seconds: float = 5.0):
+    """The same oracle sample on one host core: a child interpreter whose BLAS and
+    OpenMP pools are capped at one thread before numpy loads.  The child sees no
+    GPU and draws the batch on the CPU (same shapes and distributions)."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", **{k: "1" for k in THREAD_ENV})
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, synth; "
+            "cfg = synth.CONFIGS[%r].with_(T=%d); "
+            "print(json.dumps(bench.cpu_baseline(cfg, %r)))" % (ROOT, cfg.name, cfg.T, seconds))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=300)
+    if r.returncode != 0:
+        return {"error": (r.stderr.strip().splitlines() or ["failed"])[-1]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_baseline(cfg, seconds: float = 15.0):
@@ -591,6 +613,7 @@ def run_ours(args, cfg, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+        result["cpu_baseline"]["one_thread"] = cpu_baseline_one_thread(cfg)
     if rank == 0:
         print(json.dumps(result), flush=True)
 
