@@ -185,3 +185,41 @@ def test_host_placement_on_profiled_counts(occ):
     C = coact.coactivation(ids, cfg.n_experts)
     L, _ = occ.occult_place(C, cfg.n_vdev)
     assert (L.numpy() == placement.place(C, cfg.n_vdev)).all()
+
+
+# entry points that take no layer descriptor first (checked by their own tests)
+_NOT_DESC_FIRST = ("occult_strerror", "occult_check_desc", "occult_workspace_size",
+                   "occult_device_error", "occult_selftest_wait", "occult_place")
+
+
+def test_every_entry_point_refuses_null_buffers_before_launching(occ):
+    """Every call taking a layer descriptor, given a valid non-empty layer and
+    null buffers, returns OCCULT_ERR_INVALID_ARG: its arguments are checked on
+    the host before anything launches (on this machine, without a GPU, a call
+    that got past its checks would report a CUDA error instead)."""
+    from combine_top_route_gb300 import _SIGNATURES
+    L = occ.lib()
+    good = _desc(occ)
+    sim = _desc(occ, route_mode=occ.ROUTE_SIMILARITY_PRUNED, limit_devices=2)
+    checked = []
+    for name, (_, argtypes) in _SIGNATURES.items():
+        if name in _NOT_DESC_FIRST:
+            continue
+        args = []
+        for i, t in enumerate(argtypes):
+            if i == 0:
+                args.append(ctypes.byref(sim if name == "occult_route_similarity" else good))
+            elif t is ctypes.c_void_p:
+                args.append(ctypes.c_void_p(0))
+            elif t is ctypes.c_int32 or t is ctypes.c_int:
+                args.append(1)            # one source / one profiled token / a flag
+            elif t is ctypes.c_int64:
+                args.append(ctypes.c_int64(16))
+            elif t is ctypes.c_size_t:
+                args.append(ctypes.c_size_t(1 << 30))
+            else:
+                raise AssertionError(f"{name}: argument {i} of type {t}")
+        rc = getattr(L, name)(*args)
+        assert rc == occ.ERR_INVALID_ARG, f"{name} returned {rc}"
+        checked.append(name)
+    assert len(checked) >= 20
