@@ -258,11 +258,14 @@ def cpu_baseline_one_thread(cfg, seconds: float = 5.0):
     code = ("import json, sys; sys.path.insert(0, %r); import bench, synth; "
             "cfg = synth.CONFIGS[%r].with_(T=%d); "
             "print(json.dumps(bench.cpu_baseline(cfg, %r)))" % (ROOT, cfg.name, cfg.T, seconds))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
-                       timeout=300)
-    if r.returncode != 0:
-        return {"error": (r.stderr.strip().splitlines() or ["failed"])[-1]}
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                           timeout=300)
+        if r.returncode != 0:
+            return {"error": (r.stderr.strip().splitlines() or ["failed"])[-1]}
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.TimeoutExpired, OSError, ValueError, IndexError) as e:
+        return {"error": f"{type(e).__name__}: {e}"}
 
 
 def cpu_baseline(cfg, seconds: float = 15.0):
