@@ -85,3 +85,9 @@ def test_thread_caps_set_the_reported_cores(monkeypatch):
     o = bench.OracleSample(synth.CONFIGS["tiny_f32"])
     assert o.cores == 1
     assert o.run(32) > 0
+
+
+def test_one_core_baseline_runs_in_a_capped_child():
+    r = bench.cpu_baseline_one_thread(synth.CONFIGS["tiny_f32"], 0.5)
+    assert "error" not in r, r
+    assert r["cores"] == 1 and r["kind"] == "oracle" and r["value"] > 0
