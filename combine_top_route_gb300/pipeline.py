@@ -84,6 +84,13 @@ class OccultMoE:
         self.device = dev
         self.w = {k: v.to(dev, dt).contiguous() for k, v in weights.items()}
         placement = torch.as_tensor(placement, dtype=torch.int32)
+        # the kernels index by the placement without checking it (it lives in
+        # device memory): it must hold every expert exactly once
+        n_loc = desc.n_experts // max(1, desc.n_vdev)
+        if (tuple(placement.shape) != (desc.n_vdev, n_loc)
+                or sorted(placement.reshape(-1).tolist()) != list(range(desc.n_experts))):
+            raise ValueError(f"placement must be [{desc.n_vdev}, {n_loc}] holding every one of "
+                             f"the {desc.n_experts} experts exactly once")
         e2v = torch.empty(desc.n_experts, dtype=torch.int32)
         for d in range(placement.shape[0]):
             for e in placement[d].tolist():

@@ -226,7 +226,10 @@ int occult_router_grad(const occult_desc_t* desc, const float* logits, const int
  * occult_build_brim -- BRIM0 (Algorithm 3) and BRIM1 (Algorithm 5).
  *   ids, gates, vmask  from occult_route.
  *   placement   int32 [Nd, n_loc] device-major expert lists; slot s = d*n_loc + j
- *               holds expert placement[s].
+ *               holds expert placement[s].  It must hold every expert exactly
+ *               once (as occult_place writes it): device buffers are not
+ *               checked, and any other content is undefined behaviour.  The
+ *               same holds for ids and the other outputs of earlier steps.
  *   brim0    out int32 [Nd, T]: running counter over active (d, t) pairs taken
  *               device by device, token by token; -1 where token t uses no
  *               expert of device d.  Non-negative values are SFD row indices.

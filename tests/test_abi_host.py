@@ -223,3 +223,24 @@ def test_every_entry_point_refuses_null_buffers_before_launching(occ):
         assert rc == occ.ERR_INVALID_ARG, f"{name} returned {rc}"
         checked.append(name)
     assert len(checked) >= 20
+
+
+@pytest.mark.parametrize("bad", ["duplicate", "missing", "shape", "out_of_range"])
+def test_layer_refuses_a_placement_that_is_not_a_partition(occ, bad):
+    """The kernels index by the placement without checking it, so the binding
+    refuses one that does not hold every expert exactly once (before any buffer
+    is allocated: this runs on the CPU)."""
+    import torch
+    cfg = synth.CONFIGS["tiny_f32"]
+    ds = occ.desc_for(cfg)
+    L = np.arange(cfg.n_experts, dtype=np.int32).reshape(cfg.n_vdev, -1)
+    if bad == "duplicate":
+        L[0, 0] = L[0, 1]
+    elif bad == "missing":
+        L[1, 0] = L[0, 0]
+    elif bad == "shape":
+        L = L.reshape(-1)
+    else:
+        L[0, 0] = cfg.n_experts
+    with pytest.raises(ValueError):
+        occ.OccultMoE(ds, {}, torch.as_tensor(L), device="cpu")
