@@ -244,3 +244,31 @@ def test_layer_refuses_a_placement_that_is_not_a_partition(occ, bad):
         L[0, 0] = cfg.n_experts
     with pytest.raises(ValueError):
         occ.OccultMoE(ds, {}, torch.as_tensor(L), device="cpu")
+
+
+def test_header_is_plain_c_and_links(occ, tmp_path):
+    """occult.h compiles as C99 with warnings as errors, and a C program that
+    takes the address of every declared entry point links against liboccult.so
+    (nothing is run: the program would need a GPU)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_symbols()
+    src = tmp_path / "use_abi.c"
+    src.write_text(
+        '#include "occult.h"\n#include <stdio.h>\n'
+        "int main(void) {\n"
+        "  const void* fns[] = {\n"
+        + "".join(f"    (const void*)&{n},\n" for n in names)
+        + "  };\n"
+        "  occult_desc_t d = {0};\n"
+        "  printf(\"%d %d\\n\", (int)(sizeof fns / sizeof fns[0]), occult_check_desc(&d));\n"
+        "  return 0;\n}\n")
+    lib_dir = os.path.dirname(occ.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                        str(tmp_path / "use_abi"), "-L", lib_dir, "-loccult",
+                        "-Wl,--allow-shlib-undefined"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
