@@ -31,23 +31,27 @@ static __device__ __align__(256) int32_t g_brim_scratch[OCCULT_STATIC_SCRATCH_BY
 
 constexpr int kMaxDevices = 64;
 
-struct ScratchSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t status = cudaSuccess;
-};
-ScratchSlot g_slots[kMaxDevices];
+// Device address of the array on each device, once it has been looked up.
+std::mutex g_slots_mutex;
+void* g_slots[kMaxDevices] = {};
 
-// Device address of the array on the current device, looked up once per device
-// with that device current (a host-side name of the array is not an address the
-// GPU can use).
+// Device address of the array on the current device, looked up with that device
+// current (a host-side name of the array is not an address the GPU can use).
+// Only a successful lookup is kept: after a failed one (say, the device was not
+// usable yet) the next call asks again.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return OCCULT_ERR_CUDA;
-  ScratchSlot& s = g_slots[dev];
-  std::call_once(s.once, [&] { s.status = cudaGetSymbolAddress(&s.ptr, g_brim_scratch); });
-  if (s.status != cudaSuccess || s.ptr == nullptr) return OCCULT_ERR_CUDA;
-  *out = s.ptr;
+  std::lock_guard<std::mutex> lock(g_slots_mutex);
+  if (g_slots[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_brim_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // the failure is reported here, not to a later call
+      return OCCULT_ERR_CUDA;
+    }
+    g_slots[dev] = p;
+  }
+  *out = g_slots[dev];
   return OCCULT_OK;
 }
 

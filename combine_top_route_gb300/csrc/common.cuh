@@ -176,15 +176,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
-// Four rows y0..y3 of the same column window starting at x (box one row high).
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int y0,
-                                            int y1, int y2, int y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-         "r"(smem_u32(bar)) : "memory");
-}
 // 16-byte asynchronous global -> shared copies (L1 bypassed), tracked per thread
 // in commit groups.
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {

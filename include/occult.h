@@ -273,8 +273,9 @@ int occult_build_brim(const occult_desc_t* desc, const int32_t* ids, const float
  *             on the GPU (unordered streams) race and give wrong results; order
  *             them on one stream or with events.
  *   Set-up:   the first call on a device looks up the array's device address
- *             with that device current; make that first call before any stream
- *             capture on the device.
+ *             with that device current (a lookup that fails returns
+ *             OCCULT_ERR_CUDA and is tried again by the next call); make that
+ *             first call before any stream capture on the device.
  */
 #define OCCULT_STATIC_SCRATCH_BYTES 1183744
 int occult_build_brim_noalloc(const occult_desc_t* desc, const int32_t* ids, const float* gates,

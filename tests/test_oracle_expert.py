@@ -84,3 +84,54 @@ def test_stacked_shared_experts_equal_their_sum():
     y = expert.shared_experts(x, ws1, ws2)
     ref = expert.swiglu_expert(x, a1, a2) + expert.swiglu_expert(x, b1, b2)
     np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_shared_gate_closed_form(golden):
+    """sigmoid of +ln 3 is 3/4 and of -ln 3 is 1/4: a flipped sign swaps them."""
+    g = golden("closed_forms.json")["shared_gate"]
+    x = np.array(g["x"])
+    np.testing.assert_allclose(expert.shared_gate(x, np.array(g["w_sg_pos"])), g["s_pos"],
+                               rtol=1e-15)
+    np.testing.assert_allclose(expert.shared_gate(x, np.array(g["w_sg_neg"])), g["s_neg"],
+                               rtol=1e-14)
+
+
+def test_shared_expert_scalar_closed_form(golden):
+    g = golden("closed_forms.json")["shared_expert_scalar"]
+    ws1 = np.array([[g["w_g"]], [g["w_u"]]])
+    ws2 = np.array([[g["w_d"]]])
+    y = expert.shared_experts(np.array([[g["x"]]]), ws1, ws2, np.array([g["w_sg"]]))
+    assert abs(y[0, 0] - g["y"]) < 1e-14
+    # the layer output adds it to the routed experts' Eq. 1 sum
+    w = {"w1": ws1[None], "w2": ws2[None], "ws1": ws1, "ws2": ws2, "w_sg": np.array([g["w_sg"]])}
+    routed = expert.moe_topk(np.array([[g["x"]]]), np.array([[0]]), np.array([[1.0]]),
+                             w["w1"], w["w2"])
+    out = expert.layer_output(np.array([[g["x"]]]), np.array([[0]]), np.array([[1.0]]), w)
+    assert abs(out[0, 0] - (routed[0, 0] + g["y"])) < 1e-14
+
+
+@pytest.mark.parametrize("gated", [True, False])
+def test_shared_experts_match_torch_formulation(gated):
+    """Independent torch-CPU formulation of two stacked shared experts, with and
+    without the sigmoid gate (fp64): each expert computed on its own rows of the
+    stacked weights and summed."""
+    rng = np.random.default_rng(6)
+    T, d, I = 11, 8, 5
+    x = rng.standard_normal((T, d))
+    e1 = rng.standard_normal((2 * I, d)) * 0.3, rng.standard_normal((d, I)) * 0.3
+    e2 = rng.standard_normal((2 * I, d)) * 0.3, rng.standard_normal((d, I)) * 0.3
+    # stacked along the intermediate axis: gate rows of both, then up rows of both
+    ws1 = np.concatenate([e1[0][:I], e2[0][:I], e1[0][I:], e2[0][I:]])
+    ws2 = np.concatenate([e1[1], e2[1]], axis=1)
+    w_sg = rng.standard_normal(d) if gated else None
+    y = expert.shared_experts(x, ws1, ws2, w_sg)
+    tx = torch.from_numpy(x)
+    out = torch.zeros(T, d, dtype=torch.float64)
+    for a, b in (e1, e2):
+        ta, tb = torch.from_numpy(a), torch.from_numpy(b)
+        out += torch.nn.functional.linear(
+            torch.nn.functional.silu(torch.nn.functional.linear(tx, ta[:I]))
+            * torch.nn.functional.linear(tx, ta[I:]), tb)
+    if gated:
+        out = torch.sigmoid(tx @ torch.from_numpy(w_sg))[:, None] * out
+    np.testing.assert_allclose(y, out.numpy(), rtol=1e-12, atol=1e-13)

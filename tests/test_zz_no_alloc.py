@@ -85,3 +85,47 @@ def test_noalloc_rejects_layers_beyond_its_scratch(occ):
     ptrs = [ctypes.c_void_p(dummy.data_ptr())] * 11
     rc = occ.lib().occult_build_brim_noalloc(ctypes.byref(ds), *ptrs, None)
     assert rc == occ.ERR_WORKSPACE
+
+
+def _ids_for(cfg, ds, occ):
+    """Routed ids of the seeded batch (through occult_route: both entry points
+    under test get the same ids, whatever they are) and the device masks."""
+    case = make_case(cfg, device="cpu", tensors=False)
+    T, k = cfg.T, cfg.top_k
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    gates = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    vmask = torch.empty(T, dtype=torch.int32, device="cuda")
+    e2v = torch.as_tensor(case.e2v.astype(np.int32)).cuda()
+    occ.occult_route(ds, case.logits.cuda(), e2v, ids, gates, vmask)
+    L = torch.as_tensor(case.placement.reshape(-1).astype(np.int32)).cuda()
+    return ids, gates, vmask, L
+
+
+@pytest.mark.parametrize("T,Ne,Nd", [(32768, 256, 32), (97600, 64, 8)])
+def test_noalloc_at_its_size_limit(occ, T, Ne, Nd):
+    """The largest layers the static scratch holds (the two figures the header
+    states) are accepted and equal the workspace entry point; one more token is
+    refused with OCCULT_ERR_WORKSPACE before any launch."""
+    cfg = synth.CONFIGS["olmoe_fwd"].with_(name=f"noalloc_{T}_{Ne}", T=T, n_experts=Ne,
+                                           n_vdev=Nd, prof_tokens=4096)
+    ds = occ.desc_for(cfg)
+    assert occ.workspace_size(ds, occ.WS_BUILD_BRIM) <= occ.STATIC_SCRATCH_BYTES
+    ids, gates, vmask, L = _ids_for(cfg, ds, occ)
+    want = _outputs(cfg, ds)
+    ws = torch.empty(occ.workspace_size(ds, occ.WS_BUILD_BRIM), dtype=torch.uint8, device="cuda")
+    occ.occult_build_brim(ds, ids, gates, vmask, L, ws=ws, **want)
+    got = _outputs(cfg, ds)
+    occ.occult_build_brim_noalloc(ds, ids, gates, vmask, L, **got)
+    torch.cuda.synchronize()
+    for n in want:
+        assert torch.equal(got[n], want[n]), f"{n} differs at T={T}, Ne={Ne}"
+
+    over = cfg.with_(T=T + 1)
+    ds1 = occ.desc_for(over)
+    assert occ.workspace_size(ds1, occ.WS_BUILD_BRIM) > occ.STATIC_SCRATCH_BYTES
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    ptrs = [ctypes.c_void_p(dummy.data_ptr())] * 11
+    assert occ.lib().occult_build_brim_noalloc(ctypes.byref(ds1), *ptrs, None) == occ.ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert (dummy == 0).all()
+    assert occ.device_error() == 0
