@@ -65,7 +65,7 @@ def moe_backward(x: np.ndarray, ids: np.ndarray, gates: np.ndarray, w1: np.ndarr
         dh = g * dhp
         dG = dh * U * sig * (1.0 + G * (1.0 - sig))
         dU = dh * s
-        np.add.at(dx, rows, dG @ wg + dU @ wu)
+        dx[rows] += dG @ wg + dU @ wu        # a token holds an expert at most once
         dw2[e] = dyr.T @ (g * h)
         dw1[e, :I] = dG.T @ a
         dw1[e, I:] = dU.T @ a

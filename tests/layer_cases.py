@@ -126,6 +126,18 @@ def oracle_brims(case: Case, ids, gates) -> obrim.Brims:
     return obrim.Brims(ids, gates, case.placement)
 
 
+def scatter_add_rows(dst: np.ndarray, idx: np.ndarray, rows: np.ndarray) -> None:
+    """dst[idx[i]] += rows[i] for every i, repeated indices summed (rows sharing an
+    index are added together first, in order, then once into dst)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    if idx.size == 0:
+        return
+    order = np.argsort(idx, kind="stable")
+    s_idx = idx[order]
+    starts = np.concatenate([[0], np.nonzero(np.diff(s_idx))[0] + 1])
+    dst[s_idx[starts]] += np.add.reduceat(rows[order], starts, axis=0)
+
+
 # Per-element error bounds of intermediates, derived from the arithmetic.  The
 # 2e-2 * rms bar is the layer-output bar; the EPD intermediate h is heavy-tailed
 # (a product silu(G) * U; max|h| reaches ~45 rms), so its bf16 rounding alone
@@ -134,27 +146,42 @@ BF16_HALF_ULP = 2.0 ** -8     # |round_bf16(v) - v| <= 2^-8 |v|
 F32_EPS = 2.0 ** -24
 
 
-def h_bound(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, gate: float, h_ref: np.ndarray,
-            layer_dtype: str) -> np.ndarray:
-    """Bound on |h_gpu - h_ref| for one EPD row.
+def abs_contract(a_abs: np.ndarray, b_abs: np.ndarray) -> np.ndarray:
+    """a_abs @ b_abs for non-negative matrices, as an upper bound: the product is
+    taken in fp32 (fast) and raised by 1 %, which covers its own rounding (a sum
+    of K non-negative fp32 terms, each rounded on the way in, is within
+    (K + 2) 2^-24 of the exact value: under 1 % for K < 160000)."""
+    r = np.asarray(a_abs, dtype=np.float32) @ np.asarray(b_abs, dtype=np.float32)
+    return r.astype(np.float64) * 1.01
 
-    G = W_g a and U = W_u a accumulate K = len(a) products in fp32: their error is
-    at most 2 K 2^-24 sum|w||a| (twice the textbook gamma_K, for any internal
+
+def h_bound(a: np.ndarray, wg: np.ndarray, wu: np.ndarray, gate, h_ref: np.ndarray,
+            layer_dtype: str) -> np.ndarray:
+    """Bound on |h_gpu - h_ref| for one EPD row (a [d], gate a scalar, h_ref [I]) or
+    for several rows of one expert at once (a [n, d], gate [n], h_ref [n, I]).
+
+    G = W_g a and U = W_u a accumulate K = d products in fp32: their error is at
+    most 2 K 2^-24 sum|w||a| (twice the textbook gamma_K, for any internal
     ordering of the tensor-core sum).  silu has slope <= 1.1, so the fp32 value of
     h = g silu(G) U is off by at most g (1.1 |U| dG + |silu G| dU + 1.1 dG dU) plus
     a few fp32 roundings; bf16 layers then round h once more (2^-8 relative).
     """
-    a = a.astype(np.float64)
-    K = a.size
-    dG = 2 * K * F32_EPS * (np.abs(wg) @ np.abs(a))
-    dU = 2 * K * F32_EPS * (np.abs(wu) @ np.abs(a))
-    G = wg.astype(np.float64) @ a
-    U_abs = np.abs(wu.astype(np.float64) @ a)
+    single = np.ndim(a) == 1
+    a = np.atleast_2d(np.asarray(a, dtype=np.float64))
+    wg = np.asarray(wg, dtype=np.float64)
+    wu = np.asarray(wu, dtype=np.float64)
+    g = np.abs(np.atleast_1d(np.asarray(gate, dtype=np.float64)))[:, None]
+    h_ref = np.atleast_2d(h_ref)
+    K = a.shape[1]
+    aa = np.abs(a)
+    dG = 2 * K * F32_EPS * abs_contract(aa, np.abs(wg).T)
+    dU = 2 * K * F32_EPS * abs_contract(aa, np.abs(wu).T)
+    G = a @ wg.T
+    U_abs = np.abs(a @ wu.T)
     s_abs = np.abs(G / (1.0 + np.exp(-G)))
-    d32 = abs(gate) * (1.1 * U_abs * dG + s_abs * dU + 1.1 * dG * dU) + 8 * F32_EPS * np.abs(h_ref)
-    if layer_dtype == "f32":
-        return d32
-    return BF16_HALF_ULP * (np.abs(h_ref) + d32) + d32
+    d32 = g * (1.1 * U_abs * dG + s_abs * dU + 1.1 * dG * dU) + 8 * F32_EPS * np.abs(h_ref)
+    out = d32 if layer_dtype == "f32" else BF16_HALF_ULP * (np.abs(h_ref) + d32) + d32
+    return out[0] if single else out
 
 
 def sfd_bound(w2: np.ndarray, h_abs_rows, layer_dtype: str) -> np.ndarray:
@@ -171,6 +198,17 @@ def sfd_bound(w2: np.ndarray, h_abs_rows, layer_dtype: str) -> np.ndarray:
     rel = (1.01 * BF16_HALF_ULP if layer_dtype == "bf16" else 8 * F32_EPS)
     rel += (2 * I + 2 * len(h_abs_rows) + 4) * F32_EPS
     return rel * B
+
+
+# Random-walk bounds.  The worst-case error of a sum of K terms, each carrying an
+# independent rounding error e_i with |e_i| <= b_i, is sum b_i; the errors of
+# round-to-nearest of distinct values behave as independent and zero-mean, and
+# for such errors Hoeffding's inequality gives |sum e_i| <= LAMBDA sqrt(sum b_i^2)
+# except with probability 2 exp(-LAMBDA^2 / 2) (4e-22 per element at 10).  The
+# long reductions of dgates (over I) and dx (over 2I) use this form: their
+# worst-case bounds are sqrt(K) times looser than the errors the arithmetic
+# makes and would let a dropped EPD row pass.
+LAMBDA = 10.0
 
 
 def expert_backward_bounds(x, dy, w1e, w2e, gate, layer_dtype="bf16"):
@@ -197,8 +235,10 @@ def expert_backward_bounds(x, dy, w1e, w2e, gate, layer_dtype="bf16"):
     acc = lambda K, m: 2 * K * F32_EPS * m  # noqa: E731  fp32 accumulation of K terms
     G = x @ wg.T
     U = x @ wu.T
-    aG = acc(d, np.abs(x) @ np.abs(wg).T)
-    aU = acc(d, np.abs(x) @ np.abs(wu).T)
+    # fp32 accumulation of G and U over d terms, as a random walk (see dh' below)
+    acc_rw = lambda K, m: LAMBDA * np.sqrt(K) * F32_EPS * m  # noqa: E731
+    aG = acc_rw(d, abs_contract(np.abs(x), np.abs(wg).T))
+    aU = acc_rw(d, abs_contract(np.abs(x), np.abs(wu).T))
     dG_st = aG * (1 + u) + u * np.abs(G)      # |stored bf16 G - G|
     dU_st = aU * (1 + u) + u * np.abs(U)
     sig = 1.0 / (1.0 + np.exp(-G))
@@ -207,12 +247,19 @@ def expert_backward_bounds(x, dy, w1e, w2e, gate, layer_dtype="bf16"):
     h1_32 = np.abs(g) * (1.1 * np.abs(U) * aG + np.abs(s) * aU + 1.1 * aG * aU) + 8 * F32_EPS * np.abs(h1)
     h1_b = h1_32 * (1 + u) + u * np.abs(h1)
     dhp = dy @ wd
-    ddhp = acc(d, np.abs(dy) @ np.abs(wd))
+    # dh' = dy W_d: its fp32 accumulation error over d terms as a random walk
+    # (Higham and Mary's probabilistic bound, LAMBDA sqrt(d) 2^-24 sum|terms|):
+    # its worst case, 2 d 2^-24 sum|terms|, would dominate every bound below it
+    ddhp = acc_rw(d, abs_contract(np.abs(dy), np.abs(wd)))
     ds = 1.1 * dG_st
     sU = s * U
     dg = np.sum(dhp * sU, axis=1)
-    dg_b = np.sum(ddhp * np.abs(sU) + np.abs(dhp) * (ds * np.abs(U) + np.abs(s) * dU_st + ds * dU_st),
-                  axis=1) + acc(I, np.sum(np.abs(dhp * sU), axis=1)) + 1e-30
+    # dg sums I products whose errors come from independent roundings (fp32 sums
+    # of other output columns, bf16 G and U of other units): a random-walk bound
+    # on them (Hoeffding, LAMBDA), the fp32 sum of the products worst case
+    dg_terms = ddhp * np.abs(sU) + np.abs(dhp) * (ds * np.abs(U) + np.abs(s) * dU_st + ds * dU_st)
+    dg_b = (LAMBDA * np.sqrt(np.sum(dg_terms ** 2, axis=1))
+            + acc(I, np.sum(np.abs(dhp * sU), axis=1)) + 1e-30)
     silu1 = sig * (1.0 + G * (1.0 - sig))
     dG = g * dhp * U * silu1
     dU = g * dhp * s
@@ -224,9 +271,16 @@ def expert_backward_bounds(x, dy, w1e, w2e, gate, layer_dtype="bf16"):
     dU_b = dU_pre * (1 + u) + u * np.abs(dU)
     dx_rows = dG @ wg + dU @ wu
     dGa, dUa = np.abs(dG) + dG_b, np.abs(dU) + dU_b
-    dx_rows_b = dG_b @ np.abs(wg) + dU_b @ np.abs(wu) + acc(2 * I, dGa @ np.abs(wg) + dUa @ np.abs(wu))
+    # each bound below is (rounding of the operands) + (fp32 accumulation of K
+    # terms); both are contractions with the same absolute operand, so they are
+    # summed before the one matrix product
+    # a dx row contracts 2I values of dG | dU with independent rounding errors
+    # (random-walk bound, LAMBDA) plus the worst-case fp32 accumulation
+    dx_rows_b = (LAMBDA * np.sqrt(abs_contract(dG_b ** 2, wg ** 2) + abs_contract(dU_b ** 2, wu ** 2))
+                 + abs_contract(acc(2 * I, dGa), np.abs(wg)) + abs_contract(acc(2 * I, dUa), np.abs(wu)))
     ax = np.abs(x)
-    dW1_b = np.concatenate([dG_b.T @ ax, dU_b.T @ ax]) + acc(n, np.concatenate([dGa.T @ ax, dUa.T @ ax]))
-    dW2_b = np.abs(dy).T @ h1_b + acc(n, np.abs(dy).T @ (np.abs(h1) + h1_b))
+    dW1_b = np.concatenate([abs_contract((dG_b + acc(n, dGa)).T, ax),
+                            abs_contract((dU_b + acc(n, dUa)).T, ax)])
+    dW2_b = abs_contract(np.abs(dy).T, h1_b + acc(n, np.abs(h1) + h1_b))
     return dict(dG=dG, dU=dU, dG_b=dG_b, dU_b=dU_b, dx_rows=dx_rows, dx_rows_b=dx_rows_b,
                 dg=dg, dg_b=dg_b, h1=h1, h1_b=h1_b, dW1_b=dW1_b, dW2_b=dW2_b)

@@ -14,7 +14,7 @@ import torch
 
 import synth
 from layer_cases import F32_EPS, assert_close_layer, expert_backward_bounds, make_case, \
-    oracle_brims, reference_output
+    oracle_brims, reference_output, scatter_add_rows
 from oracle import backward as obackward
 from oracle import brim as obrim
 from oracle import routing as orouting
@@ -222,8 +222,8 @@ def test_sharded_training_step(occ):
     for e in np.unique(ids):
         r, sl = np.nonzero(ids == e)
         bb = expert_backward_bounds(x[r], dy_h[r], w1[e], w2[e], gates[r, sl])
-        np.add.at(dx_b, r, bb["dx_rows_b"])
-        np.add.at(dx_abs, r, np.abs(bb["dx_rows"]) + bb["dx_rows_b"])
+        scatter_add_rows(dx_b, r, bb["dx_rows_b"])
+        scatter_add_rows(dx_abs, r, np.abs(bb["dx_rows"]) + bb["dx_rows_b"])
     dx_b += 2 * k * F32_EPS * dx_abs
     err = np.abs(g_sh[0].cpu().numpy().astype(np.float64) - ref["dx"])
     assert (err <= dx_b + 1e-30).all()
