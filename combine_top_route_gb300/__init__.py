@@ -100,6 +100,11 @@ _SIGNATURES = {
                                          _I32, _VP]),
     "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 16 + [ctypes.c_size_t, _VP]),
     "occult_expert_bwd_merge": (ctypes.c_int, [_D] + [_VP] * 17 + [ctypes.c_size_t, _VP]),
+    "occult_expert_dgrad_down": (ctypes.c_int, [_D] + [_VP] * 10 + [ctypes.c_size_t, _VP]),
+    "occult_expert_dgrad_up": (ctypes.c_int, [_D] + [_VP] * 7 + [_I32, _VP]),
+    "occult_expert_wgrad_down": (ctypes.c_int, [_D] + [_VP] * 7),
+    "occult_expert_wgrad_up": (ctypes.c_int, [_D] + [_VP] * 7),
+    "occult_zero_f32": (ctypes.c_int, [_VP, ctypes.c_int64, _VP]),
     "occult_gate_grad": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
                                             ctypes.c_size_t, _VP]),
@@ -328,6 +333,61 @@ def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, pla
           _dev(dg_epd, f32, T * k, "dg_epd"),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
+
+
+def occult_expert_dgrad_down(desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd,
+                             dgu_epd, dg_epd, ws, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
+    need = workspace_size(desc, WS_EXPERT_BWD)
+    _call("occult_expert_dgrad_down", ctypes.byref(desc),
+          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd"),
+          _dev(epd_src, i32, T * k, "epd_src"), _dev(epd_gate, f32, T * k, "epd_gate"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(placement, i32, Ne, "placement"),
+          _dev(w2, dt, Ne * d * I, "w2"), _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"),
+          _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
+          _stream(stream))
+
+
+def occult_expert_dgrad_up(desc, dgu_epd, epd_src, exp_off, placement, w1, dx, sfd_tok=None,
+                           zero_dx=False, stream=None):
+    """dx rows of the backward; merged into dx [T, d] when sfd_tok is given (occult.h)."""
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, i32 = desc.torch_dtype, torch.int32
+    _call("occult_expert_dgrad_up", ctypes.byref(desc),
+          _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(placement, i32, Ne, "placement"),
+          _dev(w1, dt, Ne * 2 * I * d, "w1"),
+          _dev(sfd_tok, i32, T * min(k, desc.n_vdev), "sfd_tok", nullable=True),
+          _dev(dx, torch.float32, (T if sfd_tok is not None else T * k) * d, "dx"),
+          int(bool(zero_dx)), _stream(stream))
+
+
+def occult_expert_wgrad_down(desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, i32 = desc.torch_dtype, torch.int32
+    _call("occult_expert_wgrad_down", ctypes.byref(desc),
+          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd"),
+          _dev(epd_src, i32, T * k, "epd_src"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(placement, i32, Ne, "placement"), _dev(h_epd, dt, T * k * I, "h_epd"),
+          _dev(dw2, torch.float32, Ne * d * I, "dw2"), _stream(stream))
+
+
+def occult_expert_wgrad_up(desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1, stream=None):
+    T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
+    dt, i32 = desc.torch_dtype, torch.int32
+    _call("occult_expert_wgrad_up", ctypes.byref(desc),
+          _dev(x_sfd, dt, T * min(k, desc.n_vdev) * d, "x_sfd"),
+          _dev(epd_src, i32, T * k, "epd_src"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(placement, i32, Ne, "placement"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
+          _dev(dw1, torch.float32, Ne * 2 * I * d, "dw1"), _stream(stream))
+
+
+def occult_zero_f32(buf, stream=None):
+    """buf (fp32, contiguous, on the device) = 0."""
+    _call("occult_zero_f32", _dev(buf, torch.float32, buf.numel(), "buf"),
+          ctypes.c_int64(buf.numel()), _stream(stream))
 
 
 def occult_gate_grad(desc, ids, placement, brim0, seg_off, brim1, exp_off, dg_epd, dgates,

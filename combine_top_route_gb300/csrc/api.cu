@@ -397,6 +397,116 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g) : launch_grouped_gemm_f32(ctx, g);
 }
 
+// The four GEMMs of the expert backward.  Argument checks are done by the public
+// entry points; T > 0 here.
+
+// dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg
+static int dgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dy_sfd,
+                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
+                      const int32_t* placement, const void* w2, const void* gu_epd,
+                      void* dgu_epd, float* dg_epd, void* ws) {
+  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
+  float* dg_part = static_cast<float*>(ws);
+  GroupedGemm g;
+  g.a_mode = OP_GATHER_K;
+  g.b_mode = OP_TMA_MN;
+  g.epi = EPI_SWIGLU_BWD;
+  g.A = dy_sfd; g.a_rows = n_sfd_max; g.a_cols = d;
+  g.gather = epd_src;
+  g.B = w2; g.b_rows = static_cast<int64_t>(Ne) * d; g.b_cols = I;
+  g.b_group_rows = d;
+  g.n_groups = Ne;
+  g.seg_off = exp_off; g.seg_group = placement; g.n_seg = Ne; g.max_rows = rows;
+  g.K = d; g.N_out = I;
+  g.row_gate = epd_gate;
+  g.out = dgu_epd; g.ldo = 2ll * I;
+  g.gu_in = gu_epd; g.dg_part = dg_part;
+  int rc = launch_grouped_gemm_bf16(ctx, g);
+  if (rc) return rc;
+  return launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), 2 * ((I + 255) / 256), dg_epd);
+}
+
+// dx_epd = [dG|dU] . [W_g; W_u] (W1 read MN-major), fp32; with sfd_tok given the
+// rows are added into dx[token] (fp32 atomics) instead of written to dx_out's EPD rows
+static int dgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dgu_epd,
+                    const int32_t* epd_src, const int32_t* exp_off, const int32_t* placement,
+                    const void* w1, const int32_t* sfd_tok, float* dx_out) {
+  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
+  GroupedGemm h;
+  h.a_mode = OP_TMA_K;
+  h.b_mode = OP_TMA_MN;
+  h.epi = EPI_F32;
+  h.A = dgu_epd; h.a_rows = rows; h.a_cols = 2ll * I;
+  h.B = w1; h.b_rows = 2ll * I * Ne; h.b_cols = d;
+  h.b_group_rows = 2ll * I;
+  h.n_groups = Ne;
+  h.seg_off = exp_off; h.seg_group = placement; h.n_seg = Ne; h.max_rows = rows;
+  h.K = 2 * I; h.N_out = d;
+  h.out = dx_out; h.ldo = d;
+  if (sfd_tok) {
+    h.out_src = epd_src;
+    h.out_tok = sfd_tok;
+  }
+  return launch_grouped_gemm_bf16(ctx, h);
+}
+
+// dW_d[e] = sum over e's rows of dy_sfd[src] (x) h' : M = d, N = I
+static int wgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dy_sfd,
+                      const int32_t* epd_src, const int32_t* exp_off, const int32_t* placement,
+                      const void* h_epd, float* dw2) {
+  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
+  GroupedGemm w;
+  w.wgrad = true;
+  w.a_mode = OP_GATHER_MN;
+  w.b_mode = OP_TMA_MN;
+  w.epi = EPI_F32;
+  w.A = dy_sfd; w.a_rows = n_sfd_max; w.a_cols = d;
+  w.gather = epd_src;
+  w.B = h_epd; w.b_rows = rows; w.b_cols = I;
+  w.seg_off = exp_off; w.seg_group = placement; w.n_seg = Ne;
+  w.M_total = d; w.N_out = I;
+  w.out = dw2; w.ldo = I; w.out_group_stride = static_cast<int64_t>(d) * I;
+  return launch_grouped_gemm_bf16(ctx, w);
+}
+
+// [dW_g; dW_u][e] = sum over e's rows of [dG|dU] (x) x_sfd[src] : M = 2I, N = d
+static int wgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* x_sfd,
+                    const int32_t* epd_src, const int32_t* exp_off, const int32_t* placement,
+                    const void* dgu_epd, float* dw1) {
+  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
+  const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
+  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
+  GroupedGemm v;
+  v.wgrad = true;
+  v.a_mode = OP_TMA_MN;
+  v.b_mode = OP_GATHER_MN;
+  v.epi = EPI_F32;
+  v.A = dgu_epd; v.a_rows = rows; v.a_cols = 2ll * I;
+  v.B = x_sfd; v.b_rows = n_sfd_max; v.b_cols = d;
+  v.gather = epd_src;
+  v.seg_off = exp_off; v.seg_group = placement; v.n_seg = Ne;
+  v.M_total = 2 * I; v.N_out = d;
+  v.out = dw1; v.ldo = d; v.out_group_stride = 2ll * I * d;
+  return launch_grouped_gemm_bf16(ctx, v);
+}
+
+static int zero_weights(const LaunchCtx& ctx, float* w, size_t n) {
+  return cudaMemsetAsync(w, 0, n * sizeof(float), ctx.stream) == cudaSuccess ? OCCULT_OK
+                                                                             : OCCULT_ERR_CUDA;
+}
+
+static size_t w1_elems(const occult_desc_t* desc) {
+  return static_cast<size_t>(desc->n_experts) * 2 * desc->inter * desc->d;
+}
+static size_t w2_elems(const occult_desc_t* desc) {
+  return static_cast<size_t>(desc->n_experts) * desc->d * desc->inter;
+}
+
 // The expert backward; with sfd_tok given, the dgrad through [W_g; W_u] adds its
 // rows into dx[token] (fp32 atomics) instead of writing the EPD rows to dx_out.
 static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
@@ -414,89 +524,23 @@ static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
-  if (sfd_tok && desc->T > 0) {
+  if (desc->T == 0) {
+    // no rows: every weight gradient is zero
+    rc = zero_weights(ctx, dw1, w1_elems(desc));
+    return rc ? rc : zero_weights(ctx, dw2, w2_elems(desc));
+  }
+  if (sfd_tok) {
     rc = launch_zero_f32(ctx, dx_out, static_cast<size_t>(desc->T) * desc->d);
     if (rc) return rc;
   }
-  if (desc->T == 0) {
-    // no rows: every weight gradient is zero
-    const size_t n1 = static_cast<size_t>(desc->n_experts) * 2 * desc->inter * desc->d;
-    const size_t n2 = static_cast<size_t>(desc->n_experts) * desc->d * desc->inter;
-    if (cudaMemsetAsync(dw1, 0, n1 * sizeof(float), ctx.stream) != cudaSuccess ||
-        cudaMemsetAsync(dw2, 0, n2 * sizeof(float), ctx.stream) != cudaSuccess)
-      return OCCULT_ERR_CUDA;
-    return OCCULT_OK;
-  }
-  const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
-  const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
-  const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
-  float* dg_part = static_cast<float*>(ws);
-  {
-    // dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg
-    GroupedGemm g;
-    g.a_mode = OP_GATHER_K;
-    g.b_mode = OP_TMA_MN;
-    g.epi = EPI_SWIGLU_BWD;
-    g.A = dy_sfd; g.a_rows = n_sfd_max; g.a_cols = d;
-    g.gather = epd_src;
-    g.B = w2; g.b_rows = static_cast<int64_t>(Ne) * d; g.b_cols = I;
-    g.b_group_rows = d;
-    g.n_groups = Ne;
-    g.seg_off = exp_off; g.seg_group = placement; g.n_seg = Ne; g.max_rows = rows;
-    g.K = d; g.N_out = I;
-    g.row_gate = epd_gate;
-    g.out = dgu_epd; g.ldo = 2ll * I;
-    g.gu_in = gu_epd; g.dg_part = dg_part;
-    rc = launch_grouped_gemm_bf16(ctx, g);
-    if (rc) return rc;
-    rc = launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), 2 * ((I + 255) / 256), dg_epd);
-    if (rc) return rc;
-    // dx_epd = [dG|dU] . [W_g; W_u] (W1 read MN-major), fp32
-    GroupedGemm h;
-    h.a_mode = OP_TMA_K;
-    h.b_mode = OP_TMA_MN;
-    h.epi = EPI_F32;
-    h.A = dgu_epd; h.a_rows = rows; h.a_cols = 2ll * I;
-    h.B = w1; h.b_rows = 2ll * I * Ne; h.b_cols = d;
-    h.b_group_rows = 2ll * I;
-    h.n_groups = Ne;
-    h.seg_off = exp_off; h.seg_group = placement; h.n_seg = Ne; h.max_rows = rows;
-    h.K = 2 * I; h.N_out = d;
-    h.out = dx_out; h.ldo = d;
-    if (sfd_tok) {
-      h.out_src = epd_src;
-      h.out_tok = sfd_tok;
-    }
-    rc = launch_grouped_gemm_bf16(ctx, h);
-    if (rc) return rc;
-  }
-  // dW_d[e] = sum over e's rows of dy_sfd[src] (x) h' : M = d, N = I
-  GroupedGemm w;
-  w.wgrad = true;
-  w.a_mode = OP_GATHER_MN;
-  w.b_mode = OP_TMA_MN;
-  w.epi = EPI_F32;
-  w.A = dy_sfd; w.a_rows = n_sfd_max; w.a_cols = d;
-  w.gather = epd_src;
-  w.B = h_epd; w.b_rows = rows; w.b_cols = I;
-  w.seg_off = exp_off; w.seg_group = placement; w.n_seg = Ne;
-  w.M_total = d; w.N_out = I;
-  w.out = dw2; w.ldo = I; w.out_group_stride = static_cast<int64_t>(d) * I;
-  rc = launch_grouped_gemm_bf16(ctx, w);
+  rc = dgrad_down(ctx, desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd, dgu_epd,
+                  dg_epd, ws);
   if (rc) return rc;
-  // [dW_g; dW_u][e] = sum over e's rows of [dG|dU] (x) x_sfd[src] : M = 2I, N = d
-  GroupedGemm v;
-  v.wgrad = true;
-  v.a_mode = OP_TMA_MN;
-  v.b_mode = OP_GATHER_MN;
-  v.epi = EPI_F32;
-  v.A = dgu_epd; v.a_rows = rows; v.a_cols = 2ll * I;
-  v.B = x_sfd; v.b_rows = n_sfd_max; v.b_cols = d;
-  v.gather = epd_src;
-  v.seg_off = exp_off; v.seg_group = placement; v.n_seg = Ne;
-  v.M_total = 2 * I; v.N_out = d;
-  v.out = dw1; v.ldo = d; v.out_group_stride = 2ll * I * d;
-  return launch_grouped_gemm_bf16(ctx, v);
+  rc = dgrad_up(ctx, desc, dgu_epd, epd_src, exp_off, placement, w1, sfd_tok, dx_out);
+  if (rc) return rc;
+  rc = wgrad_down(ctx, desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2);
+  if (rc) return rc;
+  return wgrad_up(ctx, desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1);
 }
 
 int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
@@ -518,6 +562,78 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
   if (desc && desc->T > 0 && !sfd_tok) return OCCULT_ERR_INVALID_ARG;
   return expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
                     gu_epd, dgu_epd, dx, sfd_tok, dw1, dw2, dg_epd, ws, ws_bytes, stream);
+}
+
+int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
+                             const int32_t* epd_src, const float* epd_gate,
+                             const int32_t* exp_off, const int32_t* placement, const void* w2,
+                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* ws,
+                             size_t ws_bytes, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(exp_off && placement && w2);
+  OCCULT_REQUIRE(desc->T == 0 || (dy_sfd && epd_src && epd_gate && gu_epd && dgu_epd && dg_epd));
+  const size_t need = expert_bwd_ws_bytes(*desc);
+  if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
+  OCCULT_CTX(stream);
+  if (desc->T == 0) return OCCULT_OK;
+  return dgrad_down(ctx, desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd, dgu_epd,
+                    dg_epd, ws);
+}
+
+int occult_expert_dgrad_up(const occult_desc_t* desc, const void* dgu_epd, const int32_t* epd_src,
+                           const int32_t* exp_off, const int32_t* placement, const void* w1,
+                           const int32_t* sfd_tok, float* dx, int32_t zero_dx,
+                           occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(exp_off && placement && w1);
+  OCCULT_REQUIRE(zero_dx == 0 || zero_dx == 1);
+  OCCULT_REQUIRE(!(zero_dx && !sfd_tok));
+  OCCULT_REQUIRE(desc->T == 0 || (dgu_epd && epd_src && dx));
+  OCCULT_CTX(stream);
+  if (desc->T == 0) return OCCULT_OK;
+  if (zero_dx) {
+    rc = launch_zero_f32(ctx, dx, static_cast<size_t>(desc->T) * desc->d);
+    if (rc) return rc;
+  }
+  return dgrad_up(ctx, desc, dgu_epd, epd_src, exp_off, placement, w1, sfd_tok, dx);
+}
+
+int occult_expert_wgrad_down(const occult_desc_t* desc, const void* dy_sfd,
+                             const int32_t* epd_src, const int32_t* exp_off,
+                             const int32_t* placement, const void* h_epd, float* dw2,
+                             occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(exp_off && placement && dw2);
+  OCCULT_REQUIRE(desc->T == 0 || (dy_sfd && epd_src && h_epd));
+  OCCULT_CTX(stream);
+  if (desc->T == 0) return zero_weights(ctx, dw2, w2_elems(desc));
+  return wgrad_down(ctx, desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2);
+}
+
+int occult_expert_wgrad_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
+                           const int32_t* exp_off, const int32_t* placement,
+                           const void* dgu_epd, float* dw1, occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(exp_off && placement && dw1);
+  OCCULT_REQUIRE(desc->T == 0 || (x_sfd && epd_src && dgu_epd));
+  OCCULT_CTX(stream);
+  if (desc->T == 0) return zero_weights(ctx, dw1, w1_elems(desc));
+  return wgrad_up(ctx, desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1);
+}
+
+int occult_zero_f32(float* buf, int64_t n, occult_stream_t stream) {
+  OCCULT_REQUIRE(n >= 0 && (n == 0 || buf));
+  OCCULT_CTX(stream);
+  if (n == 0) return OCCULT_OK;
+  return launch_zero_f32(ctx, buf, static_cast<size_t>(n));
 }
 
 int occult_gate_grad(const occult_desc_t* desc, const int32_t* ids, const int32_t* placement,

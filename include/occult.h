@@ -487,6 +487,63 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
                             float* dg_epd, void* ws, size_t ws_bytes, occult_stream_t stream);
 
 /*
+ * The four GEMMs of occult_expert_bwd as separate calls, for callers that time,
+ * overlap or reorder them (same derivatives of Eq. 1, same layouts; the paper
+ * gives no backward pseudo-code, Sec. 1).  Run in this order they equal
+ * occult_expert_bwd / occult_expert_bwd_merge.  bf16 layers only.
+ *
+ * occult_expert_dgrad_down -- dh'_r = W_d[e]^T dy_sfd[src_r], then dg_r and
+ *   dG | dU as in occult_expert_bwd.
+ *   dgu_epd out bf16 [T*k, 2I];  dg_epd out fp32 [T*k];
+ *   ws      occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
+ */
+int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
+                             const int32_t* epd_src, const float* epd_gate,
+                             const int32_t* exp_off, const int32_t* placement, const void* w2,
+                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* ws,
+                             size_t ws_bytes, occult_stream_t stream);
+
+/*
+ * occult_expert_dgrad_up -- dx rows [dG | dU]_r . [W_g; W_u] (fp32).
+ *   sfd_tok NULL: dx is dx_epd, out fp32 [T*k, d], one row per EPD row (merge it
+ *            with occult_combine); zero_dx must be 0.
+ *   sfd_tok given (int32 [T*min(k,Nd)], token of every SFD row): dx is fp32
+ *            [T, d] and every row is added into its token's row with fp32 atomics
+ *            (no fixed order); zero_dx = 1 zeroes dx first, 0 adds to it.
+ */
+int occult_expert_dgrad_up(const occult_desc_t* desc, const void* dgu_epd, const int32_t* epd_src,
+                           const int32_t* exp_off, const int32_t* placement, const void* w1,
+                           const int32_t* sfd_tok, float* dx, int32_t zero_dx,
+                           occult_stream_t stream);
+
+/*
+ * occult_expert_wgrad_down -- dw2[e] = sum over e's EPD rows r of
+ *   dy_sfd[src_r] h'_r^T, out fp32 [Ne, d, I] (written; zeros for experts
+ *   without rows).
+ */
+int occult_expert_wgrad_down(const occult_desc_t* desc, const void* dy_sfd,
+                             const int32_t* epd_src, const int32_t* exp_off,
+                             const int32_t* placement, const void* h_epd, float* dw2,
+                             occult_stream_t stream);
+
+/*
+ * occult_expert_wgrad_up -- dw1[e] = sum over e's EPD rows r of
+ *   [dG | dU]_r x_sfd[src_r]^T, out fp32 [Ne, 2I, d] (written; zeros for experts
+ *   without rows).
+ */
+int occult_expert_wgrad_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
+                           const int32_t* exp_off, const int32_t* placement,
+                           const void* dgu_epd, float* dw1, occult_stream_t stream);
+
+/*
+ * occult_zero_f32 -- buf[0..n) = 0 (fp32), asynchronously: the starting value of
+ * a buffer that fp32 atomic merges add into (Sec. 3.1 footnote 3: the merging
+ * SMM adds into an fp32 tensor), e.g. y before occult_expert_down_merge with
+ * zero_y = 0, or dx before occult_expert_dgrad_up with zero_dx = 0.
+ */
+int occult_zero_f32(float* buf, int64_t n, occult_stream_t stream);
+
+/*
  * occult_gate_grad -- gate gradients back in token order: dgates[t, j] =
  * dg_epd[EPD row of (t, ids[t, j])], the row found as in the combine (BRIM0 gives
  * the token's received row on the expert's device, BRIM1 its EPD row).

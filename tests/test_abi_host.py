@@ -189,7 +189,18 @@ def test_host_placement_on_profiled_counts(occ):
 
 # entry points that take no layer descriptor first (checked by their own tests)
 _NOT_DESC_FIRST = ("occult_strerror", "occult_check_desc", "occult_workspace_size",
-                   "occult_device_error", "occult_selftest_wait", "occult_place")
+                   "occult_device_error", "occult_selftest_wait", "occult_place",
+                   "occult_zero_f32")
+
+
+def test_zero_f32_refuses_bad_arguments(occ):
+    """A null buffer with a non-zero length, or a negative length, is refused on
+    the host."""
+    L = occ.lib()
+    assert L.occult_zero_f32(None, ctypes.c_int64(16), None) == occ.ERR_INVALID_ARG
+    buf = (ctypes.c_float * 4)()
+    assert L.occult_zero_f32(ctypes.cast(buf, ctypes.c_void_p), ctypes.c_int64(-1),
+                             None) == occ.ERR_INVALID_ARG
 
 
 def test_every_entry_point_refuses_null_buffers_before_launching(occ):

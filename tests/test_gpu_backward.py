@@ -168,3 +168,47 @@ def test_atomic_and_ordered_merges_agree(occ, name):
     assert (moe_a.dlogits.cpu().numpy() == moe_o.dlogits.cpu().numpy()).all()
     err = np.abs(out_a[0].astype(np.float64) - out_o[0])
     assert (err <= 2 * cfg.top_k * F32_EPS * dx_abs + 1e-30).all()
+
+
+@pytest.mark.parametrize("name", ["train_slice_1024", "pair_ragged"])
+def test_split_backward_equals_fused(occ, name):
+    """The four backward GEMMs called one by one (occult_expert_dgrad_down,
+    _dgrad_up, _wgrad_down, _wgrad_up) give the fused call's results: the weight
+    and gate gradients bit for bit, dx (fp32 atomic adds in no fixed order)
+    within 2 k 2^-24 sum|rows|; so does the ordered form (EPD rows + combine)."""
+    cfg = CASES[name]
+    case = make_case(cfg)
+    dy = synth.upstream_grad(cfg, device="cuda")
+    moe, (dx, dw1, dw2, dgates) = train_step(occ, case, dy)   # the fused call
+    ds = moe.desc
+    dg_epd = moe.dg_epd.clone()
+    dgu = torch.empty_like(moe.dgu_epd)
+    dg2 = torch.empty_like(moe.dg_epd)
+    dx2 = torch.full_like(moe.dx, float("nan"))
+    dw1_2 = torch.full_like(moe.dw1, float("nan"))
+    dw2_2 = torch.full_like(moe.dw2, float("nan"))
+    occ.occult_expert_dgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
+                                 moe.placement, moe.w["w2"], moe.gu_epd, dgu, dg2, moe.bwd_ws)
+    occ.occult_expert_dgrad_up(ds, dgu, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
+                               dx2, sfd_tok=moe.sfd_tok, zero_dx=True)
+    occ.occult_expert_wgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.exp_off, moe.placement,
+                                 moe.h_epd, dw2_2)
+    occ.occult_expert_wgrad_up(ds, moe.x_sfd, moe.epd_src, moe.exp_off, moe.placement, dgu,
+                               dw1_2)
+    # the ordered form: fp32 EPD rows, merged by the combine
+    dx_epd = torch.empty(cfg.T * cfg.top_k, cfg.d, dtype=torch.float32, device="cuda")
+    occ.occult_expert_dgrad_up(ds, dgu, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
+                               dx_epd)
+    dx3 = torch.empty_like(moe.dx)
+    occ.occult_combine(ds, dx_epd, moe.brim0, moe.seg_off, moe.brim1, moe.exp_off, dx3)
+    torch.cuda.synchronize()
+    assert occ.device_error() == 0
+    assert torch.equal(dgu, moe.dgu_epd) and torch.equal(dg2, dg_epd)
+    assert (dw1_2.cpu().numpy() == dw1).all() and (dw2_2.cpu().numpy() == dw2).all()
+    dx_abs = np.zeros((cfg.T, cfg.d))
+    tok = moe.sfd_tok.cpu().numpy()[moe.epd_src.cpu().numpy()]
+    scatter_add_rows(dx_abs, tok, np.abs(dx_epd.cpu().numpy().astype(np.float64)))
+    bound = 2 * cfg.top_k * F32_EPS * dx_abs + 1e-30
+    for got in (dx2, dx3):
+        err = np.abs(got.cpu().numpy().astype(np.float64) - dx)
+        assert (err <= bound).all()
