@@ -176,6 +176,28 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
+// 2-D tiled TMA store of a box from this CTA's shared memory; tracked in bulk
+// groups of the issuing thread (bulk_commit / bulk_wait_read / bulk_wait).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x,
+                                             int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+      :: "l"(map), "r"(smem_u32(smem_src)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until the bulk groups of this thread, all but the newest N, have read
+// their shared-memory sources (the buffers may be overwritten).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+// Waits until the bulk groups of this thread, all but the newest N, have completed.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
+}
 // 16-byte asynchronous global -> shared copies (L1 bypassed), tracked per thread
 // in commit groups.
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc) {

@@ -70,8 +70,15 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr bool epi_staged(int epi, bool swap = false) {
   return swap || epi != EPI_SWIGLU;
 }
+// The SwiGLU backward's epilogue keeps two 4 KB slots a warp (G | U of one 32 x 32
+// chunk copied ahead of use, dG | dU written back in place): 64 KB, which a pair
+// pays for with one operand stage.
+__host__ __device__ constexpr int epi_bytes_for(int epi, bool swap = false) {
+  return epi == EPI_SWIGLU_BWD && !swap ? 8 * 2 * 4096 : (epi_staged(epi, swap) ? 8 * 32 * 32 * 4 : 0);
+}
 __host__ __device__ constexpr int stages_for(bool pair, int epi = EPI_F32, bool swap = false) {
-  return pair ? (epi_staged(epi, swap) ? 6 : 7) : 4;
+  return epi == EPI_SWIGLU_BWD && !swap ? (pair ? 5 : 3)
+                                        : (pair ? (epi_staged(epi, swap) ? 6 : 7) : 4);
 }
 __host__ __device__ constexpr int b_stage_bytes(bool pair) { return pair ? kBTileBytes / 2 : kBTileBytes; }
 __host__ __device__ constexpr int stage_bytes(bool pair) { return kATileBytes + b_stage_bytes(pair); }
@@ -93,20 +100,31 @@ struct SmemTail {
   uint64_t gfull[kMaxStages];        // a pair's odd CTA: its own cp.async arrivals
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t gu_full[2 * kEpiWarps];   // SwiGLU backward: a G|U slot's TMA load landed
   uint32_t tmem_base;
   int abort_flag;
   int mt_off[kMaxSeg + 1];
 };
-// per epilogue warp: 32 rows x 32 words, XOR-swizzled; after the tail (rounded up
-// to 128 bytes so that the 16-byte accesses stay aligned), when staged
+// per epilogue warp: 32 rows x 32 words, XOR-swizzled (the SwiGLU backward: two
+// such 4 KB slots); after the tail (rounded up to 128 bytes so that the 16-byte
+// accesses stay aligned), when staged
 constexpr int kTailBytes = (static_cast<int>(sizeof(SmemTail)) + 127) & ~127;
 constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
+// Offset of the epilogue buffers from the tail: the SwiGLU backward's slots are
+// TMA boxes with the 64-byte swizzle and start on 1024-byte boundaries.
+__host__ __device__ constexpr int epi_off(int epi, bool swap = false) {
+  return epi == EPI_SWIGLU_BWD && !swap ? (kTailBytes + 1023) & ~1023 : kTailBytes;
+}
+static_assert(epi_bytes_for(EPI_F32) == kEpiBytes && epi_bytes_for(EPI_SWIGLU_BWD) == 2 * kEpiBytes,
+              "epilogue buffers: 4 KB a warp, 8 KB a warp for the SwiGLU backward");
 __host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false) {
-  return 1024 /*alignment slack*/ + stages_for(pair, epi, swap) * stage_bytes(pair) + kTailBytes +
-         (epi_staged(epi, swap) ? kEpiBytes : 0);
+  return 1024 /*alignment slack*/ + stages_for(pair, epi, swap) * stage_bytes(pair) +
+         epi_off(epi, swap) + epi_bytes_for(epi, swap);
 }
 static_assert(smem_bytes(false, EPI_F32) <= 232448 && smem_bytes(true, EPI_F32) <= 232448 &&
-              smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448,
+              smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448 &&
+              smem_bytes(false, EPI_SWIGLU_BWD) <= 232448 &&
+              smem_bytes(true, EPI_SWIGLU_BWD) <= 232448,
               "shared memory");
 
 struct Params {
@@ -293,8 +311,11 @@ __device__ __forceinline__ void red_rows32(uint32_t* buf, const uint32_t* v, flo
   __syncwarp();
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+// silu and the logistic function with CUDA's fast exponential and division
+// intrinsics (a few ulp; the IEEE division cost the SwiGLU backward 12 % of its
+// time).  For g < -87 the denominator overflows and both give 0.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
 // This thread's G and U segments of a SwiGLU-backward tile (BN / 2 columns of
 // one row, fewer at the matrix's edge) fetched into L2.
@@ -306,15 +327,14 @@ __device__ __forceinline__ void gu_prefetch_l2(const __nv_bfloat16* g, int I, in
   }
 }
 
-// G and U of 16 columns of one row for the SwiGLU backward: rows of the
-// forward's save are [G | U], 2*I bf16; r[0..1] get G, r[2..3] U.
-__device__ __forceinline__ void load_gu16(const __nv_bfloat16* g, int I, uint4 (&r)[4]) {
-  r[0] = __ldg(reinterpret_cast<const uint4*>(g));
-  r[1] = __ldg(reinterpret_cast<const uint4*>(g + 8));
-  r[2] = __ldg(reinterpret_cast<const uint4*>(g + I));
-  r[3] = __ldg(reinterpret_cast<const uint4*>(g + I + 8));
+// The SwiGLU backward's G and U for one warp's chunk of 32 rows x 32 columns sit
+// in a 4 KB slot: G in [0, 2 KB), U in [2 KB, 4 KB), each a TMA box of 64-byte
+// rows with the 64-byte swizzle: row r's 16-byte piece j (columns 8j..8j+7) at
+// r * 64 + ((j ^ ((r >> 1) & 3)) << 4), so that lane r reading its own row's
+// piece j touches every bank once per eight lanes.
+__device__ __forceinline__ uint32_t gu_slot_off(int r, int j) {
+  return static_cast<uint32_t>(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
 }
-
 // Shared-memory descriptor of one K=16 slice of an operand tile.
 //  K-major: rows along M/N at 128 B, 8-row groups every 1024 B; slice kk starts
 //           32 bytes further inside the swizzle atom.
@@ -333,7 +353,9 @@ namespace {
 template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP>
 __global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const Params p) {
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC,
+                       const __grid_constant__ CUtensorMap tmD, const Params p) {
   pdl_wait();
   pdl_trigger();
   static_assert(!(PAIR && !WGRAD && (op_mn(AM) || op_gathered(BMODE))),
@@ -346,6 +368,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 "swapped units: paired forward GEMMs with K-major rows and weights");
   // Swapped: the stage's first 16 KB hold this CTA's 128 weight rows (the MMA's
   // A), the next 16 KB its half of the unit's rows (the MMA's B).
+  // the SwiGLU forward, with or without the G|U save
+  constexpr bool kSwiGLU = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_SAVE;
   constexpr int kStages = stages_for(PAIR, EPI, SWAP);
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
@@ -382,6 +406,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(&tail->tfull[a], 1);
       mbar_init(&tail->tempty[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&tail->gu_full[i], 1);
     tail->abort_flag = 0;
     mbar_fence_init();
   }
@@ -412,6 +437,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (EPI == EPI_SWIGLU_BWD && !SWAP) {
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmD);
+      }
     }
   } else if (warp == 1) {
     if (PAIR) tmem_alloc_pair(&tail->tmem_base, kTmemCols);
@@ -437,7 +466,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     bool ok = true;
     for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
       const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
-      const int n0 = ti.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+      const int n0 = ti.nt * (kSwiGLU ? BN / 2 : BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
@@ -452,7 +481,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             // the unit's rows (only the first nmma/2 are read by the MMA)
             if (leader) mbar_arrive_expect_tx(bar, kTmaBytes);
             const uint32_t lbar = full_lead + stage * 8;
-            if (EPI == EPI_SWIGLU) {
+            if (kSwiGLU) {
               // TMEM lane quarter q holds 16 gate rows and the 16 up rows of the
               // same intermediate units, so that one warp's epilogue sees both:
               // one 5-D box (K, 16 rows, gate/up, 4 groups of 16 units, expert)
@@ -475,7 +504,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 tma_load_2d_pair(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, lbar);
             if (BMODE == OP_TMA_K) {
               const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0 +
-                               rank * (EPI == EPI_SWIGLU ? p.half_n : BN / 2);
+                               rank * (kSwiGLU ? p.half_n : BN / 2);
               tma_load_2d_pair(sb, &tmB, kb * BK, brow, lbar);
             } else if (BMODE == OP_TMA_MN) {
               for (int a = 0; a < 2; ++a)
@@ -490,7 +519,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             if (BMODE == OP_TMA_K) {
               const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0;
-              if (EPI == EPI_SWIGLU) {
+              if (kSwiGLU) {
                 tma_load_2d(sb, &tmB, kb * BK, brow, bar);
                 tma_load_2d(sb + kBTileBytes / 2, &tmB, kb * BK, brow + p.half_n, bar);
               } else {
@@ -593,6 +622,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int half = (warp - kEpiWarp0) / 4;  // which half of the tile's columns
     const int row = quarter * 32 + lane;
+    // SwiGLU backward: this warp's two G | U slots, the slot of the next chunk to
+    // process, whether that chunk (the next tile's first) is already in flight,
+    // the parity each slot's barrier completes with next, the slots with a load
+    // in flight
+    constexpr bool kGuStaged = EPI == EPI_SWIGLU_BWD && !SWAP;
+    uint8_t* gbuf = reinterpret_cast<uint8_t*>(tail) + epi_off(EPI, SWAP) + (warp - kEpiWarp0) * 8192;
+    uint64_t* gbar = &tail->gu_full[2 * (warp - kEpiWarp0)];
+    int gslot = 0;
+    bool gnext = false;
+    uint32_t gpar = 0, gpend = 0;
     int it = 0;
     bool ok = true;
     for (int tau = unit0; tau < total; tau = unit_at<WGRAD>(++it, unit0, n_units)) {
@@ -622,7 +661,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       float g_pre = 0.f;
       if (EPI == EPI_SWIGLU_BWD && !SWAP && valid) g_pre = p.row_gate[grow];
-      if (EPI == EPI_SWIGLU && !SWAP) g_pre = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
+      if (kSwiGLU && !SWAP) g_pre = (valid && p.row_gate) ? p.row_gate[grow] : 1.0f;
       int64_t dst_pre = 0;
       if (EPI == EPI_F32_RED && !SWAP && valid) dst_pre = p.out_tok[p.out_src[grow]];
       constexpr int kSwapChunks = 4;  // a swapped unit's columns: at most 4 chunks a warp
@@ -641,6 +680,29 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       }
+      // valid 32-column chunks of this warp's half of a SwiGLU-backward tile
+      auto gu_chunks = [&](const TileInfo& t) {
+        return max(0, min(4, (p.N_out - t.nt * BN - half * (BN / 2)) / 32));
+      };
+      // this warp's 32 x 32 chunk of G and of U (column c of its half of tile t)
+      // into slot sl by two TMA boxes, issued by lane 0 once the slot's last TMA
+      // store has read it (rows past the matrix arrive as zeros)
+      auto gu_load = [&](int sl, const TileInfo& t, int c) {
+        if (lane == 0) {
+          bulk_wait_read<0>();
+          mbar_arrive_expect_tx(gbar + sl, 4096);
+          const int col = t.nt * BN + half * (BN / 2) + c;
+          const int r0 = t.m0 + quarter * 32;
+          tma_load_2d(gbuf + sl * 4096, &tmC, col, r0, gbar + sl);
+          tma_load_2d(gbuf + sl * 4096 + 2048, &tmC, p.half_n + col, r0, gbar + sl);
+        }
+        gpend |= 1u << sl;
+      };
+      if (kGuStaged && !gnext && gu_chunks(ti) > 0) {
+        // no chunk of this tile in flight yet: its first one now, while the MMAs run
+        gu_load(gslot, ti, 0);
+      }
+      gnext = false;
       if (!mbar_wait(&tail->tfull[a], aph, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t t_row = tbase + a * BN + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -729,6 +791,40 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             __syncwarp();
           }
         }
+      } else if (EPI == EPI_SWIGLU_SAVE) {
+        // h and the saved G | U leave through this warp's staging buffer, eight
+        // rows of 64 bytes per store instruction (a row per lane would touch 32
+        // rows per instruction, three times per chunk, and throttle the LSU)
+        const float g = g_pre;
+        const int col0 = ti.nt * (BN / 2);
+        const int64_t ld_gu = 2 * static_cast<int64_t>(p.N_out);
+        __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0;
+        __nv_bfloat16* gout = p.gu_out + wrow0 * ld_gu + col0;
+#pragma unroll 1
+        for (int c = half * (BN / 4); c < (half + 1) * (BN / 4); c += 32) {
+          tmem_ld32(t_row + c, v0);
+          tmem_ld32(t_row + BN / 2 + c, v1);
+          tmem_ld_wait();
+          if (col0 + c < p.N_out) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = g * silu_f(__uint_as_float(v0[2 * i])) * __uint_as_float(v1[2 * i]);
+              const float h1 =
+                  g * silu_f(__uint_as_float(v0[2 * i + 1])) * __uint_as_float(v1[2 * i + 1]);
+              pk[i] = pack_bf16x2(h0, h1);
+            }
+            store_rows<16>(ebuf, pk, reinterpret_cast<char*>(hout + c), p.ldo * 2, wrows);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+            store_rows<16>(ebuf, pk, reinterpret_cast<char*>(gout + c), ld_gu * 2, wrows);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            store_rows<16>(ebuf, pk, reinterpret_cast<char*>(gout + p.N_out + c), ld_gu * 2, wrows);
+          }
+        }
       } else if (EPI == EPI_SWIGLU) {
         const float g = g_pre;
         const int col0 = ti.nt * (BN / 2);
@@ -776,51 +872,98 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       } else if (EPI == EPI_SWIGLU_BWD) {
         // accumulator = dh' (gradient of the modulated intermediate) for the
-        // tile's 256 columns of I; G and U come from the forward (fetched into
-        // L2 a tile ahead)
+        // tile's 256 columns of I.  G and U of the forward arrive chunk by chunk
+        // in this warp's two slots by TMA, one chunk ahead (the next tile's first
+        // chunk during this tile's last); dG and dU overwrite them in place and
+        // leave by TMA stores (a warp with fewer than 32 rows of the segment
+        // stores its rows itself, so that no store reaches past the segment).
         const float g = g_pre;
-        const int col0 = ti.nt * BN;
+        const int col0 = ti.nt * BN + half * (BN / 2);
         const int I = p.half_n;
+        const int nch = gu_chunks(ti);
         float dg = 0.f;
 #pragma unroll 1
-        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-          if (col0 + c >= p.N_out) break;
-          tmem_ld32(t_row + c, v0);
-          uint32_t pg[16], pu[16];
-          const __nv_bfloat16* gsrc = gu_row + (c - half * (BN / 2));
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            uint4 r[4];
-            load_gu16(gsrc + 16 * i, I, r);
-            pg[8 * i] = r[0].x; pg[8 * i + 1] = r[0].y; pg[8 * i + 2] = r[0].z; pg[8 * i + 3] = r[0].w;
-            pg[8 * i + 4] = r[1].x; pg[8 * i + 5] = r[1].y; pg[8 * i + 6] = r[1].z; pg[8 * i + 7] = r[1].w;
-            pu[8 * i] = r[2].x; pu[8 * i + 1] = r[2].y; pu[8 * i + 2] = r[2].z; pu[8 * i + 3] = r[2].w;
-            pu[8 * i + 4] = r[3].x; pu[8 * i + 5] = r[3].y; pu[8 * i + 6] = r[3].z; pu[8 * i + 7] = r[3].w;
-          }
-          tmem_ld_wait();
-          uint32_t og[16], ou[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float dG[2], dU[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float G = __uint_as_float(h ? (pg[i] & 0xffff0000u) : (pg[i] << 16));
-              const float U = __uint_as_float(h ? (pu[i] & 0xffff0000u) : (pu[i] << 16));
-              const float dhp = __uint_as_float(v0[2 * i + h]);
-              const float sg = sigmoid_f(G);
-              const float s = G * sg;
-              dg = fmaf(dhp, s * U, dg);
-              const float dh = g * dhp;
-              dG[h] = dh * U * sg * (1.0f + G * (1.0f - sg));
-              dU[h] = dh * s;
+        for (int ch = 0; ch < nch; ++ch) {
+          const int c = ch * 32;
+          tmem_ld32(t_row + half * (BN / 2) + c, v0);
+          // the chunk after this one: this tile's next, or the next tile's first
+          if (ch + 1 < nch) {
+            gu_load(gslot ^ 1, ti, c + 32);
+          } else {
+            const int tau_n = unit_at<WGRAD>(it + 1, unit0, n_units);
+            if (tau_n < total) {
+              const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP>(tau_n, p, tail->mt_off, rank);
+              if (gu_chunks(tn) > 0) {
+                gu_load(gslot ^ 1, tn, 0);
+                gnext = true;
+              }
             }
-            og[i] = pack_bf16x2(dG[0], dG[1]);
-            ou[i] = pack_bf16x2(dU[0], dU[1]);
           }
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0 + c;
-          store_rows<16>(ebuf, og, reinterpret_cast<char*>(o), p.ldo * 2, wrows);
-          store_rows<16>(ebuf, ou, reinterpret_cast<char*>(o + I), p.ldo * 2, wrows);
+          if (!mbar_wait(gbar + gslot, (gpar >> gslot) & 1u, abort_flag)) {
+            tmem_ld_wait();
+            ok = false;
+            break;
+          }
+          gpar ^= 1u << gslot;
+          gpend &= ~(1u << gslot);
+          uint8_t* slot = gbuf + gslot * 4096;
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4* gp = reinterpret_cast<uint4*>(slot + gu_slot_off(lane, j));
+            uint4* up = reinterpret_cast<uint4*>(slot + 2048 + gu_slot_off(lane, j));
+            const uint4 gq = *gp, uq = *up;
+            const uint32_t pg[4] = {gq.x, gq.y, gq.z, gq.w};
+            const uint32_t pu[4] = {uq.x, uq.y, uq.z, uq.w};
+            uint32_t og[4], ou[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float dG[2], dU[2];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const float G = __uint_as_float(h ? (pg[i] & 0xffff0000u) : (pg[i] << 16));
+                const float U = __uint_as_float(h ? (pu[i] & 0xffff0000u) : (pu[i] << 16));
+                const float dhp = __uint_as_float(v0[8 * j + 2 * i + h]);
+                const float sg = sigmoid_f(G);
+                const float sv = G * sg;
+                dg = fmaf(dhp, sv * U, dg);
+                const float dh = g * dhp;
+                dG[h] = dh * U * sg * (1.0f + G * (1.0f - sg));
+                dU[h] = dh * sv;
+              }
+              og[i] = pack_bf16x2(dG[0], dG[1]);
+              ou[i] = pack_bf16x2(dU[0], dU[1]);
+            }
+            *gp = make_uint4(og[0], og[1], og[2], og[3]);
+            *up = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+          }
+          // this lane's writes ordered before the TMA engine's accesses to the
+          // slot (the store below, the load two chunks on)
+          fence_proxy_async_smem();
+          if (wrows == 32) {
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, slot, col0 + c, static_cast<int>(wrow0));
+              tma_store_2d(&tmD, slot + 2048, I + col0 + c, static_cast<int>(wrow0));
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0 + c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = (lane >> 2) + 8 * i, j = lane & 3;
+              if (r < wrows) {
+                st_v4(o + r * p.ldo + j * 8, *reinterpret_cast<const uint4*>(slot + gu_slot_off(r, j)));
+                st_v4(o + r * p.ldo + I + j * 8,
+                      *reinterpret_cast<const uint4*>(slot + 2048 + gu_slot_off(r, j)));
+              }
+            }
+          }
+          __syncwarp();        // the slot is refilled two chunks on
+          gslot ^= 1;
         }
+        if (!ok) break;
         // one partial per (row, N tile, column half)
         if (valid) p.dg_part[grow * (2 * p.n_tiles_n) + 2 * ti.nt + half] = dg;
       } else if (EPI == EPI_F32_RED) {
@@ -859,6 +1002,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (PAIR && !leader) mbar_arrive_cluster(tempty_lead + a * 8);
         else mbar_arrive(&tail->tempty[a]);
       }
+    }
+    if (kGuStaged) {
+      // the TMA stores complete, and a load still in flight (after a timeout)
+      // lands, before the CTA may exit
+      if (lane == 0) bulk_wait<0>();
+      volatile int no_abort = 0;
+      for (int sl = 0; sl < 2; ++sl)
+        if (gpend & (1u << sl)) mbar_wait(gbar + sl, (gpar >> sl) & 1u, &no_abort);
+      __syncwarp();
     }
     if (!ok) {
       if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
@@ -979,9 +1131,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle
+// (or the given one).
 int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
-             uint32_t box_rows) {
+             uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return OCCULT_ERR_CUDA;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -989,7 +1142,7 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint3
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? OCCULT_OK : OCCULT_ERR_CUDA;
 }
@@ -1024,7 +1177,8 @@ int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t
 }
 
 template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP = false>
-int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb, const Params& p) {
+int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb,
+              const CUtensorMap& mc, const CUtensorMap& md, const Params& p) {
   auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR, SWAP>;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[2];
@@ -1053,7 +1207,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   });
   if (attr_err != cudaSuccess || (PAIR && n_pairs < 1)) return OCCULT_ERR_CUDA;
   cfg.gridDim = dim3(PAIR ? 2 * n_pairs : ctx.num_sms);
-  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, p));
+  return cuda_status(cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, md, p));
 }
 
 }  // namespace
@@ -1082,7 +1236,8 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // N) so that a segment's last unit computes its rows rounded up to 16, not to
   // 256 (decode-sized segments stay on single CTAs: a swapped pair measured
   // slower there, 164 vs 135 us for the DeepSeek decode up-projection).
-  const int epi_eff = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED : g.epi;
+  const int epi_eff = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED
+                    : (g.epi == EPI_SWIGLU && g.gu_out ? EPI_SWIGLU_SAVE : g.epi);
   const bool swap = pair && !g.wgrad && g.seg_off && g.b_mode == OP_TMA_K &&
                     ((epi_eff == EPI_SWIGLU && g.a_mode == OP_GATHER_K && !g.gu_out) ||
                      ((epi_eff == EPI_F32 || epi_eff == EPI_F32_RED) && g.a_mode == OP_TMA_K));
@@ -1098,6 +1253,15 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     rc = operand_map(&mb, g.b_mode, g.B, g.b_rows, g.b_cols,
                      (pair || g.epi == EPI_SWIGLU) ? BN / 2 : BN);
   if (rc) return rc;
+  // the SwiGLU backward's G|U (in) and dG|dU (out): [rows, 2 N_out] bf16, boxes of
+  // 32 columns x 32 rows with the 64-byte swizzle; unused (zero) otherwise
+  CUtensorMap mc{}, md{};
+  if (epi_eff == EPI_SWIGLU_BWD) {
+    if (reinterpret_cast<uintptr_t>(g.gu_in) % 16 != 0) return OCCULT_ERR_UNSUPPORTED;
+    rc = make_map(&mc, g.gu_in, g.max_rows, 2ll * g.N_out, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!rc) rc = make_map(&md, g.out, g.max_rows, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc) return rc;
+  }
   Params p{};
   p.seg_off = g.seg_off;
   p.seg_group = g.seg_group;
@@ -1129,18 +1293,19 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // the instantiations the layer uses
 #define OCCULT_ROWS_GEMM(AM_, BM_, EP_)                                                 \
   if (am == AM_ && bm == BM_ && ep == EP_)                                             \
-    return pair ? launch_tc<AM_, BM_, EP_, false, true>(ctx, ma, mb, p)                \
-                : launch_tc<AM_, BM_, EP_, false, false>(ctx, ma, mb, p);
+    return pair ? launch_tc<AM_, BM_, EP_, false, true>(ctx, ma, mb, mc, md, p)                \
+                : launch_tc<AM_, BM_, EP_, false, false>(ctx, ma, mb, mc, md, p);
   if (swap) {
     if (am == OP_GATHER_K && ep == EPI_SWIGLU)
-      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false, true, true>(ctx, ma, mb, p);
+      return launch_tc<OP_GATHER_K, OP_TMA_K, EPI_SWIGLU, false, true, true>(ctx, ma, mb, mc, md, p);
     if (am == OP_TMA_K && ep == EPI_F32)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false, true, true>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32, false, true, true>(ctx, ma, mb, mc, md, p);
     if (am == OP_TMA_K && ep == EPI_F32_RED)
-      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32_RED, false, true, true>(ctx, ma, mb, p);
+      return launch_tc<OP_TMA_K, OP_TMA_K, EPI_F32_RED, false, true, true>(ctx, ma, mb, mc, md, p);
   }
   if (!g.wgrad) {
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_K, EPI_SWIGLU)     // up-projection
+    OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_K, EPI_SWIGLU_SAVE)  // the same, G|U saved
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_SWIGLU)        // shared experts' up-projection
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32)           // down-projections
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32_RED)       // down-projection + merge
@@ -1150,11 +1315,11 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
 #undef OCCULT_ROWS_GEMM
   } else if (ep == EPI_F32) {
     if (am == OP_GATHER_MN && bm == OP_TMA_MN)
-      return pair ? launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, true>(ctx, ma, mb, p)
-                  : launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, p);
+      return pair ? launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, true>(ctx, ma, mb, mc, md, p)
+                  : launch_tc<OP_GATHER_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, mc, md, p);
     if (am == OP_TMA_MN && bm == OP_GATHER_MN)
-      return pair ? launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, true>(ctx, ma, mb, p)
-                  : launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, p);
+      return pair ? launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, true>(ctx, ma, mb, mc, md, p)
+                  : launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, mc, md, p);
   }
   return OCCULT_ERR_UNSUPPORTED;
 }

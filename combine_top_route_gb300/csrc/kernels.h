@@ -66,7 +66,9 @@ enum : int { OP_TMA_K = 0, OP_GATHER_K = 1, OP_TMA_MN = 2, OP_GATHER_MN = 3 };
 // SwiGLU backward -> dG|dU in the layer dtype plus partial gate gradients.
 // EPI_F32_RED: fp32 rows added (red.global.add) into out[out_tok[out_src[r]]]
 // instead of stored at row r (the merge of Algorithm 8 as fp32 atomic adds).
-enum : int { EPI_SWIGLU = 0, EPI_F32 = 1, EPI_SWIGLU_BWD = 2, EPI_F32_RED = 3 };
+// EPI_SWIGLU_SAVE: EPI_SWIGLU with G|U saved (chosen by the launcher when gu_out
+// is given; its stores go through shared memory).
+enum : int { EPI_SWIGLU = 0, EPI_F32 = 1, EPI_SWIGLU_BWD = 2, EPI_F32_RED = 3, EPI_SWIGLU_SAVE = 4 };
 
 // Grouped GEMM over segments.
 //  rows mode (wgrad = false): output rows [seg_off[s], seg_off[s+1]) use weight

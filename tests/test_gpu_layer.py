@@ -8,8 +8,8 @@ import pytest
 import torch
 
 import synth
-from layer_cases import (alg1_placement, assert_close_layer, h_bound, make_case, oracle_brims,
-                         reference_output, scatter_add_rows, sfd_bound)
+from layer_cases import (F32_EPS, abs_contract, alg1_placement, assert_close_layer, h_bound,
+                         make_case, oracle_brims, reference_output, scatter_add_rows, sfd_bound)
 from oracle import brim as obrim
 from oracle import coact as ocoact
 from oracle import expert as oexpert
@@ -318,19 +318,33 @@ def test_expert_ffn(occ, name):
                           case.weights["w2"], h, y)
     torch.cuda.synchronize()
     check_h_all_rows(h.float().cpu().numpy(), b, x, w1, cfg)
+    # y_epd = W_d h' from the oracle's fp64 h'; the GPU reads its own h' (within
+    # h_bound of the oracle's) and accumulates I products in fp32:
+    #   |dy| <= |W_d| h_b + 2 I 2^-24 |W_d| (|h'| + h_b)
+    # (one EPD row is heavy-tailed like h', so the 2e-2 rms bar of the layer
+    # output, a sum of k rows, does not apply to it)
     I = cfg.inter
-    ref = np.zeros((b.n_epd, cfg.d))
-    for s in range(len(b.exp_off) - 1):
-        r0, r1 = int(b.exp_off[s]), int(b.exp_off[s + 1])
-        if r1 > r0:
-            e = int(b.epd_exp[r0])
-            a = x[b.epd_tok[r0:r1]].astype(np.float64)
-            hh = (b.epd_gate[r0:r1, None].astype(np.float64) * oexpert.silu(a @ w1[e, :I].T)
-                  * (a @ w1[e, I:].T))
-            ref[r0:r1] = hh @ w2[e].T
     got = y.cpu().numpy()
     assert np.isfinite(got).all(), "an EPD row was left unwritten"
-    assert_close_layer(got, ref, cfg.dtype, "y_epd")
+    worst = 0.0
+    for s in range(len(b.exp_off) - 1):
+        r0, r1 = int(b.exp_off[s]), int(b.exp_off[s + 1])
+        if r1 == r0:
+            continue
+        e = int(b.epd_exp[r0])
+        a = x[b.epd_tok[r0:r1]].astype(np.float64)
+        g = b.epd_gate[r0:r1].astype(np.float64)
+        hh = g[:, None] * oexpert.silu(a @ w1[e, :I].T) * (a @ w1[e, I:].T)
+        h_b = h_bound(a, w1[e, :I], w1[e, I:], g, hh, cfg.dtype)
+        ref = hh @ w2[e].T.astype(np.float64)
+        wd_abs = np.abs(w2[e]).T
+        bound = (abs_contract(h_b, wd_abs)
+                 + 2 * I * F32_EPS * abs_contract(np.abs(hh) + h_b, wd_abs) + 1e-30)
+        err = np.abs(got[r0:r1] - ref)
+        assert (err <= bound).all(), (
+            f"y_epd rows of slot {s} (expert {e}): worst excess {float(np.max(err - bound)):.3e}")
+        worst = max(worst, float(np.max(err / bound)))
+    print(f"y_epd: worst diff/bound {worst:.3f}")
     assert occ.device_error() == 0
 
 
