@@ -183,8 +183,7 @@ def test_sharded_layer(occ, name):
     moe, y, _ = run_layer(occ, case, src_off=split)
     assert moe.launches_per_forward == 13 + (2 + int(cfg.shared_gate) if cfg.n_shared else 0)
     ids, gates, margin = case.oracle_route()
-    toks = np.arange(min(cfg.T, 96))
-    toks = toks[margin[toks] > 1e-5]
+    toks = np.nonzero(margin > 1e-5)[0]
     assert_close_layer(y.cpu().numpy()[toks], reference_output(case, toks, ids, gates), cfg.dtype)
     _, y_single, _ = run_layer(occ, case)
     assert torch.equal(y, y_single)
