@@ -176,6 +176,27 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];"
       :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
+// TMA gather of four rows y0..y3 of the columns x .. x + box-1 (the map's box is
+// one row high) into four consecutive box rows at smem_dst; rows outside the
+// matrix arrive as zeros.  complete_tx on an mbarrier of this CTA, or (pair form)
+// of either CTA of the pair (`bar_cluster` is a shared::cluster address).
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int x, int y0,
+                                            int y1, int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+         "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const CUtensorMap* map, int x,
+                                                 int y0, int y1, int y2, int y3,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"(smem_u32(smem_dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+         "r"(bar_cluster) : "memory");
+}
 // 2-D tiled TMA store of a box from this CTA's shared memory; tracked in bulk
 // groups of the issuing thread (bulk_commit / bulk_wait_read / bulk_wait).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x,

@@ -33,10 +33,12 @@
 //                forwards the completion of its gathered stages to the even one.
 //   warps 2..9   epilogue: tcgen05.ld of the accumulator, two warps per TMEM
 //                lane quarter (half of the columns each).
-//   warps 10..13 cp.async producers for a gathered operand (rows picked by the
-//                condensed BRIM1), written straight into the 128-byte swizzle the
-//                tensor cores read; zero-filled past a segment's end.  (TMA
-//                tile::gather4 measured 2.3x slower on the up-projection.)
+//   warps 10..13 producers for a gathered operand (rows picked by the condensed
+//                BRIM1): K-major rows (forward, dgrad) by cp.async, written
+//                straight into the 128-byte swizzle the tensor cores read and
+//                zero-filled past a segment's end (TMA tile::gather4 measured 2.3x
+//                slower there); MN-major rows (weight gradients) by TMA
+//                tile::gather4, four 128-byte rows an instruction.
 // Operands are K-major (rows along K) or MN-major (rows along K of a matrix
 // stored K x MN); both use the 128-byte swizzle.  Every wait is bounded (2 s).
 #include <cudaTypedefs.h>
@@ -112,19 +114,23 @@ constexpr int kTailBytes = (static_cast<int>(sizeof(SmemTail)) + 127) & ~127;
 constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
 // Offset of the epilogue buffers from the tail: the SwiGLU backward's slots are
 // TMA boxes with the 64-byte swizzle and start on 1024-byte boundaries.
-__host__ __device__ constexpr int epi_off(int epi, bool swap = false) {
-  return epi == EPI_SWIGLU_BWD && !swap ? (kTailBytes + 1023) & ~1023 : kTailBytes;
+__host__ __device__ constexpr int epi_off(int epi, bool swap = false, bool wgrad = false) {
+  return (epi == EPI_SWIGLU_BWD && !swap) || wgrad ? (kTailBytes + 1023) & ~1023 : kTailBytes;
 }
 static_assert(epi_bytes_for(EPI_F32) == kEpiBytes && epi_bytes_for(EPI_SWIGLU_BWD) == 2 * kEpiBytes,
               "epilogue buffers: 4 KB a warp, 8 KB a warp for the SwiGLU backward");
-__host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false) {
+// (the weight gradients' staging buffers are TMA store sources: 1024-byte aligned)
+__host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false,
+                                             bool wgrad = false) {
   return 1024 /*alignment slack*/ + stages_for(pair, epi, swap) * stage_bytes(pair) +
-         epi_off(epi, swap) + epi_bytes_for(epi, swap);
+         epi_off(epi, swap, wgrad) + epi_bytes_for(epi, swap);
 }
 static_assert(smem_bytes(false, EPI_F32) <= 232448 && smem_bytes(true, EPI_F32) <= 232448 &&
               smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448 &&
               smem_bytes(false, EPI_SWIGLU_BWD) <= 232448 &&
-              smem_bytes(true, EPI_SWIGLU_BWD) <= 232448,
+              smem_bytes(true, EPI_SWIGLU_BWD) <= 232448 &&
+              smem_bytes(false, EPI_F32, false, true) <= 232448 &&
+              smem_bytes(true, EPI_F32, false, true) <= 232448,
               "shared memory");
 
 struct Params {
@@ -142,6 +148,8 @@ struct Params {
   const int32_t* gather;       // source row of every gathered operand row
   const __nv_bfloat16* g_ptr;  // gathered operand's matrix
   int64_t g_ld;                // its row length (elements)
+  int g_rows;                  // its rows (an MN-major gather names row g_rows for a
+                               // row past the segment: outside the map, zero-filled)
   int64_t b_group_rows;        // B rows per weight group (forward / dgrad)
   int half_n;                  // SwiGLU: up rows' offset in a B group; SwiGLU bwd: I
   // epilogue
@@ -374,10 +382,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr int kStageBytes = stage_bytes(PAIR);
   constexpr int kBBytes = b_stage_bytes(PAIR);
   constexpr bool kGather = op_gathered(AM) || op_gathered(BMODE);
+  // MN-major gathers (weight gradients) are TMA tile::gather4 loads counted in the
+  // stage's transaction bytes; K-major gathers are cp.async copies counted as
+  // arrivals (and, in a pair, forwarded by the odd CTA)
+  constexpr bool kGatherMN = AM == OP_GATHER_MN || BMODE == OP_GATHER_MN;
+  constexpr bool kGatherCp = kGather && !kGatherMN;
   constexpr uint32_t kIdesc = idesc_for(AM, BMODE, PAIR);
   // TMA bytes of one stage of one CTA; a pair's even CTA expects both CTAs' bytes
-  constexpr uint32_t kTmaCta =
-      (op_gathered(AM) ? 0u : uint32_t(kATileBytes)) + (op_gathered(BMODE) ? 0u : uint32_t(kBBytes));
+  constexpr uint32_t kTmaCta = (AM == OP_GATHER_K ? 0u : uint32_t(kATileBytes)) +
+                               (BMODE == OP_GATHER_K ? 0u : uint32_t(kBBytes));
   constexpr uint32_t kTmaBytes = PAIR ? 2 * kTmaCta : kTmaCta;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -398,7 +411,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < kStages; ++s) {
       // the TMA arrival, plus one per cp.async producer thread (and, in a pair,
       // one forwarded from the odd CTA for all of its producer threads)
-      mbar_init(&tail->full[s], kGather ? 1 + 128 + (PAIR ? 1 : 0) : 1);
+      mbar_init(&tail->full[s], kGatherCp ? 1 + 128 + (PAIR ? 1 : 0) : 1);
       mbar_init(&tail->empty[s], 1);
       mbar_init(&tail->gfull[s], 128);
     }
@@ -413,7 +426,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (WGRAD) {
     // the segments in order of decreasing rows (ties by index) into mt_off, the
     // rows staged in the epilogue buffers, which nothing else uses yet
-    int* len = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes);
+    int* len = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(tail) + epi_off(EPI, SWAP, WGRAD));
     for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) len[s] = seg_at(p, s + 1) - seg_at(p, s);
     __syncthreads();
     for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
@@ -567,7 +580,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                      : mbar_wait(&tail->full[stage], phase, abort_flag))) { ok = false; break; }
           // cp.async data arrived through the generic proxy: make it visible to
           // the tensor cores' (async proxy) operand reads
-          if (kGather) fence_proxy_async_smem();
+          if (kGatherCp) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kATileBytes;
@@ -594,7 +607,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
       }
-    } else if (PAIR && kGather && lane == 0) {
+    } else if (PAIR && kGatherCp && lane == 0) {
       // ---- odd CTA: forwards its gathered stages to the even CTA -------------
       // Its cp.async copies complete on its own barrier; once a stage's have all
       // landed, they are made visible to the async proxy (the even CTA's MMAs
@@ -708,7 +721,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t t_row = tbase + a * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
       const int64_t wrow0 = ti.m0 + quarter * 32;
-      uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes) +
+      uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) +
+                                                   epi_off(EPI, SWAP, WGRAD)) +
                        (warp - kEpiWarp0) * 32 * 32;
       uint32_t v0[32], v1[32];
       if (SWAP) {
@@ -990,8 +1004,29 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int i = 0; i < 32; ++i) v0[i] = 0u;
             }
-            store_rows<32>(ebuf, v0, reinterpret_cast<char*>(obase + wrow0 * p.ldo + col0 + c),
-                           p.ldo * 4, wrows);
+            if (WGRAD && wrows == 32) {
+              // the warp's 32 x 32 fp32 block as one TMA box store: the staging
+              // buffer holds it in the 128-byte swizzle the box takes (once the
+              // previous box has been read out of it)
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                stage_v4(ebuf, j, make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]));
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmD, ebuf, col0 + c, ti.grp * p.M_total + static_cast<int>(wrow0));
+                bulk_commit();
+              }
+            } else {
+              if (WGRAD) {
+                if (lane == 0) bulk_wait_read<0>();  // the buffer's last box has left
+                __syncwarp();
+              }
+              store_rows<32>(ebuf, v0, reinterpret_cast<char*>(obase + wrow0 * p.ldo + col0 + c),
+                             p.ldo * 4, wrows);
+            }
           }
         }
       }
@@ -1003,6 +1038,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         else mbar_arrive(&tail->tempty[a]);
       }
     }
+    if (WGRAD && lane == 0) bulk_wait<0>();  // the weight gradients' boxes are out
     if (kGuStaged) {
       // the TMA stores complete, and a load still in flight (after a timeout)
       // lands, before the CTA may exit
@@ -1018,12 +1054,71 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
-  if (kGather && warp >= kGatherWarp0) {
-    // ---- cp.async producers for the gathered operand ---------------------------
+  if (kGatherMN && warp >= kGatherWarp0) {
+    // ---- TMA gathers of the MN-major operand (weight gradients) -----------------
+    // K row k of a stage is EPD row k0 + kb*64 + k, whose source row the gather
+    // array names (past the segment's end: row g_rows, outside the map, zeros).  Warp gw takes rows
+    // 16 gw .. 16 gw + 15; lane j < 16 holds row 16 gw + j's source, loaded four
+    // stages ahead.  Lane i < 4 * atoms issues one tile::gather4: rows
+    // 16 gw + 4 (i % 4) .. + 3 of MN atom i / 4 (64 columns, 128 bytes a row),
+    // landing in the 128-byte-swizzled MN-major layout the MMA reads, counted in
+    // the stage's transaction bytes on the (even CTA's) full barrier.
+    constexpr bool kOnA = AM == OP_GATHER_MN;
+    constexpr int kAtoms = (kOnA ? BM : (PAIR ? BN / 2 : BN)) / 64;
+    const CUtensorMap* gmap = kOnA ? &tmA : &tmB;
+    const int gw = warp - kGatherWarp0;
+    const int grp = lane & 3, atom = lane >> 2;
+    const int k_first = 16 * gw + 4 * grp;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+      auto load_idx = [&](int kb) -> int {
+        const int r = ti.k0 + kb * BK + 16 * gw + (lane & 15);
+        return r < ti.k1 ? p.gather[r] : p.g_rows;
+      };
+      int idx_cur = ti.kb > 0 ? load_idx(0) : p.g_rows;
+      int idx_1 = ti.kb > 1 ? load_idx(1) : p.g_rows;
+      int idx_2 = ti.kb > 2 ? load_idx(2) : p.g_rows;
+      int idx_3 = ti.kb > 3 ? load_idx(3) : p.g_rows;
+      const int mn0 = kOnA ? ti.m0 : ti.nt * BN + (PAIR ? rank * (BN / 2) : 0);
+      for (int kb = 0; kb < ti.kb; ++kb) {
+        const int idx_4 = kb + 4 < ti.kb ? load_idx(kb + 4) : p.g_rows;
+        if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        const int y0 = __shfl_sync(0xffffffffu, idx_cur, 4 * grp);
+        const int y1 = __shfl_sync(0xffffffffu, idx_cur, 4 * grp + 1);
+        const int y2 = __shfl_sync(0xffffffffu, idx_cur, 4 * grp + 2);
+        const int y3 = __shfl_sync(0xffffffffu, idx_cur, 4 * grp + 3);
+        if (lane < 4 * kAtoms) {
+          uint8_t* sa = smem + stage * kStageBytes;
+          uint8_t* dst = (kOnA ? sa : sa + kATileBytes) + atom * kMnAtomBytes +
+                         (k_first >> 3) * 1024 + (k_first & 7) * 128;
+          if (PAIR)
+            tma_gather4_pair(dst, gmap, mn0 + 64 * atom, y0, y1, y2, y3, full_lead + stage * 8);
+          else
+            tma_gather4(dst, gmap, mn0 + 64 * atom, y0, y1, y2, y3, &tail->full[stage]);
+        }
+        __syncwarp();
+        idx_cur = idx_1;
+        idx_1 = idx_2;
+        idx_2 = idx_3;
+        idx_3 = idx_4;
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  if (kGatherCp && warp >= kGatherWarp0) {
+    // ---- cp.async producers for the gathered K-major operand --------------------
     // Every thread arrives on a stage's full barrier asynchronously, when its
     // copies for that stage have landed (cp.async.mbarrier.arrive); the MMA thread
     // fences them for the async proxy after its wait.
-    const int gt = (warp - kGatherWarp0) * 32 + lane;   // 0..127
+    static_assert(!kGatherCp || AM == OP_GATHER_K, "cp.async gathers are K-major A operands");
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -1034,7 +1129,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       // at r*128 + ((c ^ (r % 8)) * 16)
       const __nv_bfloat16* src_k[8];
       uint32_t dst_k[8];
-      if (AM == OP_GATHER_K) {
+      {
         const int gw = warp - kGatherWarp0, chunk = lane & 7, rsub = lane >> 3;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -1044,54 +1139,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           src_k[i] = p.g_ptr + static_cast<int64_t>(p.gather[ti.m0 + rr]) * p.g_ld + chunk * 8;
         }
       }
-      // MN-major gathers: a warp touches 16 K rows of a stage; lane j < 16 holds
-      // the source row of the warp's j-th one, loaded four stages ahead (-1 past
-      // the segment's end) and handed to the copying lanes by shuffle
-      // chunks per K row: the A tile's 128 columns, or B's 256 (a pair: this CTA's 128)
-      constexpr int CPR = (AM == OP_GATHER_MN ? BM : (PAIR ? BN / 2 : BN)) / 8;
-      const int gw = warp - kGatherWarp0;
-      const int jrow = CPR == 32 ? gw + 4 * (lane & 15) : 2 * gw + (lane & 1) + 8 * ((lane & 15) >> 1);
-      auto load_idx = [&](int kb) -> int {
-        const int r = ti.k0 + kb * BK + jrow;
-        return r < ti.k1 ? p.gather[r] : -1;
-      };
-      int idx_cur = (WGRAD && ti.kb > 0) ? load_idx(0) : -1;
-      int idx_1 = (WGRAD && ti.kb > 1) ? load_idx(1) : -1;
-      int idx_2 = (WGRAD && ti.kb > 2) ? load_idx(2) : -1;
-      int idx_3 = (WGRAD && ti.kb > 3) ? load_idx(3) : -1;
       for (int kb = 0; kb < ti.kb; ++kb) {
-        const int idx_4 = (WGRAD && kb + 4 < ti.kb) ? load_idx(kb + 4) : -1;
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
-        if (AM == OP_GATHER_K) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cp_async_16((SWAP ? sa + kATileBytes : sa) + dst_k[i], src_k[i] + kb * BK);
-        } else {
-          // MN-major rows (weight gradients): K row k of the stage is EPD row
-          // k0 + kb*64 + k; chunk c covers MN elements 8c..8c+7 of the tile; rows
-          // past the segment's end and columns past the matrix are zero-filled
-          constexpr bool kOnA = (AM == OP_GATHER_MN);
-          uint8_t* base = kOnA ? sa : sa + kATileBytes;
-          const int mn0 = kOnA ? ti.m0 : ti.nt * BN + (PAIR ? rank * (BN / 2) : 0);
-          const int mn_total = kOnA ? p.M_total : p.N_out;
-#pragma unroll
-          for (int i = 0; i < CPR / 2; ++i) {
-            const int q = gt + 128 * i;
-            const int k = q / CPR, c = q % CPR;
-            const int j = CPR == 32 ? i : (lane >> 4) + 2 * i;
-            const int src_row = __shfl_sync(0xffffffffu, idx_cur, j);
-            const bool in = src_row >= 0 && mn0 + c * 8 < mn_total;
-            const __nv_bfloat16* src = p.g_ptr;
-            if (in) src = p.g_ptr + static_cast<int64_t>(src_row) * p.g_ld + mn0 + c * 8;
-            const int off = (c >> 3) * kMnAtomBytes + (k >> 3) * 1024 + (k & 7) * 128 +
-                            (((c & 7) ^ (k & 7)) << 4);
-            cp_async_16_zfill(base + off, src, in ? 16u : 0u);
-          }
-        }
-        idx_cur = idx_1;
-        idx_1 = idx_2;
-        idx_2 = idx_3;
-        idx_3 = idx_4;
+        for (int i = 0; i < 8; ++i) cp_async_16((SWAP ? sa + kATileBytes : sa) + dst_k[i], src_k[i] + kb * BK);
         cp_async_arrive_noinc(PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
@@ -1134,14 +1186,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle
 // (or the given one).
 int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, uint32_t box_cols,
-             uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+             CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return OCCULT_ERR_CUDA;
+  const int esize = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esize};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? OCCULT_OK : OCCULT_ERR_CUDA;
@@ -1172,7 +1226,9 @@ int operand_map(CUtensorMap* m, int mode, const void* ptr, int64_t rows, int64_t
                 uint32_t k_major_rows) {
   if (mode == OP_TMA_K) return make_map(m, ptr, rows, cols, BK, k_major_rows);
   if (mode == OP_TMA_MN) return make_map(m, ptr, rows, cols, 64, BK);
-  // gathered operands are copied by cp.async: a valid placeholder map
+  // MN-major gathers: tile::gather4 of 64-column rows (the box is one row high)
+  if (mode == OP_GATHER_MN) return make_map(m, ptr, rows, cols, 64, 1);
+  // K-major gathers are copied by cp.async: a valid placeholder map
   return make_map(m, ptr, rows, cols, BK, BK);
 }
 
@@ -1183,7 +1239,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(threads_for(AM, BMODE));
-  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP);
+  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP, WGRAD);
   cfg.stream = ctx.stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
@@ -1199,7 +1255,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   static int n_pairs = 0;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_bytes(PAIR, EPI, SWAP));
+                                    smem_bytes(PAIR, EPI, SWAP, WGRAD));
     if (PAIR && attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
       attr_err = cudaOccupancyMaxActiveClusters(&n_pairs, kern, &cfg);
@@ -1256,6 +1312,12 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // the SwiGLU backward's G|U (in) and dG|dU (out): [rows, 2 N_out] bf16, boxes of
   // 32 columns x 32 rows with the 64-byte swizzle; unused (zero) otherwise
   CUtensorMap mc{}, md{};
+  if (g.wgrad) {
+    // the weight gradients' fp32 output [n_groups * M_total, ldo], 32 x 32 boxes
+    rc = make_map(&md, g.out, static_cast<int64_t>(g.n_seg) * g.M_total, g.ldo, 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    if (rc) return rc;
+  }
   if (epi_eff == EPI_SWIGLU_BWD) {
     if (reinterpret_cast<uintptr_t>(g.gu_in) % 16 != 0) return OCCULT_ERR_UNSUPPORTED;
     rc = make_map(&mc, g.gu_in, g.max_rows, 2ll * g.N_out, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -1277,6 +1339,7 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   const bool a_gathered = op_gathered(g.a_mode);
   p.g_ptr = static_cast<const __nv_bfloat16*>(a_gathered ? g.A : g.B);
   p.g_ld = a_gathered ? g.a_cols : g.b_cols;
+  p.g_rows = static_cast<int>(a_gathered ? g.a_rows : g.b_rows);
   p.b_group_rows = g.b_group_rows;
   p.half_n = g.epi == EPI_SWIGLU ? g.N_out : (g.epi == EPI_SWIGLU_BWD ? g.N_out : 0);
   p.row_gate = g.row_gate;
