@@ -114,23 +114,19 @@ constexpr int kTailBytes = (static_cast<int>(sizeof(SmemTail)) + 127) & ~127;
 constexpr int kEpiBytes = kEpiWarps * 32 * 32 * 4;
 // Offset of the epilogue buffers from the tail: the SwiGLU backward's slots are
 // TMA boxes with the 64-byte swizzle and start on 1024-byte boundaries.
-__host__ __device__ constexpr int epi_off(int epi, bool swap = false, bool wgrad = false) {
-  return (epi == EPI_SWIGLU_BWD && !swap) || wgrad ? (kTailBytes + 1023) & ~1023 : kTailBytes;
+__host__ __device__ constexpr int epi_off(int epi, bool swap = false) {
+  return epi == EPI_SWIGLU_BWD && !swap ? (kTailBytes + 1023) & ~1023 : kTailBytes;
 }
 static_assert(epi_bytes_for(EPI_F32) == kEpiBytes && epi_bytes_for(EPI_SWIGLU_BWD) == 2 * kEpiBytes,
               "epilogue buffers: 4 KB a warp, 8 KB a warp for the SwiGLU backward");
-// (the weight gradients' staging buffers are TMA store sources: 1024-byte aligned)
-__host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false,
-                                             bool wgrad = false) {
+__host__ __device__ constexpr int smem_bytes(bool pair, int epi, bool swap = false) {
   return 1024 /*alignment slack*/ + stages_for(pair, epi, swap) * stage_bytes(pair) +
-         epi_off(epi, swap, wgrad) + epi_bytes_for(epi, swap);
+         epi_off(epi, swap) + epi_bytes_for(epi, swap);
 }
 static_assert(smem_bytes(false, EPI_F32) <= 232448 && smem_bytes(true, EPI_F32) <= 232448 &&
               smem_bytes(false, EPI_SWIGLU) <= 232448 && smem_bytes(true, EPI_SWIGLU) <= 232448 &&
               smem_bytes(false, EPI_SWIGLU_BWD) <= 232448 &&
-              smem_bytes(true, EPI_SWIGLU_BWD) <= 232448 &&
-              smem_bytes(false, EPI_F32, false, true) <= 232448 &&
-              smem_bytes(true, EPI_F32, false, true) <= 232448,
+              smem_bytes(true, EPI_SWIGLU_BWD) <= 232448,
               "shared memory");
 
 struct Params {
@@ -426,7 +422,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (WGRAD) {
     // the segments in order of decreasing rows (ties by index) into mt_off, the
     // rows staged in the epilogue buffers, which nothing else uses yet
-    int* len = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(tail) + epi_off(EPI, SWAP, WGRAD));
+    int* len = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes);
     for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) len[s] = seg_at(p, s + 1) - seg_at(p, s);
     __syncthreads();
     for (int s = threadIdx.x; s < p.n_seg; s += blockDim.x) {
@@ -721,8 +717,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t t_row = tbase + a * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int wrows = max(0, min(32, ti.rows - quarter * 32));  // valid rows of this warp
       const int64_t wrow0 = ti.m0 + quarter * 32;
-      uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) +
-                                                   epi_off(EPI, SWAP, WGRAD)) +
+      uint32_t* ebuf = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(tail) + kTailBytes) +
                        (warp - kEpiWarp0) * 32 * 32;
       uint32_t v0[32], v1[32];
       if (SWAP) {
@@ -1004,29 +999,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
               for (int i = 0; i < 32; ++i) v0[i] = 0u;
             }
-            if (WGRAD && wrows == 32) {
-              // the warp's 32 x 32 fp32 block as one TMA box store: the staging
-              // buffer holds it in the 128-byte swizzle the box takes (once the
-              // previous box has been read out of it)
-              if (lane == 0) bulk_wait_read<0>();
-              __syncwarp();
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                stage_v4(ebuf, j, make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]));
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_store_2d(&tmD, ebuf, col0 + c, ti.grp * p.M_total + static_cast<int>(wrow0));
-                bulk_commit();
-              }
-            } else {
-              if (WGRAD) {
-                if (lane == 0) bulk_wait_read<0>();  // the buffer's last box has left
-                __syncwarp();
-              }
-              store_rows<32>(ebuf, v0, reinterpret_cast<char*>(obase + wrow0 * p.ldo + col0 + c),
-                             p.ldo * 4, wrows);
-            }
+            store_rows<32>(ebuf, v0, reinterpret_cast<char*>(obase + wrow0 * p.ldo + col0 + c),
+                           p.ldo * 4, wrows);
           }
         }
       }
@@ -1038,7 +1012,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         else mbar_arrive(&tail->tempty[a]);
       }
     }
-    if (WGRAD && lane == 0) bulk_wait<0>();  // the weight gradients' boxes are out
     if (kGuStaged) {
       // the TMA stores complete, and a load still in flight (after a timeout)
       // lands, before the CTA may exit
@@ -1239,7 +1212,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(threads_for(AM, BMODE));
-  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP, WGRAD);
+  cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP);
   cfg.stream = ctx.stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
@@ -1255,7 +1228,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   static int n_pairs = 0;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    smem_bytes(PAIR, EPI, SWAP, WGRAD));
+                                    smem_bytes(PAIR, EPI, SWAP));
     if (PAIR && attr_err == cudaSuccess) {
       cfg.gridDim = dim3(2 * (ctx.num_sms / 2));
       attr_err = cudaOccupancyMaxActiveClusters(&n_pairs, kern, &cfg);
@@ -1312,12 +1285,6 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // the SwiGLU backward's G|U (in) and dG|dU (out): [rows, 2 N_out] bf16, boxes of
   // 32 columns x 32 rows with the 64-byte swizzle; unused (zero) otherwise
   CUtensorMap mc{}, md{};
-  if (g.wgrad) {
-    // the weight gradients' fp32 output [n_groups * M_total, ldo], 32 x 32 boxes
-    rc = make_map(&md, g.out, static_cast<int64_t>(g.n_seg) * g.M_total, g.ldo, 32, 32,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
-    if (rc) return rc;
-  }
   if (epi_eff == EPI_SWIGLU_BWD) {
     if (reinterpret_cast<uintptr_t>(g.gu_in) % 16 != 0) return OCCULT_ERR_UNSUPPORTED;
     rc = make_map(&mc, g.gu_in, g.max_rows, 2ll * g.N_out, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
