@@ -407,7 +407,7 @@ def run_ours(args, cfg, world, rank, local):
                                                               moe.x_sfd, moe.sfd_tok, stream)))
     calls.append(("expert_up", lambda: occ.occult_expert_up(
         ds, moe.x_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement, moe.w["w1"],
-        moe.h_epd, moe.gu_epd, stream=stream)))
+        moe.h_epd, moe.gu_epd, x_epd=moe.x_epd, stream=stream)))
     atomic = moe.merge == "atomic"
     if atomic:
         # shared experts write y; the down-projection adds every EPD row into its
@@ -458,17 +458,18 @@ def run_ours(args, cfg, world, rank, local):
         calls += [
             ("dgrad_down", lambda: occ.occult_expert_dgrad_down(
                 ds, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
-                moe.w["w2"], moe.gu_epd, moe.dgu_epd, moe.dg_epd, moe.bwd_ws, stream)),
+                moe.w["w2"], moe.gu_epd, moe.dgu_epd, moe.dg_epd, moe.bwd_ws, dy_epd=moe.dy_epd,
+                stream=stream)),
             ("dgrad_up", lambda: occ.occult_expert_dgrad_up(
                 ds, moe.dgu_epd, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
                 moe.dx if atomic else moe.dx_epd, sfd_tok=moe.sfd_tok if atomic else None,
                 zero_dx=False, stream=stream)),
             ("wgrad_down", lambda: occ.occult_expert_wgrad_down(
-                ds, moe.dy_sfd, moe.epd_src, moe.exp_off, moe.placement, moe.h_epd, moe.dw2,
-                stream)),
+                ds, None, None, moe.exp_off, moe.placement, moe.h_epd, moe.dw2,
+                dy_epd=moe.dy_epd, stream=stream)),
             ("wgrad_up", lambda: occ.occult_expert_wgrad_up(
-                ds, moe.x_sfd, moe.epd_src, moe.exp_off, moe.placement, moe.dgu_epd, moe.dw1,
-                stream)),
+                ds, None, None, moe.exp_off, moe.placement, moe.dgu_epd, moe.dw1,
+                x_epd=moe.x_epd, stream=stream)),
         ]
         if not atomic:
             calls.append(("combine_dx", lambda: occ.occult_combine(
@@ -584,11 +585,12 @@ def run_ours(args, cfg, world, rank, local):
     n_epd = T * k
     S = cfg.n_shared * cfg.shared_inter
     # algorithmic work per launch: FLOPs and the bytes that must cross HBM once
-    # (the training step's up-projection also writes G | U for the backward)
+    # (the training step's up-projection also writes G | U and the padded EPD copy
+    # of its gathered x rows for the backward)
     work = {
         "expert_up": (4.0 * d * I * n_epd,
                       cfg.n_experts * 2 * I * d * b + n_sfd * d * b + n_epd * I * b
-                      + (n_epd * 2 * I * b if train else 0)),
+                      + (n_epd * 2 * I * b + n_epd * d * b if train else 0)),
     }
     if atomic:
         # weights, h, and y written once (read once more when it holds the shared
@@ -602,17 +604,18 @@ def run_ours(args, cfg, world, rank, local):
         work["shared_ffn"] = (6.0 * d * S * T, 3 * S * d * b + T * d * b + T * S * b + T * d * 4)
     if train:
         # the backward's four GEMMs, twice the forward's FLOPs in all.  Bytes of each:
-        #  dgrad_down  W_d, the gathered dy rows, G|U read, dG|dU written
+        #  dgrad_down  W_d, the gathered dy rows, G|U read, dG|dU and the padded
+        #              EPD copy of the dy rows written
         #  dgrad_up    dG|dU, [W_g; W_u], dx written once (merged) or fp32 EPD rows
-        #  wgrad_down  the gathered dy rows, h', dW_d written in fp32
-        #  wgrad_up    dG|dU, the gathered x rows, dW_g|u written in fp32
+        #  wgrad_down  the dy rows' EPD copy, h', dW_d written in fp32
+        #  wgrad_up    dG|dU, the x rows' EPD copy, dW_g|u written in fp32
         Ne = cfg.n_experts
         work["dgrad_down"] = (2.0 * d * I * n_epd, Ne * d * I * b + n_sfd * d * b
-                              + 2 * n_epd * 2 * I * b)
+                              + 2 * n_epd * 2 * I * b + n_epd * d * b)
         work["dgrad_up"] = (4.0 * d * I * n_epd, n_epd * 2 * I * b + Ne * 2 * I * d * b
                             + (T * d * 4 if atomic else n_epd * d * 4))
-        work["wgrad_down"] = (2.0 * d * I * n_epd, n_sfd * d * b + n_epd * I * b + Ne * d * I * 4)
-        work["wgrad_up"] = (4.0 * d * I * n_epd, n_epd * 2 * I * b + n_sfd * d * b
+        work["wgrad_down"] = (2.0 * d * I * n_epd, n_epd * d * b + n_epd * I * b + Ne * d * I * 4)
+        work["wgrad_up"] = (4.0 * d * I * n_epd, n_epd * 2 * I * b + n_epd * d * b
                             + Ne * 2 * I * d * 4)
     ridge = tflops * 1e12 / (hbm * 1e9)  # flop per byte where the two roofs meet
     kernels = {c: {"ms": per_call[c]} for c in names}

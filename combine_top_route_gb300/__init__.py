@@ -38,6 +38,7 @@ WS_BUILD_BRIM = 0
 WS_PROFILE_COACT = 1
 WS_EXPERT_BWD = 2
 STATIC_SCRATCH_BYTES = 1183744   # OCCULT_STATIC_SCRATCH_BYTES
+EPD_PAD = 128                    # OCCULT_EPD_PAD
 
 
 class occult_desc_t(ctypes.Structure):
@@ -86,7 +87,7 @@ _SIGNATURES = {
     "occult_build_brim_noalloc": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                  _VP, _VP, _VP, _VP]),
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "occult_expert_up": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_expert_up": (ctypes.c_int, [_D] + [_VP] * 10),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down_merge": (ctypes.c_int, [_D] + [_VP] * 7 + [_I32, _VP]),
     "occult_expert_ffn": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -98,12 +99,12 @@ _SIGNATURES = {
     "occult_shard_plan": (ctypes.c_int, [_D, _I32] + [_VP] * 8),
     "occult_all_to_all": (ctypes.c_int, [_D, _I32, _VP, _VP, _VP, _VP, _VP, ctypes.c_int64,
                                          _I32, _VP]),
-    "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 16 + [ctypes.c_size_t, _VP]),
-    "occult_expert_bwd_merge": (ctypes.c_int, [_D] + [_VP] * 17 + [ctypes.c_size_t, _VP]),
-    "occult_expert_dgrad_down": (ctypes.c_int, [_D] + [_VP] * 10 + [ctypes.c_size_t, _VP]),
+    "occult_expert_bwd": (ctypes.c_int, [_D] + [_VP] * 18 + [ctypes.c_size_t, _VP]),
+    "occult_expert_bwd_merge": (ctypes.c_int, [_D] + [_VP] * 19 + [ctypes.c_size_t, _VP]),
+    "occult_expert_dgrad_down": (ctypes.c_int, [_D] + [_VP] * 11 + [ctypes.c_size_t, _VP]),
     "occult_expert_dgrad_up": (ctypes.c_int, [_D] + [_VP] * 7 + [_I32, _VP]),
-    "occult_expert_wgrad_down": (ctypes.c_int, [_D] + [_VP] * 7),
-    "occult_expert_wgrad_up": (ctypes.c_int, [_D] + [_VP] * 7),
+    "occult_expert_wgrad_down": (ctypes.c_int, [_D] + [_VP] * 8),
+    "occult_expert_wgrad_up": (ctypes.c_int, [_D] + [_VP] * 8),
     "occult_zero_f32": (ctypes.c_int, [_VP, ctypes.c_int64, _VP]),
     "occult_gate_grad": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_profile_coact": (ctypes.c_int, [_D, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
@@ -162,6 +163,12 @@ def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def epd_copy_rows(desc: occult_desc_t) -> int:
+    """Rows of a padded EPD copy (x_epd, dy_epd): expert e's rows start at
+    exp_off[e] + EPD_PAD * e, zeros after them to the next multiple of EPD_PAD."""
+    return desc.T * desc.top_k + EPD_PAD * desc.n_experts
 
 
 def check_desc(desc: occult_desc_t) -> int:
@@ -283,7 +290,8 @@ def occult_dispatch(desc, x, brim0, vmask, x_sfd, sfd_tok=None, stream=None):
 
 
 def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd=None,
-                     stream=None):
+                     x_epd=None, stream=None):
+    """h' (and, training, G|U and the padded EPD copy x_epd of the gathered rows)."""
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt = desc.torch_dtype
     _call("occult_expert_up", ctypes.byref(desc),
@@ -293,16 +301,19 @@ def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_e
           _dev(exp_off, torch.int32, Ne + 1, "exp_off"),
           _dev(placement, torch.int32, Ne, "placement"),
           _dev(w1, dt, Ne * 2 * I * d, "w1"), _dev(h_epd, dt, T * k * I, "h_epd"),
-          _dev(gu_epd, dt, T * k * 2 * I, "gu_epd", nullable=True), _stream(stream))
+          _dev(gu_epd, dt, T * k * 2 * I, "gu_epd", nullable=True),
+          _dev(x_epd, dt, epd_copy_rows(desc) * d, "x_epd", nullable=True), _stream(stream))
 
 
 def occult_expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
-                      gu_epd, dgu_epd, dx_epd, dw1, dw2, dg_epd, ws, stream=None):
+                      gu_epd, dgu_epd, dx_epd, dw1, dw2, dg_epd, ws, x_epd=None, dy_epd=None,
+                      stream=None):
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
     n_sfd_max = T * min(k, desc.n_vdev)
     need = workspace_size(desc, WS_EXPERT_BWD)
-    _call("occult_expert_bwd", ctypes.byref(desc), _dev(x_sfd, dt, n_sfd_max * d, "x_sfd"),
+    _call("occult_expert_bwd", ctypes.byref(desc),
+          _dev(x_sfd, dt, n_sfd_max * d, "x_sfd", nullable=x_epd is not None),
           _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
@@ -310,19 +321,22 @@ def occult_expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement
           _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
           _dev(dx_epd, f32, T * k * d, "dx_epd"), _dev(dw1, f32, Ne * 2 * I * d, "dw1"),
           _dev(dw2, f32, Ne * d * I, "dw2"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(x_epd, dt, epd_copy_rows(desc) * d, "x_epd", nullable=True),
+          _dev(dy_epd, dt, epd_copy_rows(desc) * d, "dy_epd", nullable=True),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
 
 
 def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2,
                             h_epd, gu_epd, dgu_epd, sfd_tok, dx, dw1, dw2, dg_epd, ws,
-                            stream=None):
+                            x_epd=None, dy_epd=None, stream=None):
     """occult_expert_bwd with dx merged by fp32 atomics into the token rows (occult.h)."""
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
     n_sfd_max = T * min(k, desc.n_vdev)
     need = workspace_size(desc, WS_EXPERT_BWD)
-    _call("occult_expert_bwd_merge", ctypes.byref(desc), _dev(x_sfd, dt, n_sfd_max * d, "x_sfd"),
+    _call("occult_expert_bwd_merge", ctypes.byref(desc),
+          _dev(x_sfd, dt, n_sfd_max * d, "x_sfd", nullable=x_epd is not None),
           _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
@@ -331,12 +345,14 @@ def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, pla
           _dev(sfd_tok, i32, n_sfd_max, "sfd_tok"), _dev(dx, f32, T * d, "dx"),
           _dev(dw1, f32, Ne * 2 * I * d, "dw1"), _dev(dw2, f32, Ne * d * I, "dw2"),
           _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(x_epd, dt, epd_copy_rows(desc) * d, "x_epd", nullable=True),
+          _dev(dy_epd, dt, epd_copy_rows(desc) * d, "dy_epd", nullable=True),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
 
 
 def occult_expert_dgrad_down(desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd,
-                             dgu_epd, dg_epd, ws, stream=None):
+                             dgu_epd, dg_epd, ws, dy_epd=None, stream=None):
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
     need = workspace_size(desc, WS_EXPERT_BWD)
@@ -346,6 +362,7 @@ def occult_expert_dgrad_down(desc, dy_sfd, epd_src, epd_gate, exp_off, placement
           _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(placement, i32, Ne, "placement"),
           _dev(w2, dt, Ne * d * I, "w2"), _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"),
           _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"), _dev(dg_epd, f32, T * k, "dg_epd"),
+          _dev(dy_epd, dt, epd_copy_rows(desc) * d, "dy_epd", nullable=True),
           _dev(ws, torch.uint8, need, "ws", nullable=need == 0), ctypes.c_size_t(need),
           _stream(stream))
 
@@ -364,22 +381,32 @@ def occult_expert_dgrad_up(desc, dgu_epd, epd_src, exp_off, placement, w1, dx, s
           int(bool(zero_dx)), _stream(stream))
 
 
-def occult_expert_wgrad_down(desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2, stream=None):
+def occult_expert_wgrad_down(desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2, dy_epd=None,
+                             stream=None):
+    """dW2; the dy rows gathered from dy_sfd, or read from their padded EPD copy dy_epd."""
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, i32 = desc.torch_dtype, torch.int32
+    tiles = dy_epd is not None
     _call("occult_expert_wgrad_down", ctypes.byref(desc),
-          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd"),
-          _dev(epd_src, i32, T * k, "epd_src"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd", nullable=tiles),
+          _dev(epd_src, i32, T * k, "epd_src", nullable=tiles),
+          _dev(dy_epd, dt, epd_copy_rows(desc) * d, "dy_epd", nullable=True),
+          _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(h_epd, dt, T * k * I, "h_epd"),
           _dev(dw2, torch.float32, Ne * d * I, "dw2"), _stream(stream))
 
 
-def occult_expert_wgrad_up(desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1, stream=None):
+def occult_expert_wgrad_up(desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1, x_epd=None,
+                           stream=None):
+    """dW1; the x rows gathered from x_sfd, or read from their padded EPD copy x_epd."""
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, i32 = desc.torch_dtype, torch.int32
+    tiles = x_epd is not None
     _call("occult_expert_wgrad_up", ctypes.byref(desc),
-          _dev(x_sfd, dt, T * min(k, desc.n_vdev) * d, "x_sfd"),
-          _dev(epd_src, i32, T * k, "epd_src"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(x_sfd, dt, T * min(k, desc.n_vdev) * d, "x_sfd", nullable=tiles),
+          _dev(epd_src, i32, T * k, "epd_src", nullable=tiles),
+          _dev(x_epd, dt, epd_copy_rows(desc) * d, "x_epd", nullable=True),
+          _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(dgu_epd, dt, T * k * 2 * I, "dgu_epd"),
           _dev(dw1, torch.float32, Ne * 2 * I * d, "dw1"), _stream(stream))
 

@@ -228,7 +228,8 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
 
 static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* x_sfd,
                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
-                     const int32_t* placement, const void* w1, void* h_epd, void* gu_epd) {
+                     const int32_t* placement, const void* w1, void* h_epd, void* gu_epd,
+                     void* x_epd) {
   GroupedGemm g;
   g.a_mode = OP_GATHER_K;
   g.b_mode = OP_TMA_K;
@@ -252,6 +253,7 @@ static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void
   g.N_out = desc->inter;
   g.K = desc->d;
   g.gu_out = gu_epd;
+  g.a_copy = x_epd;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g)
                                     : launch_grouped_gemm_f32(ctx, g);
 }
@@ -290,15 +292,18 @@ static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const vo
 
 int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
                      const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
-                     const void* w1, void* h_epd, void* gu_epd, occult_stream_t stream) {
+                     const void* w1, void* h_epd, void* gu_epd, void* x_epd,
+                     occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   OCCULT_REQUIRE(exp_off && placement && w1);
   OCCULT_REQUIRE(desc->T == 0 || (x_sfd && epd_src && epd_gate && h_epd));
+  OCCULT_REQUIRE(!(x_epd && !gu_epd));
   OCCULT_CTX(stream);
   if (desc->T == 0) return OCCULT_OK;
   if (gu_epd && desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
-  return expert_up(ctx, desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd);
+  return expert_up(ctx, desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd,
+                   x_epd);
 }
 
 int occult_expert_down(const occult_desc_t* desc, const void* h_epd, const int32_t* exp_off,
@@ -336,7 +341,7 @@ int occult_expert_ffn(const occult_desc_t* desc, const void* x_sfd, const int32_
                       const void* w1, const void* w2, void* h_epd, void* y_epd,
                       occult_stream_t stream) {
   int rc = occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd,
-                            nullptr, stream);
+                            nullptr, nullptr, stream);
   if (rc) return rc;
   return occult_expert_down(desc, h_epd, exp_off, placement, w2, y_epd, stream);
 }
@@ -400,11 +405,12 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
 // The four GEMMs of the expert backward.  Argument checks are done by the public
 // entry points; T > 0 here.
 
-// dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg
+// dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg; with
+// dy_epd given, the gathered dy rows are also written to that padded EPD copy
 static int dgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dy_sfd,
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w2, const void* gu_epd,
-                      void* dgu_epd, float* dg_epd, void* ws) {
+                      void* dgu_epd, float* dg_epd, void* dy_epd, void* ws) {
   const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
   const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
   const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
@@ -423,6 +429,7 @@ static int dgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const voi
   g.row_gate = epd_gate;
   g.out = dgu_epd; g.ldo = 2ll * I;
   g.gu_in = gu_epd; g.dg_part = dg_part;
+  g.a_copy = dy_epd;
   int rc = launch_grouped_gemm_bf16(ctx, g);
   if (rc) return rc;
   return launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), 2 * ((I + 255) / 256), dg_epd);
@@ -453,10 +460,11 @@ static int dgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void*
   return launch_grouped_gemm_bf16(ctx, h);
 }
 
-// dW_d[e] = sum over e's rows of dy_sfd[src] (x) h' : M = d, N = I
+// dW_d[e] = sum over e's rows of dy_sfd[src] (x) h' : M = d, N = I; the dy rows
+// gathered from dy_sfd, or read as tiles from their padded EPD copy dy_epd
 static int wgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dy_sfd,
-                      const int32_t* epd_src, const int32_t* exp_off, const int32_t* placement,
-                      const void* h_epd, float* dw2) {
+                      const int32_t* epd_src, const void* dy_epd, const int32_t* exp_off,
+                      const int32_t* placement, const void* h_epd, float* dw2) {
   const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
   const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
   const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
@@ -467,6 +475,12 @@ static int wgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const voi
   w.epi = EPI_F32;
   w.A = dy_sfd; w.a_rows = n_sfd_max; w.a_cols = d;
   w.gather = epd_src;
+  if (dy_epd) {
+    w.a_mode = OP_TMA_MN;
+    w.A = dy_epd; w.a_rows = rows + static_cast<int64_t>(OCCULT_EPD_PAD) * Ne;
+    w.a_kpad = OCCULT_EPD_PAD;
+    w.gather = nullptr;
+  }
   w.B = h_epd; w.b_rows = rows; w.b_cols = I;
   w.seg_off = exp_off; w.seg_group = placement; w.n_seg = Ne;
   w.M_total = d; w.N_out = I;
@@ -474,10 +488,11 @@ static int wgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const voi
   return launch_grouped_gemm_bf16(ctx, w);
 }
 
-// [dW_g; dW_u][e] = sum over e's rows of [dG|dU] (x) x_sfd[src] : M = 2I, N = d
+// [dW_g; dW_u][e] = sum over e's rows of [dG|dU] (x) x_sfd[src] : M = 2I, N = d; the x
+// rows gathered from x_sfd, or read as tiles from their padded EPD copy x_epd
 static int wgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* x_sfd,
-                    const int32_t* epd_src, const int32_t* exp_off, const int32_t* placement,
-                    const void* dgu_epd, float* dw1) {
+                    const int32_t* epd_src, const void* x_epd, const int32_t* exp_off,
+                    const int32_t* placement, const void* dgu_epd, float* dw1) {
   const int64_t rows = static_cast<int64_t>(desc->T) * desc->top_k;
   const int64_t n_sfd_max = static_cast<int64_t>(desc->T) * min_i(desc->top_k, desc->n_vdev);
   const int Ne = desc->n_experts, d = desc->d, I = desc->inter;
@@ -489,6 +504,12 @@ static int wgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void*
   v.A = dgu_epd; v.a_rows = rows; v.a_cols = 2ll * I;
   v.B = x_sfd; v.b_rows = n_sfd_max; v.b_cols = d;
   v.gather = epd_src;
+  if (x_epd) {
+    v.b_mode = OP_TMA_MN;
+    v.B = x_epd; v.b_rows = rows + static_cast<int64_t>(OCCULT_EPD_PAD) * Ne;
+    v.b_kpad = OCCULT_EPD_PAD;
+    v.gather = nullptr;
+  }
   v.seg_off = exp_off; v.seg_group = placement; v.n_seg = Ne;
   v.M_total = 2 * I; v.N_out = d;
   v.out = dw1; v.ldo = d; v.out_group_stride = 2ll * I * d;
@@ -513,14 +534,15 @@ static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w1, const void* w2,
                       const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_out,
-                      const int32_t* sfd_tok, float* dw1, float* dw2, float* dg_epd, void* ws,
-                      size_t ws_bytes, occult_stream_t stream) {
+                      const int32_t* sfd_tok, float* dw1, float* dw2, float* dg_epd,
+                      const void* x_epd, void* dy_epd, void* ws, size_t ws_bytes,
+                      occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && w1 && w2 && dw1 && dw2);
-  OCCULT_REQUIRE(desc->T == 0 || (x_sfd && dy_sfd && epd_src && epd_gate && h_epd && gu_epd &&
-                                  dgu_epd && dx_out && dg_epd));
+  OCCULT_REQUIRE(desc->T == 0 || ((x_sfd || x_epd) && dy_sfd && epd_src && epd_gate && h_epd &&
+                                  gu_epd && dgu_epd && dx_out && dg_epd));
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
@@ -534,23 +556,24 @@ static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
     if (rc) return rc;
   }
   rc = dgrad_down(ctx, desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd, dgu_epd,
-                  dg_epd, ws);
+                  dg_epd, dy_epd, ws);
   if (rc) return rc;
   rc = dgrad_up(ctx, desc, dgu_epd, epd_src, exp_off, placement, w1, sfd_tok, dx_out);
   if (rc) return rc;
-  rc = wgrad_down(ctx, desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2);
+  rc = wgrad_down(ctx, desc, dy_sfd, epd_src, dy_epd, exp_off, placement, h_epd, dw2);
   if (rc) return rc;
-  return wgrad_up(ctx, desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1);
+  return wgrad_up(ctx, desc, x_sfd, epd_src, x_epd, exp_off, placement, dgu_epd, dw1);
 }
 
 int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w1, const void* w2,
                       const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
-                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
-                      occult_stream_t stream) {
+                      float* dw1, float* dw2, float* dg_epd, const void* x_epd, void* dy_epd,
+                      void* ws, size_t ws_bytes, occult_stream_t stream) {
   return expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
-                    gu_epd, dgu_epd, dx_epd, nullptr, dw1, dw2, dg_epd, ws, ws_bytes, stream);
+                    gu_epd, dgu_epd, dx_epd, nullptr, dw1, dw2, dg_epd, x_epd, dy_epd, ws,
+                    ws_bytes, stream);
 }
 
 int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
@@ -558,17 +581,19 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
                             const int32_t* placement, const void* w1, const void* w2,
                             const void* h_epd, const void* gu_epd, void* dgu_epd,
                             const int32_t* sfd_tok, float* dx, float* dw1, float* dw2,
-                            float* dg_epd, void* ws, size_t ws_bytes, occult_stream_t stream) {
+                            float* dg_epd, const void* x_epd, void* dy_epd, void* ws,
+                            size_t ws_bytes, occult_stream_t stream) {
   if (desc && desc->T > 0 && !sfd_tok) return OCCULT_ERR_INVALID_ARG;
   return expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement, w1, w2, h_epd,
-                    gu_epd, dgu_epd, dx, sfd_tok, dw1, dw2, dg_epd, ws, ws_bytes, stream);
+                    gu_epd, dgu_epd, dx, sfd_tok, dw1, dw2, dg_epd, x_epd, dy_epd, ws, ws_bytes,
+                    stream);
 }
 
 int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
                              const int32_t* epd_src, const float* epd_gate,
                              const int32_t* exp_off, const int32_t* placement, const void* w2,
-                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* ws,
-                             size_t ws_bytes, occult_stream_t stream) {
+                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* dy_epd,
+                             void* ws, size_t ws_bytes, occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
@@ -579,7 +604,7 @@ int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
   OCCULT_CTX(stream);
   if (desc->T == 0) return OCCULT_OK;
   return dgrad_down(ctx, desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd, dgu_epd,
-                    dg_epd, ws);
+                    dg_epd, dy_epd, ws);
 }
 
 int occult_expert_dgrad_up(const occult_desc_t* desc, const void* dgu_epd, const int32_t* epd_src,
@@ -603,30 +628,30 @@ int occult_expert_dgrad_up(const occult_desc_t* desc, const void* dgu_epd, const
 }
 
 int occult_expert_wgrad_down(const occult_desc_t* desc, const void* dy_sfd,
-                             const int32_t* epd_src, const int32_t* exp_off,
+                             const int32_t* epd_src, const void* dy_epd, const int32_t* exp_off,
                              const int32_t* placement, const void* h_epd, float* dw2,
                              occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && dw2);
-  OCCULT_REQUIRE(desc->T == 0 || (dy_sfd && epd_src && h_epd));
+  OCCULT_REQUIRE(desc->T == 0 || ((dy_epd || (dy_sfd && epd_src)) && h_epd));
   OCCULT_CTX(stream);
   if (desc->T == 0) return zero_weights(ctx, dw2, w2_elems(desc));
-  return wgrad_down(ctx, desc, dy_sfd, epd_src, exp_off, placement, h_epd, dw2);
+  return wgrad_down(ctx, desc, dy_sfd, epd_src, dy_epd, exp_off, placement, h_epd, dw2);
 }
 
 int occult_expert_wgrad_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
-                           const int32_t* exp_off, const int32_t* placement,
+                           const void* x_epd, const int32_t* exp_off, const int32_t* placement,
                            const void* dgu_epd, float* dw1, occult_stream_t stream) {
   int rc = check(desc);
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && dw1);
-  OCCULT_REQUIRE(desc->T == 0 || (x_sfd && epd_src && dgu_epd));
+  OCCULT_REQUIRE(desc->T == 0 || ((x_epd || (x_sfd && epd_src)) && dgu_epd));
   OCCULT_CTX(stream);
   if (desc->T == 0) return zero_weights(ctx, dw1, w1_elems(desc));
-  return wgrad_up(ctx, desc, x_sfd, epd_src, exp_off, placement, dgu_epd, dw1);
+  return wgrad_up(ctx, desc, x_sfd, epd_src, x_epd, exp_off, placement, dgu_epd, dw1);
 }
 
 int occult_zero_f32(float* buf, int64_t n, occult_stream_t stream) {

@@ -62,6 +62,7 @@ constexpr int kMnAtomBytes = BK * 128;     // one 64-element MN atom over the 64
 constexpr int kEpiWarp0 = 2;               // first epilogue warp
 constexpr int kEpiWarps = 8;               // two per TMEM lane quarter, half the columns each
 constexpr int kGatherWarp0 = kEpiWarp0 + kEpiWarps;  // first cp.async producer warp
+constexpr int kCopyWarp = kGatherWarp0 + 4;           // stores the gathered A rows
 constexpr int kMaxSeg = OCCULT_MAX_EXPERTS;
 constexpr uint32_t kTmemCols = 512;
 
@@ -86,8 +87,15 @@ __host__ __device__ constexpr int b_stage_bytes(bool pair) { return pair ? kBTil
 __host__ __device__ constexpr int stage_bytes(bool pair) { return kATileBytes + b_stage_bytes(pair); }
 __host__ __device__ constexpr bool op_gathered(int m) { return m == OP_GATHER_K || m == OP_GATHER_MN; }
 __host__ __device__ constexpr bool op_mn(int m) { return m == OP_TMA_MN || m == OP_GATHER_MN; }
-__host__ __device__ constexpr int threads_for(int am, int bm) {
-  return 32 * (kGatherWarp0 + ((op_gathered(am) || op_gathered(bm)) ? 4 : 0));
+// The training GEMMs that gather K-major A rows (the up-projection with the G|U
+// save, the dgrad through W_d) can also write those rows, as they stand in the
+// stages, to a padded EPD copy that the weight gradients then read as tiles: one
+// more warp copies them out.
+__host__ __device__ constexpr bool copies_a(int am, int epi, bool wgrad, bool swap) {
+  return am == OP_GATHER_K && !wgrad && !swap && (epi == EPI_SWIGLU_SAVE || epi == EPI_SWIGLU_BWD);
+}
+__host__ __device__ constexpr int threads_for(int am, int bm, bool copy_a = false) {
+  return 32 * (kGatherWarp0 + ((op_gathered(am) || op_gathered(bm)) ? 4 : 0) + (copy_a ? 1 : 0));
 }
 // kind::f16 instruction descriptor, bf16 A/B, fp32 D, M = 128 (a CTA pair: 256),
 // N = 256; bits 15 and 16 select MN-major A and B
@@ -146,6 +154,12 @@ struct Params {
   int64_t g_ld;                // its row length (elements)
   int g_rows;                  // its rows (an MN-major gather names row g_rows for a
                                // row past the segment: outside the map, zero-filled)
+  int a_kpad, b_kpad;          // wgrad, MN-major TMA operand: segment s's K rows start
+                               // at seg_off[s] + kpad * s (a padded EPD copy) instead
+                               // of seg_off[s]
+  __nv_bfloat16* a_copy;       // copies_a: padded EPD copy of the gathered A rows
+                               // ([rows, K]; segment s's rows from seg_off[s] +
+                               // OCCULT_EPD_PAD * s), or NULL
   int64_t b_group_rows;        // B rows per weight group (forward / dgrad)
   int half_n;                  // SwiGLU: up rows' offset in a B group; SwiGLU bwd: I
   // epilogue
@@ -355,7 +369,7 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 namespace {
 
 template <int AM, int BMODE, int EPI, bool WGRAD, bool PAIR, bool SWAP>
-__global__ void __launch_bounds__(threads_for(AM, BMODE), 1)
+__global__ void __launch_bounds__(threads_for(AM, BMODE, copies_a(AM, EPI, WGRAD, SWAP)), 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC,
@@ -383,6 +397,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   // arrivals (and, in a pair, forwarded by the odd CTA)
   constexpr bool kGatherMN = AM == OP_GATHER_MN || BMODE == OP_GATHER_MN;
   constexpr bool kGatherCp = kGather && !kGatherMN;
+  constexpr bool kCopyA = copies_a(AM, EPI, WGRAD, SWAP);
+  // a stage is released by the MMAs' commit and, when the A rows are copied out,
+  // by the copy warp once its store has read them
+  const bool copy_a = kCopyA && p.a_copy != nullptr;
   constexpr uint32_t kIdesc = idesc_for(AM, BMODE, PAIR);
   // TMA bytes of one stage of one CTA; a pair's even CTA expects both CTAs' bytes
   constexpr uint32_t kTmaCta = (AM == OP_GATHER_K ? 0u : uint32_t(kATileBytes)) +
@@ -408,7 +426,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       // the TMA arrival, plus one per cp.async producer thread (and, in a pair,
       // one forwarded from the odd CTA for all of its producer threads)
       mbar_init(&tail->full[s], kGatherCp ? 1 + 128 + (PAIR ? 1 : 0) : 1);
-      mbar_init(&tail->empty[s], 1);
+      mbar_init(&tail->empty[s], copy_a ? 2 : 1);
       mbar_init(&tail->gfull[s], 128);
     }
     for (int a = 0; a < 2; ++a) {
@@ -484,6 +502,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
           // K row of an MN-major operand: weight rows (dgrad) or EPD rows (wgrad)
           const int krow = WGRAD ? ti.k0 + kb * BK : static_cast<int>(ti.grp * p.b_group_rows) + kb * BK;
+          const int krow_a = WGRAD ? krow + p.a_kpad * ti.seg : krow;
+          const int krow_b = WGRAD ? krow + p.b_kpad * ti.seg : krow;
           if (SWAP) {
             // this CTA's 128 weight rows of the unit's 256 (SwiGLU: 64 gate rows
             // and the 64 up rows of the same units) and 128 rows of its half of
@@ -510,21 +530,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (AM == OP_TMA_K) tma_load_2d_pair(sa, &tmA, kb * BK, ti.m0, lbar);
             if (AM == OP_TMA_MN)
               for (int a = 0; a < BM / 64; ++a)
-                tma_load_2d_pair(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, lbar);
+                tma_load_2d_pair(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow_a, lbar);
             if (BMODE == OP_TMA_K) {
               const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0 +
                                rank * (kSwiGLU ? p.half_n : BN / 2);
               tma_load_2d_pair(sb, &tmB, kb * BK, brow, lbar);
             } else if (BMODE == OP_TMA_MN) {
               for (int a = 0; a < 2; ++a)
-                tma_load_2d_pair(sb + a * kMnAtomBytes, &tmB, n0 + rank * (BN / 2) + 64 * a, krow, lbar);
+                tma_load_2d_pair(sb + a * kMnAtomBytes, &tmB, n0 + rank * (BN / 2) + 64 * a, krow_b, lbar);
             }
           } else {
             mbar_arrive_expect_tx(bar, kTmaBytes);
             if (AM == OP_TMA_K) {
               tma_load_2d(sa, &tmA, kb * BK, ti.m0, bar);
             } else if (AM == OP_TMA_MN) {
-              for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow, bar);
+              for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow_a, bar);
             }
             if (BMODE == OP_TMA_K) {
               const int brow = static_cast<int>(ti.grp * p.b_group_rows) + n0;
@@ -535,7 +555,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 tma_load_2d(sb, &tmB, kb * BK, brow, bar);
               }
             } else if (BMODE == OP_TMA_MN) {
-              for (int a = 0; a < BN / 64; ++a) tma_load_2d(sb + a * kMnAtomBytes, &tmB, n0 + 64 * a, krow, bar);
+              for (int a = 0; a < BN / 64; ++a) tma_load_2d(sb + a * kMnAtomBytes, &tmB, n0 + 64 * a, krow_b, bar);
             }
           }
         }
@@ -1027,7 +1047,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
-  if (kGatherMN && warp >= kGatherWarp0) {
+  if (kGatherMN && warp >= kGatherWarp0 && warp < kCopyWarp) {
     // ---- TMA gathers of the MN-major operand (weight gradients) -----------------
     // K row k of a stage is EPD row k0 + kb*64 + k, whose source row the gather
     // array names (past the segment's end: row g_rows, outside the map, zeros).  Warp gw takes rows
@@ -1086,7 +1106,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
 
-  if (kGatherCp && warp >= kGatherWarp0) {
+  if (kGatherCp && warp >= kGatherWarp0 && warp < kCopyWarp) {
     // ---- cp.async producers for the gathered K-major operand --------------------
     // Every thread arrives on a stage's full barrier asynchronously, when its
     // copies for that stage have landed (cp.async.mbarrier.arrive); the MMA thread
@@ -1100,8 +1120,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
       // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
       // at r*128 + ((c ^ (r % 8)) * 16)
+      // Rows past the tile's valid rows are zero-filled (their source address
+      // clamped to a valid row, from which nothing is read): the copy of the A
+      // rows relies on it for the zeros after a segment's rows.
       const __nv_bfloat16* src_k[8];
       uint32_t dst_k[8];
+      uint32_t live = 0;
       {
         const int gw = warp - kGatherWarp0, chunk = lane & 7, rsub = lane >> 3;
 #pragma unroll
@@ -1110,13 +1134,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           dst_k[i] = static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
           const int rr = max(0, min(r, ti.rows - 1));  // a pair's empty half reads row 0
           src_k[i] = p.g_ptr + static_cast<int64_t>(p.gather[ti.m0 + rr]) * p.g_ld + chunk * 8;
+          live |= (r < ti.rows ? 1u : 0u) << i;
         }
       }
       for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + stage * kStageBytes;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cp_async_16((SWAP ? sa + kATileBytes : sa) + dst_k[i], src_k[i] + kb * BK);
+        for (int i = 0; i < 8; ++i)
+          cp_async_16_zfill((SWAP ? sa + kATileBytes : sa) + dst_k[i], src_k[i] + kb * BK,
+                            ((live >> i) & 1u) ? 16u : 0u);
         cp_async_arrive_noinc(PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage]);
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
@@ -1127,6 +1154,57 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
       *abort_flag = 1;
     }
+  }
+
+  if (kCopyA && warp == kCopyWarp) {
+    // ---- the gathered A rows out to their padded EPD copy -----------------------
+    // Follows the stages as the MMAs do.  Once a stage's A rows have landed (in a
+    // pair's odd CTA: its own cp.async barrier), this CTA's 128 rows of k block kb
+    // are copied out in the unit of N tile kb % n_tiles_n, so that an M tile's
+    // copies are spread over its N tiles' units: 16-byte pieces from shared
+    // memory (undoing the 128-byte swizzle) to global stores, four 128-byte rows
+    // an instruction; the stage is released once the pieces are in registers.
+    // The zero-filled rows after a segment's end land in its padding.
+    if (copy_a) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const int chunk = lane & 7, rsub = lane >> 3;
+      for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+        __nv_bfloat16* dst = p.a_copy + (static_cast<int64_t>(ti.m0) + OCCULT_EPD_PAD * ti.seg) * p.K;
+        for (int kb = 0; kb < ti.kb; ++kb) {
+          uint64_t* landed = PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage];
+          if (!mbar_wait(landed, phase, abort_flag)) { ok = false; break; }
+          if (ti.rows > 0 && kb % p.n_tiles_n == ti.nt) {
+            const uint8_t* sa = smem + stage * kStageBytes;
+            char* out = reinterpret_cast<char*>(dst + kb * BK) + chunk * 16;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint4 v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int r = (g * 8 + j) * 4 + rsub;
+                v[j] = *reinterpret_cast<const uint4*>(sa + r * 128 + ((chunk ^ (r & 7)) << 4));
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int r = (g * 8 + j) * 4 + rsub;
+                st_v4(out + static_cast<int64_t>(r) * p.K * 2, v[j]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tail->empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        if (lane == 0) latch_error(p.dev_err, OCCULT_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1211,7 +1289,7 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
   auto kern = grouped_gemm_tc_kernel<AM, BMODE, EPI, WGRAD, PAIR, SWAP>;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[2];
-  cfg.blockDim = dim3(threads_for(AM, BMODE));
+  cfg.blockDim = dim3(threads_for(AM, BMODE, copies_a(AM, EPI, WGRAD, SWAP)));
   cfg.dynamicSmemBytes = smem_bytes(PAIR, EPI, SWAP);
   cfg.stream = ctx.stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1291,6 +1369,11 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     if (!rc) rc = make_map(&md, g.out, g.max_rows, g.ldo, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (rc) return rc;
   }
+  // the padded EPD copy of the gathered A rows ([rows + OCCULT_EPD_PAD * segments,
+  // K] bf16) is written in 16-byte pieces
+  if (g.a_copy && (!copies_a(g.a_mode, epi_eff, g.wgrad, swap) || !g.seg_off ||
+                   reinterpret_cast<uintptr_t>(g.a_copy) % 16 != 0))
+    return OCCULT_ERR_UNSUPPORTED;
   Params p{};
   p.seg_off = g.seg_off;
   p.seg_group = g.seg_group;
@@ -1308,6 +1391,9 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.g_ld = a_gathered ? g.a_cols : g.b_cols;
   p.g_rows = static_cast<int>(a_gathered ? g.a_rows : g.b_rows);
   p.b_group_rows = g.b_group_rows;
+  p.a_kpad = g.a_kpad;
+  p.b_kpad = g.b_kpad;
+  p.a_copy = static_cast<__nv_bfloat16*>(g.a_copy);
   p.half_n = g.epi == EPI_SWIGLU ? g.N_out : (g.epi == EPI_SWIGLU_BWD ? g.N_out : 0);
   p.row_gate = g.row_gate;
   p.out = g.out;
@@ -1350,6 +1436,10 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     if (am == OP_TMA_MN && bm == OP_GATHER_MN)
       return pair ? launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, true>(ctx, ma, mb, mc, md, p)
                   : launch_tc<OP_TMA_MN, OP_GATHER_MN, EPI_F32, true, false>(ctx, ma, mb, mc, md, p);
+    // both operands as tiles: one of them the padded EPD copy of the rows
+    if (am == OP_TMA_MN && bm == OP_TMA_MN)
+      return pair ? launch_tc<OP_TMA_MN, OP_TMA_MN, EPI_F32, true, true>(ctx, ma, mb, mc, md, p)
+                  : launch_tc<OP_TMA_MN, OP_TMA_MN, EPI_F32, true, false>(ctx, ma, mb, mc, md, p);
   }
   return OCCULT_ERR_UNSUPPORTED;
 }

@@ -89,6 +89,9 @@ struct GroupedGemm {
   const void* B = nullptr;
   int64_t b_rows = 0, b_cols = 0;  // B as stored
   const int32_t* gather = nullptr;
+  int a_kpad = 0, b_kpad = 0;         // wgrad: K rows of segment s at seg_off[s] + kpad * s
+  void* a_copy = nullptr;             // gathered K-major A (training up-projection, dgrad
+                                      // through W_d): padded EPD copy of its rows, or NULL
   int64_t b_group_rows = 0;
   int n_groups = 0;
   const int32_t* seg_off = nullptr;   // device; NULL: one segment of max_rows rows

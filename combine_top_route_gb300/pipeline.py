@@ -35,7 +35,7 @@ from . import (MAX_SOURCES, OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE
                occult_expert_down_merge, occult_expert_bwd_merge,
                occult_expert_up, occult_gate_grad, occult_merge_sfd, occult_route,
                occult_route_similarity, occult_router_grad, occult_shard_plan,
-               occult_shared_ffn, workspace_size)
+               occult_shared_ffn, epd_copy_rows, workspace_size)
 
 
 def desc_for(cfg, T: Optional[int] = None) -> occult_desc_t:
@@ -121,6 +121,10 @@ class OccultMoE:
         if train:
             # forward saves G|U; backward buffers (weight gradients are fp32)
             self.gu_epd = e(T * k, 2 * I, dtype=dt)
+            # the forward's gathered x rows and the backward's gathered dy rows in
+            # padded EPD order, so that the weight gradients read them as tiles
+            self.x_epd = e(epd_copy_rows(desc), d, dtype=dt)
+            self.dy_epd = e(epd_copy_rows(desc), d, dtype=dt)
             self.dy_sfd = e(n_sfd_max, d, dtype=dt)
             self.dgu_epd = e(T * k, 2 * I, dtype=dt)
             # fp32 EPD rows of dx only for the ordered merge
@@ -133,7 +137,7 @@ class OccultMoE:
             self.dlogits = e(T, Ne, dtype=f32)
             self.bwd_ws = e(max(1, workspace_size(desc, WS_EXPERT_BWD)), dtype=torch.uint8)
         else:
-            self.gu_epd = None
+            self.gu_epd = self.x_epd = None
         # sharded-source mode: the sources' send layout and the exchange plan
         self.src_off = None if src_off is None else [int(v) for v in src_off]
         if self.src_off is not None:
@@ -224,7 +228,8 @@ class OccultMoE:
         self.route_and_index(logits, stream)
         self._scatter(x, self.x_sfd, self.sfd_tok, stream)
         occult_expert_up(ds, self.x_sfd, self.epd_src, self.epd_gate, self.exp_off,
-                         self.placement, self.w["w1"], self.h_epd, self.gu_epd, stream)
+                         self.placement, self.w["w1"], self.h_epd, self.gu_epd, self.x_epd,
+                         stream)
         if self.merge == "atomic":
             # the shared experts write y, the routed experts' rows are added to it
             if ds.n_shared:
@@ -272,7 +277,8 @@ class OccultMoE:
             occult_expert_bwd_merge(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate,
                                     self.exp_off, self.placement, self.w["w1"], self.w["w2"],
                                     self.h_epd, self.gu_epd, self.dgu_epd, self.sfd_tok, self.dx,
-                                    self.dw1, self.dw2, self.dg_epd, self.bwd_ws, stream)
+                                    self.dw1, self.dw2, self.dg_epd, self.bwd_ws, self.x_epd,
+                                    self.dy_epd, stream)
         else:
             self._expert_bwd_ordered(stream)
         occult_gate_grad(ds, self.ids, self.placement, self.brim0, self.seg_off, self.brim1,
@@ -285,5 +291,5 @@ class OccultMoE:
         occult_expert_bwd(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate, self.exp_off,
                           self.placement, self.w["w1"], self.w["w2"], self.h_epd, self.gu_epd,
                           self.dgu_epd, self.dx_epd, self.dw1, self.dw2, self.dg_epd, self.bwd_ws,
-                          stream)
+                          self.x_epd, self.dy_epd, stream)
         self._merge(self.dx_epd, self.dx, None, stream)

@@ -70,6 +70,12 @@ extern "C" {
 #define OCCULT_MAX_EXPERTS  256
 #define OCCULT_MAX_VDEV     32
 #define OCCULT_MAX_TOPK     16
+/* Padded EPD copies of gathered rows (x_epd, dy_epd): the EPD rows
+ * exp_off[s] .. exp_off[s+1]-1 of expert slot s sit at rows
+ * exp_off[s] + OCCULT_EPD_PAD * s onwards, followed by zero rows up to a whole
+ * number of OCCULT_EPD_PAD rows from that start; such a copy has
+ * T*top_k + OCCULT_EPD_PAD * n_experts rows of d elements. */
+#define OCCULT_EPD_PAD      128
 
 typedef void* occult_stream_t;   /* cudaStream_t */
 
@@ -306,11 +312,16 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
  *   h_epd  out [T*k, I] layer dtype.
  *   gu_epd out [T*k, 2*I] bf16, nullable: the pre-activations G | U of every EPD
  *          row, saved for occult_expert_bwd (bf16 layers only).
+ *   x_epd  out bf16, nullable (requires gu_epd): the gathered rows A_r written
+ *          to their padded EPD copy (OCCULT_EPD_PAD: T*k + OCCULT_EPD_PAD*Ne
+ *          rows of d), which occult_expert_bwd reads for dw1 instead of
+ *          gathering x_sfd again.
  * bf16 layers run on the tcgen05 tensor cores (fp32 accumulate in TMEM).
  */
 int occult_expert_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
                      const float* epd_gate, const int32_t* exp_off, const int32_t* placement,
-                     const void* w1, void* h_epd, void* gu_epd, occult_stream_t stream);
+                     const void* w1, void* h_epd, void* gu_epd, void* x_epd,
+                     occult_stream_t stream);
 
 /*
  * occult_expert_down -- the second linear layer of Algorithm 8 on the EPD rows:
@@ -461,14 +472,21 @@ int occult_all_to_all(const occult_desc_t* desc, int32_t n_src, const int32_t* c
  *   dw2[e]  = sum_r dy_sfd[src_r] h'_r^T        -> fp32 [Ne, d, I]
  *   dw1[e]  = sum_r [dG | dU]_r x_sfd[src_r]^T  -> fp32 [Ne, 2I, d]
  * Weight gradients are written, not accumulated; experts without rows get zeros.
+ *   x_epd   nullable: the padded EPD copy of the x rows that occult_expert_up
+ *           wrote; given, dw1 reads it as tiles (x_sfd may then be NULL); NULL:
+ *           dw1 gathers x_sfd through epd_src.
+ *   dy_epd  nullable scratch, bf16 [T*k + OCCULT_EPD_PAD*Ne, d]: given, the
+ *           dh' GEMM writes its gathered dy rows there and dw2 reads them as
+ *           tiles; NULL: dw2 gathers dy_sfd again.
+ *   Both choices give the same bits.
  *   ws  occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
  */
 int occult_expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* dy_sfd,
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w1, const void* w2,
                       const void* h_epd, const void* gu_epd, void* dgu_epd, float* dx_epd,
-                      float* dw1, float* dw2, float* dg_epd, void* ws, size_t ws_bytes,
-                      occult_stream_t stream);
+                      float* dw1, float* dw2, float* dg_epd, const void* x_epd, void* dy_epd,
+                      void* ws, size_t ws_bytes, occult_stream_t stream);
 
 /*
  * occult_expert_bwd_merge -- occult_expert_bwd with the merge of dx folded into
@@ -484,7 +502,8 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
                             const int32_t* placement, const void* w1, const void* w2,
                             const void* h_epd, const void* gu_epd, void* dgu_epd,
                             const int32_t* sfd_tok, float* dx, float* dw1, float* dw2,
-                            float* dg_epd, void* ws, size_t ws_bytes, occult_stream_t stream);
+                            float* dg_epd, const void* x_epd, void* dy_epd, void* ws,
+                            size_t ws_bytes, occult_stream_t stream);
 
 /*
  * The four GEMMs of occult_expert_bwd as separate calls, for callers that time,
@@ -495,13 +514,15 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
  * occult_expert_dgrad_down -- dh'_r = W_d[e]^T dy_sfd[src_r], then dg_r and
  *   dG | dU as in occult_expert_bwd.
  *   dgu_epd out bf16 [T*k, 2I];  dg_epd out fp32 [T*k];
+ *   dy_epd  out bf16, nullable: the gathered dy rows written to their padded EPD
+ *           copy (OCCULT_EPD_PAD), for occult_expert_wgrad_down.
  *   ws      occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
  */
 int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
                              const int32_t* epd_src, const float* epd_gate,
                              const int32_t* exp_off, const int32_t* placement, const void* w2,
-                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* ws,
-                             size_t ws_bytes, occult_stream_t stream);
+                             const void* gu_epd, void* dgu_epd, float* dg_epd, void* dy_epd,
+                             void* ws, size_t ws_bytes, occult_stream_t stream);
 
 /*
  * occult_expert_dgrad_up -- dx rows [dG | dU]_r . [W_g; W_u] (fp32).
@@ -520,9 +541,13 @@ int occult_expert_dgrad_up(const occult_desc_t* desc, const void* dgu_epd, const
  * occult_expert_wgrad_down -- dw2[e] = sum over e's EPD rows r of
  *   dy_sfd[src_r] h'_r^T, out fp32 [Ne, d, I] (written; zeros for experts
  *   without rows).
+ *   dy_epd  nullable: the padded EPD copy of the dy rows that
+ *           occult_expert_dgrad_down wrote; given, it is read as tiles and
+ *           dy_sfd / epd_src are not read (may be NULL); NULL: the rows are
+ *           gathered from dy_sfd through epd_src.  Both give the same bits.
  */
 int occult_expert_wgrad_down(const occult_desc_t* desc, const void* dy_sfd,
-                             const int32_t* epd_src, const int32_t* exp_off,
+                             const int32_t* epd_src, const void* dy_epd, const int32_t* exp_off,
                              const int32_t* placement, const void* h_epd, float* dw2,
                              occult_stream_t stream);
 
@@ -530,9 +555,13 @@ int occult_expert_wgrad_down(const occult_desc_t* desc, const void* dy_sfd,
  * occult_expert_wgrad_up -- dw1[e] = sum over e's EPD rows r of
  *   [dG | dU]_r x_sfd[src_r]^T, out fp32 [Ne, 2I, d] (written; zeros for experts
  *   without rows).
+ *   x_epd  nullable: the padded EPD copy of the x rows (OCCULT_EPD_PAD), as
+ *          occult_expert_up writes it; given, its rows are read as tiles and
+ *          x_sfd / epd_src are not read (may be NULL); NULL: the rows are
+ *          gathered from x_sfd through epd_src.  Both give the same bits.
  */
 int occult_expert_wgrad_up(const occult_desc_t* desc, const void* x_sfd, const int32_t* epd_src,
-                           const int32_t* exp_off, const int32_t* placement,
+                           const void* x_epd, const int32_t* exp_off, const int32_t* placement,
                            const void* dgu_epd, float* dw1, occult_stream_t stream);
 
 /*

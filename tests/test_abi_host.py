@@ -101,8 +101,8 @@ def test_calls_reject_bad_arguments_before_launching(occ):
     assert L.occult_route(ctypes.byref(good), null, null, null, null, null, null) == -1
     assert L.occult_build_brim(ctypes.byref(good), *([null] * 12), ctypes.c_size_t(0), null) == -1
     assert L.occult_dispatch(ctypes.byref(good), *([null] * 6)) == -1
-    assert L.occult_expert_up(ctypes.byref(good), *([null] * 9)) == -1
-    assert L.occult_expert_bwd(ctypes.byref(good), *([null] * 16), ctypes.c_size_t(0), null) == -1
+    assert L.occult_expert_up(ctypes.byref(good), *([null] * 10)) == -1
+    assert L.occult_expert_bwd(ctypes.byref(good), *([null] * 18), ctypes.c_size_t(0), null) == -1
     assert L.occult_gate_grad(ctypes.byref(good), *([null] * 9)) == -1
     assert L.occult_expert_down(ctypes.byref(good), *([null] * 6)) == -1
     assert L.occult_combine(ctypes.byref(good), *([null] * 9)) == -1

@@ -170,12 +170,47 @@ def test_atomic_and_ordered_merges_agree(occ, name):
     assert (err <= 2 * cfg.top_k * F32_EPS * dx_abs + 1e-30).all()
 
 
+def padded_rows(occ, moe):
+    """Row of the padded EPD copy that every EPD row goes to, and the copy's
+    zero padding rows (up to a whole number of EPD_PAD rows a slot)."""
+    off = moe.exp_off.cpu().numpy().astype(np.int64)
+    n = np.diff(off)
+    slot = np.repeat(np.arange(n.size), n)
+    prow = np.arange(off[-1]) + occ.EPD_PAD * slot
+    pad = [np.arange(off[s] + occ.EPD_PAD * s + n[s],
+                     off[s] + occ.EPD_PAD * s + -(-n[s] // occ.EPD_PAD) * occ.EPD_PAD)
+           for s in range(n.size)]
+    return torch.as_tensor(prow, device="cuda"), torch.as_tensor(np.concatenate(pad),
+                                                                 device="cuda")
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_padded_epd_copies(occ, name):
+    """The training up-projection and the dgrad through W_d write the rows they
+    gather to the padded EPD copies x_epd and dy_epd: EPD row r of slot s at row
+    r + EPD_PAD s, bit for bit the SFD row epd_src[r], and zeros after each slot's
+    rows up to a whole number of EPD_PAD rows (what the weight gradients read
+    past a slot's end)."""
+    cfg = CASES[name]
+    case = make_case(cfg)
+    dy = synth.upstream_grad(cfg, device="cuda")
+    moe, _ = train_step(occ, case, dy)
+    prow, pad = padded_rows(occ, moe)
+    src = moe.epd_src.long()
+    assert torch.equal(moe.x_epd[prow], moe.x_sfd[src])
+    assert torch.equal(moe.dy_epd[prow], moe.dy_sfd[src])
+    assert pad.numel() > 0
+    assert not moe.x_epd[pad].any() and not moe.dy_epd[pad].any()
+
+
 @pytest.mark.parametrize("name", ["train_slice_1024", "pair_ragged"])
 def test_split_backward_equals_fused(occ, name):
     """The four backward GEMMs called one by one (occult_expert_dgrad_down,
     _dgrad_up, _wgrad_down, _wgrad_up) give the fused call's results: the weight
-    and gate gradients bit for bit, dx (fp32 atomic adds in no fixed order)
-    within 2 k 2^-24 sum|rows|; so does the ordered form (EPD rows + combine)."""
+    and gate gradients bit for bit, whether the weight gradients gather their
+    rows from the SFD buffers or read the padded EPD copies; dx (fp32 atomic adds
+    in no fixed order) within 2 k 2^-24 sum|rows|; so does the ordered form (EPD
+    rows + combine)."""
     cfg = CASES[name]
     case = make_case(cfg)
     dy = synth.upstream_grad(cfg, device="cuda")
@@ -184,17 +219,26 @@ def test_split_backward_equals_fused(occ, name):
     dg_epd = moe.dg_epd.clone()
     dgu = torch.empty_like(moe.dgu_epd)
     dg2 = torch.empty_like(moe.dg_epd)
+    dy_epd = torch.full_like(moe.dy_epd, float("nan"))
     dx2 = torch.full_like(moe.dx, float("nan"))
     dw1_2 = torch.full_like(moe.dw1, float("nan"))
     dw2_2 = torch.full_like(moe.dw2, float("nan"))
     occ.occult_expert_dgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
-                                 moe.placement, moe.w["w2"], moe.gu_epd, dgu, dg2, moe.bwd_ws)
+                                 moe.placement, moe.w["w2"], moe.gu_epd, dgu, dg2, moe.bwd_ws,
+                                 dy_epd=dy_epd)
     occ.occult_expert_dgrad_up(ds, dgu, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
                                dx2, sfd_tok=moe.sfd_tok, zero_dx=True)
     occ.occult_expert_wgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.exp_off, moe.placement,
                                  moe.h_epd, dw2_2)
     occ.occult_expert_wgrad_up(ds, moe.x_sfd, moe.epd_src, moe.exp_off, moe.placement, dgu,
                                dw1_2)
+    # the same from the padded EPD copies (the SFD buffers not passed)
+    dw1_3 = torch.full_like(moe.dw1, float("nan"))
+    dw2_3 = torch.full_like(moe.dw2, float("nan"))
+    occ.occult_expert_wgrad_down(ds, None, None, moe.exp_off, moe.placement, moe.h_epd, dw2_3,
+                                 dy_epd=dy_epd)
+    occ.occult_expert_wgrad_up(ds, None, None, moe.exp_off, moe.placement, dgu, dw1_3,
+                               x_epd=moe.x_epd)
     # the ordered form: fp32 EPD rows, merged by the combine
     dx_epd = torch.empty(cfg.T * cfg.top_k, cfg.d, dtype=torch.float32, device="cuda")
     occ.occult_expert_dgrad_up(ds, dgu, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
@@ -205,6 +249,9 @@ def test_split_backward_equals_fused(occ, name):
     assert occ.device_error() == 0
     assert torch.equal(dgu, moe.dgu_epd) and torch.equal(dg2, dg_epd)
     assert (dw1_2.cpu().numpy() == dw1).all() and (dw2_2.cpu().numpy() == dw2).all()
+    assert (dw1_3.cpu().numpy() == dw1).all() and (dw2_3.cpu().numpy() == dw2).all()
+    prow, _ = padded_rows(occ, moe)
+    assert torch.equal(dy_epd[prow], moe.dy_epd[prow])
     dx_abs = np.zeros((cfg.T, cfg.d))
     tok = moe.sfd_tok.cpu().numpy()[moe.epd_src.cpu().numpy()]
     scatter_add_rows(dx_abs, tok, np.abs(dx_epd.cpu().numpy().astype(np.float64)))
