@@ -286,6 +286,7 @@ static int expert_down(const LaunchCtx& ctx, const occult_desc_t* desc, const vo
   g.K = desc->inter;
   g.out_src = out_src;
   g.out_tok = out_tok;
+  g.out_rows = out_tok ? desc->T : 0;
   return desc->dtype == OCCULT_BF16 ? launch_grouped_gemm_bf16(ctx, g)
                                     : launch_grouped_gemm_f32(ctx, g);
 }
@@ -456,6 +457,7 @@ static int dgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void*
   if (sfd_tok) {
     h.out_src = epd_src;
     h.out_tok = sfd_tok;
+    h.out_rows = desc->T;
   }
   return launch_grouped_gemm_bf16(ctx, h);
 }

@@ -43,6 +43,7 @@
 // stored K x MN); both use the 128-byte swizzle.  Every wait is bounded (2 s).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -173,10 +174,23 @@ struct Params {
   const int32_t* out_src;      // fp32 reduce: SFD row of every output row
   const int32_t* out_tok;      // fp32 reduce: token (output row) of every SFD row
   int* dev_err;
+  int n_win;                   // forward / dgrad: each segment's units split into n_win
+                               // windows, visited window-major (n_win * n_seg <= 256)
 };
 
 __device__ __forceinline__ int seg_at(const Params& p, int s) {
   return p.seg_off ? p.seg_off[s] : (s ? p.single_rows : 0);
+}
+
+// Units (a pair: two M tiles) of segment s, and the first unit of its window w
+// of n_win: the windows split each segment's units evenly, in order.
+template <bool PAIR>
+__device__ __forceinline__ int seg_units(const Params& p, int s) {
+  const int mt = (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
+  return PAIR ? (mt + 1) / 2 : mt;
+}
+__device__ __forceinline__ int win_first(int units, int w, int n_win) {
+  return static_cast<int>((static_cast<int64_t>(w) * units) / n_win);
 }
 
 // The i-th unit a CTA (pair) takes.  Forward and dgrad units cost the same
@@ -212,7 +226,7 @@ struct TileInfo {
 // rounded up to 16 (each CTA holds half of the rows), so a segment's last unit
 // computes no more than 15 padding rows.  m0 / rows are then this CTA's half of
 // the rows (m0 = t0 when that half is empty), nt the weight block.
-template <bool WGRAD, bool PAIR, bool SWAP = false>
+template <bool WGRAD, bool PAIR, bool SWAP = false, bool WIN = false>
 __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const int* mt_off,
                                                 int rank) {
   TileInfo ti;
@@ -234,23 +248,30 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
   } else {
     const int mt = tau / p.n_tiles_n;
     ti.nt = tau - mt * p.n_tiles_n;
-    // largest s with mt_off[s] <= mt (segments without tiles are skipped)
-    int lo = 0, hi = p.n_seg;
+    // largest window v with mt_off[v] <= mt (windows without tiles are skipped);
+    // v = w * n_seg + s, whose units start at unit win_first(w) of segment s.
+    // Without windows v is the segment and its units start at its first row.
+    int lo = 0, hi = WIN ? p.n_win * p.n_seg : p.n_seg;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (mt_off[mid] <= mt) lo = mid; else hi = mid;
     }
-    ti.seg = lo;
+    int seg = lo, u = mt - mt_off[lo];
+    if constexpr (WIN) {
+      seg = lo % p.n_seg;
+      u += win_first(seg_units<PAIR>(p, seg), lo / p.n_seg, p.n_win);
+    }
+    ti.seg = seg;
     if (SWAP) {
-      ti.t0 = seg_at(p, lo) + (mt - mt_off[lo]) * (2 * BM);
-      ti.urows = min(2 * BM, seg_at(p, lo + 1) - ti.t0);
+      ti.t0 = seg_at(p, seg) + u * (2 * BM);
+      ti.urows = min(2 * BM, seg_at(p, seg + 1) - ti.t0);
       ti.nmma = (ti.urows + 15) & ~15;
       const int half = ti.nmma / 2;
       ti.rows = max(0, min(half, ti.urows - rank * half));
       ti.m0 = ti.rows > 0 ? ti.t0 + rank * half : ti.t0;
     } else {
-      ti.m0 = seg_at(p, lo) + (PAIR ? 2 * (mt - mt_off[lo]) + rank : mt - mt_off[lo]) * BM;
-      ti.rows = min(BM, seg_at(p, lo + 1) - ti.m0);
+      ti.m0 = seg_at(p, seg) + (PAIR ? 2 * u + rank : u) * BM;
+      ti.rows = min(BM, seg_at(p, seg + 1) - ti.m0);
       if (PAIR && ti.rows <= 0) {
         ti.m0 -= BM;
         ti.rows = 0;
@@ -398,6 +419,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr bool kGatherMN = AM == OP_GATHER_MN || BMODE == OP_GATHER_MN;
   constexpr bool kGatherCp = kGather && !kGatherMN;
   constexpr bool kCopyA = copies_a(AM, EPI, WGRAD, SWAP);
+  // the merges visit their units window-major (Params::n_win)
+  constexpr bool kWin = EPI == EPI_F32_RED;
+  const int n_win = kWin ? p.n_win : 1;
   // a stage is released by the MMAs' commit and, when the A rows are copied out,
   // by the copy warp once its store has read them
   const bool copy_a = kCopyA && p.a_copy != nullptr;
@@ -453,14 +477,23 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0) {
     if (lane == 0) {
       if (!WGRAD) {
-        // M-tile (pair: two-tile unit) prefix over segments (at most 256)
+        // M-tile (pair: two-tile unit) prefix over the windows of the segments,
+        // window-major (at most 256 windows in all)
         int acc = 0;
-        for (int s = 0; s < p.n_seg; ++s) {
-          tail->mt_off[s] = acc;
-          const int mt = (seg_at(p, s + 1) - seg_at(p, s) + BM - 1) / BM;
-          acc += PAIR ? (mt + 1) / 2 : mt;
+        if constexpr (kWin) {
+          for (int v = 0; v < n_win * p.n_seg; ++v) {
+            tail->mt_off[v] = acc;
+            const int s = v % p.n_seg, w = v / p.n_seg;
+            const int units = seg_units<PAIR>(p, s);
+            acc += win_first(units, w + 1, n_win) - win_first(units, w, n_win);
+          }
+        } else {
+          for (int s = 0; s < p.n_seg; ++s) {
+            tail->mt_off[s] = acc;
+            acc += seg_units<PAIR>(p, s);
+          }
         }
-        tail->mt_off[p.n_seg] = acc;
+        tail->mt_off[n_win * p.n_seg] = acc;
       }
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
@@ -479,7 +512,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   tc_fence_after();
 
   const int total = WGRAD ? p.n_seg * (PAIR ? p.n_tiles_m / 2 : p.n_tiles_m) * p.n_tiles_n
-                          : tail->mt_off[p.n_seg] * p.n_tiles_n;
+                          : tail->mt_off[n_win * p.n_seg] * p.n_tiles_n;
   const uint32_t tbase = tail->tmem_base;
   volatile int* abort_flag = &tail->abort_flag;
   // the even CTA's full and accumulator-empty barriers, as cluster addresses
@@ -492,7 +525,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
       const int n0 = ti.nt * (kSwiGLU ? BN / 2 : BN);
       for (int kb = 0; kb < ti.kb; ++kb) {
         if (!mbar_wait(&tail->empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
@@ -583,7 +616,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       int it = 0;
       bool ok = true;
       for (int tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++it, unit0, n_units)) {
-        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
         const int a = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!(PAIR ? mbar_wait_cluster(&tail->tempty[a], aph ^ 1u, abort_flag)
@@ -632,7 +665,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       uint32_t phase = 0;
       bool ok = true;
       for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
-        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
         for (int kb = 0; kb < ti.kb; ++kb) {
           if (!mbar_wait(&tail->gfull[stage], phase, abort_flag)) { ok = false; break; }
           fence_proxy_async_smem();
@@ -664,7 +697,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     int it = 0;
     bool ok = true;
     for (int tau = unit0; tau < total; tau = unit_at<WGRAD>(++it, unit0, n_units)) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
       const int a = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       const bool valid = row < ti.rows;
@@ -682,7 +715,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (it == 0 && valid && c0 < p.N_out) gu_prefetch_l2(gu_row, p.half_n, p.N_out - c0);
         const int tau_n = unit_at<WGRAD>(it + 1, unit0, n_units);
         if (tau_n < total) {
-          const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP>(tau_n, p, tail->mt_off, rank);
+          const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau_n, p, tail->mt_off, rank);
           const int cn = tn.nt * BN + half * (BN / 2);
           if (row < tn.rows && cn < p.N_out)
             gu_prefetch_l2(p.gu_in + (tn.m0 + row) * ld_gu + cn, p.half_n, p.N_out - cn);
@@ -921,7 +954,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           } else {
             const int tau_n = unit_at<WGRAD>(it + 1, unit0, n_units);
             if (tau_n < total) {
-              const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP>(tau_n, p, tail->mt_off, rank);
+              const TileInfo tn = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau_n, p, tail->mt_off, rank);
               if (gu_chunks(tn) > 0) {
                 gu_load(gslot ^ 1, tn, 0);
                 gnext = true;
@@ -1066,7 +1099,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
       auto load_idx = [&](int kb) -> int {
         const int r = ti.k0 + kb * BK + 16 * gw + (lane & 15);
         return r < ti.k1 ? p.gather[r] : p.g_rows;
@@ -1116,7 +1149,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t phase = 0;
     bool ok = true;
     for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
-      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+      const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
       // K-major rows (forward / dgrad A): lane l copies 16-byte chunk (l % 8) of
       // rows (l / 8) + 4 i, i < 8, of this warp's 32 rows; chunk c of row r lands
       // at r*128 + ((c ^ (r % 8)) * 16)
@@ -1171,7 +1204,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       const int chunk = lane & 7, rsub = lane >> 3;
       for (int i = 0, tau = unit0; tau < total && ok; tau = unit_at<WGRAD>(++i, unit0, n_units)) {
-        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP>(tau, p, tail->mt_off, rank);
+        const TileInfo ti = decode_tile<WGRAD, PAIR, SWAP, kWin>(tau, p, tail->mt_off, rank);
         __nv_bfloat16* dst = p.a_copy + (static_cast<int64_t>(ti.m0) + OCCULT_EPD_PAD * ti.seg) * p.K;
         for (int kb = 0; kb < ti.kb; ++kb) {
           uint64_t* landed = PAIR && !leader ? &tail->gfull[stage] : &tail->full[stage];
@@ -1319,6 +1352,14 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
 
 }  // namespace
 
+// Largest part of a merged output that one window of units adds into.  On the
+// 32768-token training shape (y: 268 MB fp32) two windows took the swapped
+// down-projection from 970 to 945 us and four to 958 us (each window reads W_d
+// again); the dgrad through [W_g; W_u] re-reads twice the weights and ran
+// slower with windows (1455 us; 1484 with two, 1543 with four): none there.
+constexpr int64_t kMergeWindowBytesSwap = int64_t(160) << 20;
+constexpr int64_t kMergeWindowBytesRows = int64_t(1) << 62;
+
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
   if (!g.wgrad && g.K % BK != 0) return OCCULT_ERR_UNSUPPORTED;
@@ -1378,6 +1419,17 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.seg_off = g.seg_off;
   p.seg_group = g.seg_group;
   p.n_seg = g.n_seg;
+  // The merges add into an fp32 output of out_rows x N_out that need not fit in
+  // L2: each segment's rows (token order) are split into windows visited
+  // window-major, so that the rows being added to at a time span about
+  // 1 / n_win of the tokens (at the price of reading the weights n_win times).
+  p.n_win = 1;
+  if (epi_eff == EPI_F32_RED && g.seg_off && g.out_rows > 0) {
+    const int64_t out_bytes = g.out_rows * g.N_out * 4;
+    const int64_t win_bytes = swap ? kMergeWindowBytesSwap : kMergeWindowBytesRows;
+    const int64_t want = (out_bytes + win_bytes - 1) / win_bytes;
+    p.n_win = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, kMaxSeg / g.n_seg)));
+  }
   p.single_rows = static_cast<int>(g.max_rows);
   p.K = g.K;
   p.N_out = g.N_out;

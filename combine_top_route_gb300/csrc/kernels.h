@@ -110,6 +110,7 @@ struct GroupedGemm {
   float* dg_part = nullptr;           // EPI_SWIGLU_BWD: [rows, 2 * ceil(N_out/256)]
   const int32_t* out_src = nullptr;   // EPI_F32_RED: SFD row of every output row
   const int32_t* out_tok = nullptr;   // EPI_F32_RED: token of every SFD row
+  int64_t out_rows = 0;               // EPI_F32_RED: rows of the merged output (tokens)
 };
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g);
