@@ -5,10 +5,10 @@
 
 One step = one training step of the layer (the default workload, ``olmoe_train``):
 the forward path (route -> BRIM build -> dispatch -> grouped SwiGLU expert GEMMs
--> merge of the expert outputs) and its backward (dispatch of dy -> the four
-backward GEMMs -> gate and router-logit gradients) over one batch of the
-OLMoE-shaped bf16 training workload (T=32768, d=2048, Ne=64, k=8, I=1024,
-Nd=16 virtual devices), with the Algorithm 1 placement from a 16384-token
+-> merge of the expert outputs) and its backward (dispatch of dy to its padded
+EPD rows -> the four backward GEMMs -> gate and router-logit gradients) over one
+batch of the OLMoE-shaped bf16 training workload (T=32768, d=2048, Ne=64, k=8,
+I=1024, Nd=16 virtual devices), with the Algorithm 1 placement from a 16384-token
 profiling batch computed through the library (the batch routed and its
 co-activation counted on the GPU, Algorithm 1 on the host; reported under
 "offline", not timed).  ``--config olmoe_fwd`` and the others time the forward
@@ -449,15 +449,17 @@ def run_ours(args, cfg, world, rank, local):
         raise SystemExit("the timed training step runs single-source")
     if train:
         calls += [
-            ("dispatch_dy", lambda: occ.occult_dispatch(ds, dy, moe.brim0, moe.vmask, moe.dy_sfd,
-                                                        None, stream)),
+            # one source: dy straight to the padded EPD rows the backward GEMMs read
+            ("dispatch_dy", lambda: occ.occult_dispatch_epd(ds, dy, moe.ids, moe.placement,
+                                                            moe.brim0, moe.seg_off, moe.brim1,
+                                                            moe.exp_off, moe.dy_epd, stream)),
         ]
         # the expert backward as its four GEMMs (each timed on its own)
         if atomic:
             calls.append(("zero_dx", lambda: occ.occult_zero_f32(moe.dx, stream)))
         calls += [
             ("dgrad_down", lambda: occ.occult_expert_dgrad_down(
-                ds, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
+                ds, None, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
                 moe.w["w2"], moe.gu_epd, moe.dgu_epd, moe.dg_epd, moe.bwd_ws, dy_epd=moe.dy_epd,
                 stream=stream)),
             ("dgrad_up", lambda: occ.occult_expert_dgrad_up(
@@ -604,14 +606,13 @@ def run_ours(args, cfg, world, rank, local):
         work["shared_ffn"] = (6.0 * d * S * T, 3 * S * d * b + T * d * b + T * S * b + T * d * 4)
     if train:
         # the backward's four GEMMs, twice the forward's FLOPs in all.  Bytes of each:
-        #  dgrad_down  W_d, the gathered dy rows, G|U read, dG|dU and the padded
-        #              EPD copy of the dy rows written
+        #  dgrad_down  W_d, dy's padded EPD rows, G|U read, dG|dU written
         #  dgrad_up    dG|dU, [W_g; W_u], dx written once (merged) or fp32 EPD rows
         #  wgrad_down  the dy rows' EPD copy, h', dW_d written in fp32
         #  wgrad_up    dG|dU, the x rows' EPD copy, dW_g|u written in fp32
         Ne = cfg.n_experts
-        work["dgrad_down"] = (2.0 * d * I * n_epd, Ne * d * I * b + n_sfd * d * b
-                              + 2 * n_epd * 2 * I * b + n_epd * d * b)
+        work["dgrad_down"] = (2.0 * d * I * n_epd, Ne * d * I * b + n_epd * d * b
+                              + 2 * n_epd * 2 * I * b)
         work["dgrad_up"] = (4.0 * d * I * n_epd, n_epd * 2 * I * b + Ne * 2 * I * d * b
                             + (T * d * 4 if atomic else n_epd * d * 4))
         work["wgrad_down"] = (2.0 * d * I * n_epd, n_epd * d * b + n_epd * I * b + Ne * d * I * 4)
@@ -627,7 +628,7 @@ def run_ours(args, cfg, world, rank, local):
             kernels[c]["GB/s"] = n * 4 / per_call[c] / 1e6
             hbm_kernels.append(c)
     if train:
-        kernels["dispatch_dy"]["GB/s"] = (T * d * b + n_sfd * d * b) / per_call["dispatch_dy"] / 1e6
+        kernels["dispatch_dy"]["GB/s"] = (T * d * b + n_epd * d * b) / per_call["dispatch_dy"] / 1e6
         hbm_kernels.append("dispatch_dy")
     if sharded:
         # the exchanges read and write every SFD row once; stage one reads the

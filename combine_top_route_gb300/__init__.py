@@ -87,6 +87,7 @@ _SIGNATURES = {
     "occult_build_brim_noalloc": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                  _VP, _VP, _VP, _VP]),
     "occult_dispatch": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "occult_dispatch_epd": (ctypes.c_int, [_D] + [_VP] * 9),
     "occult_expert_up": (ctypes.c_int, [_D] + [_VP] * 10),
     "occult_expert_down": (ctypes.c_int, [_D, _VP, _VP, _VP, _VP, _VP, _VP]),
     "occult_expert_down_merge": (ctypes.c_int, [_D] + [_VP] * 7 + [_I32, _VP]),
@@ -289,6 +290,18 @@ def occult_dispatch(desc, x, brim0, vmask, x_sfd, sfd_tok=None, stream=None):
           _dev(sfd_tok, torch.int32, n_sfd_max, "sfd_tok", nullable=True), _stream(stream))
 
 
+def occult_dispatch_epd(desc, x, ids, placement, brim0, seg_off, brim1, exp_off, x_epd,
+                        stream=None):
+    """Token rows straight to the padded EPD layout (one source; see occult.h)."""
+    T, d, Ne, k, Nd = desc.T, desc.d, desc.n_experts, desc.top_k, desc.n_vdev
+    i32 = torch.int32
+    _call("occult_dispatch_epd", ctypes.byref(desc), _dev(x, desc.torch_dtype, T * d, "x"),
+          _dev(ids, i32, T * k, "ids"), _dev(placement, i32, Ne, "placement"),
+          _dev(brim0, i32, Nd * T, "brim0"), _dev(seg_off, i32, Nd + 1, "seg_off"),
+          _dev(brim1, i32, Ne * T, "brim1"), _dev(exp_off, i32, Ne + 1, "exp_off"),
+          _dev(x_epd, desc.torch_dtype, epd_copy_rows(desc) * d, "x_epd"), _stream(stream))
+
+
 def occult_expert_up(desc, x_sfd, epd_src, epd_gate, exp_off, placement, w1, h_epd, gu_epd=None,
                      x_epd=None, stream=None):
     """h' (and, training, G|U and the padded EPD copy x_epd of the gathered rows)."""
@@ -314,7 +327,8 @@ def occult_expert_bwd(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, placement
     need = workspace_size(desc, WS_EXPERT_BWD)
     _call("occult_expert_bwd", ctypes.byref(desc),
           _dev(x_sfd, dt, n_sfd_max * d, "x_sfd", nullable=x_epd is not None),
-          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd", nullable=dy_epd is not None),
+          _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
           _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
@@ -337,7 +351,8 @@ def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, pla
     need = workspace_size(desc, WS_EXPERT_BWD)
     _call("occult_expert_bwd_merge", ctypes.byref(desc),
           _dev(x_sfd, dt, n_sfd_max * d, "x_sfd", nullable=x_epd is not None),
-          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd"), _dev(epd_src, i32, T * k, "epd_src"),
+          _dev(dy_sfd, dt, n_sfd_max * d, "dy_sfd", nullable=dy_epd is not None),
+          _dev(epd_src, i32, T * k, "epd_src"),
           _dev(epd_gate, f32, T * k, "epd_gate"), _dev(exp_off, i32, Ne + 1, "exp_off"),
           _dev(placement, i32, Ne, "placement"), _dev(w1, dt, Ne * 2 * I * d, "w1"),
           _dev(w2, dt, Ne * d * I, "w2"), _dev(h_epd, dt, T * k * I, "h_epd"),
@@ -357,7 +372,7 @@ def occult_expert_dgrad_down(desc, dy_sfd, epd_src, epd_gate, exp_off, placement
     dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
     need = workspace_size(desc, WS_EXPERT_BWD)
     _call("occult_expert_dgrad_down", ctypes.byref(desc),
-          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd"),
+          _dev(dy_sfd, dt, T * min(k, desc.n_vdev) * d, "dy_sfd", nullable=dy_epd is not None),
           _dev(epd_src, i32, T * k, "epd_src"), _dev(epd_gate, f32, T * k, "epd_gate"),
           _dev(exp_off, i32, Ne + 1, "exp_off"), _dev(placement, i32, Ne, "placement"),
           _dev(w2, dt, Ne * d * I, "w2"), _dev(gu_epd, dt, T * k * 2 * I, "gu_epd"),

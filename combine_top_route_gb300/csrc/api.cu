@@ -226,6 +226,19 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
   return launch_dispatch(ctx, *desc, x, brim0, vmask, x_sfd, sfd_tok);
 }
 
+int occult_dispatch_epd(const occult_desc_t* desc, const void* x, const int32_t* ids,
+                        const int32_t* placement, const int32_t* brim0, const int32_t* seg_off,
+                        const int32_t* brim1, const int32_t* exp_off, void* x_epd,
+                        occult_stream_t stream) {
+  int rc = check(desc);
+  if (rc) return rc;
+  if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
+  OCCULT_REQUIRE(placement && exp_off);
+  OCCULT_REQUIRE(desc->T == 0 || (x && ids && brim0 && seg_off && brim1 && x_epd));
+  OCCULT_CTX(stream);
+  return launch_dispatch_epd(ctx, *desc, x, ids, placement, brim0, seg_off, brim1, exp_off, x_epd);
+}
+
 static int expert_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void* x_sfd,
                      const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                      const int32_t* placement, const void* w1, void* h_epd, void* gu_epd,
@@ -407,7 +420,8 @@ int occult_shared_ffn(const occult_desc_t* desc, const void* x, const void* ws1,
 // entry points; T > 0 here.
 
 // dh' = dy_sfd[src] . W_d (W_d read MN-major), SwiGLU backward -> dG|dU, dg; with
-// dy_epd given, the gathered dy rows are also written to that padded EPD copy
+// dy_epd given, the gathered dy rows are also written to that padded EPD copy.
+// Without dy_sfd the dy rows are read as tiles from dy_epd (occult_dispatch_epd).
 static int dgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const void* dy_sfd,
                       const int32_t* epd_src, const float* epd_gate, const int32_t* exp_off,
                       const int32_t* placement, const void* w2, const void* gu_epd,
@@ -431,6 +445,13 @@ static int dgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const voi
   g.out = dgu_epd; g.ldo = 2ll * I;
   g.gu_in = gu_epd; g.dg_part = dg_part;
   g.a_copy = dy_epd;
+  if (!dy_sfd) {
+    g.a_mode = OP_TMA_K;
+    g.A = dy_epd; g.a_rows = rows + static_cast<int64_t>(OCCULT_EPD_PAD) * Ne;
+    g.a_pad = OCCULT_EPD_PAD;
+    g.gather = nullptr;
+    g.a_copy = nullptr;
+  }
   int rc = launch_grouped_gemm_bf16(ctx, g);
   if (rc) return rc;
   return launch_dg_reduce(ctx, dg_part, static_cast<int>(rows), 2 * ((I + 255) / 256), dg_epd);
@@ -480,7 +501,7 @@ static int wgrad_down(const LaunchCtx& ctx, const occult_desc_t* desc, const voi
   if (dy_epd) {
     w.a_mode = OP_TMA_MN;
     w.A = dy_epd; w.a_rows = rows + static_cast<int64_t>(OCCULT_EPD_PAD) * Ne;
-    w.a_kpad = OCCULT_EPD_PAD;
+    w.a_pad = OCCULT_EPD_PAD;
     w.gather = nullptr;
   }
   w.B = h_epd; w.b_rows = rows; w.b_cols = I;
@@ -509,7 +530,7 @@ static int wgrad_up(const LaunchCtx& ctx, const occult_desc_t* desc, const void*
   if (x_epd) {
     v.b_mode = OP_TMA_MN;
     v.B = x_epd; v.b_rows = rows + static_cast<int64_t>(OCCULT_EPD_PAD) * Ne;
-    v.b_kpad = OCCULT_EPD_PAD;
+    v.b_pad = OCCULT_EPD_PAD;
     v.gather = nullptr;
   }
   v.seg_off = exp_off; v.seg_group = placement; v.n_seg = Ne;
@@ -543,8 +564,8 @@ static int expert_bwd(const occult_desc_t* desc, const void* x_sfd, const void* 
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && w1 && w2 && dw1 && dw2);
-  OCCULT_REQUIRE(desc->T == 0 || ((x_sfd || x_epd) && dy_sfd && epd_src && epd_gate && h_epd &&
-                                  gu_epd && dgu_epd && dx_out && dg_epd));
+  OCCULT_REQUIRE(desc->T == 0 || ((x_sfd || x_epd) && (dy_sfd || dy_epd) && epd_src && epd_gate &&
+                                  h_epd && gu_epd && dgu_epd && dx_out && dg_epd));
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);
@@ -600,7 +621,8 @@ int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,
   if (rc) return rc;
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(exp_off && placement && w2);
-  OCCULT_REQUIRE(desc->T == 0 || (dy_sfd && epd_src && epd_gate && gu_epd && dgu_epd && dg_epd));
+  OCCULT_REQUIRE(desc->T == 0 || ((dy_sfd || dy_epd) && epd_src && epd_gate && gu_epd && dgu_epd &&
+                                  dg_epd));
   const size_t need = expert_bwd_ws_bytes(*desc);
   if (ws_bytes < need || (need > 0 && !ws)) return OCCULT_ERR_WORKSPACE;
   OCCULT_CTX(stream);

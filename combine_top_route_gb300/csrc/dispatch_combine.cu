@@ -2,6 +2,11 @@
 //  * dispatch -- Appendix A.2 Algorithm 4, stage one of scattering (ORI -> SFD):
 //    each token row is read once and written to the SFD row BRIM0 gives it on
 //    every device it uses.
+//  * dispatch to EPD -- with a single source the first all-to-all is the
+//    identity, so stage one, the exchange and the device-local expansion
+//    (Algorithm 5's EPD rows) can be one pass: each token row is read once and
+//    written to the EPD row of each of its experts, in the padded layout the
+//    GEMMs read as tiles.
 //  * combine  -- the two-stage merge: stage one (EPD -> SFD) sums a received
 //    row's local experts (the aggregation of Algorithm 8, done without atomics),
 //    stage two (SFD -> ORI, Algorithm 9) sums the token's devices in order
@@ -52,6 +57,63 @@ dispatch_kernel(const T* __restrict__ x, const int32_t* __restrict__ brim0,
       }
     }
     if (sfd_tok && my_row >= 0) sfd_tok[my_row] = t;
+  }
+}
+
+// Token t's row to the padded EPD row of each of its k experts: slot s =
+// slot_of[ids[t, j]] on device dv = s / n_loc, EPD row exp_off[dv * n_loc] +
+// BRIM1[s][BRIM0[dv][t] - seg_off[dv]] (the device's EPD rows are numbered in
+// slot order, as Algorithm 5 counts them), stored at that row + OCCULT_EPD_PAD * s.
+// The rows after each slot's rows, up to a whole number of OCCULT_EPD_PAD from the
+// slot's start, are zeroed.
+__global__ void __launch_bounds__(kWarps * 32)
+dispatch_epd_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ids,
+                    const int32_t* __restrict__ placement, const int32_t* __restrict__ brim0,
+                    const int32_t* __restrict__ seg_off, const int32_t* __restrict__ brim1,
+                    const int32_t* __restrict__ exp_off, int ntok, int k, int Ne, int n_loc,
+                    int D, __nv_bfloat16* __restrict__ x_epd) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_slot_of[OCCULT_MAX_EXPERTS];
+  for (int s = threadIdx.x; s < Ne; s += blockDim.x) s_slot_of[placement[s]] = s;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int nvec = D / 8;
+  const int warp0 = blockIdx.x * kWarps + (threadIdx.x >> 5), n_warps = gridDim.x * kWarps;
+  for (int t = warp0; t < ntok; t += n_warps) {
+    int my_row = 0;
+    if (lane < k) {
+      const int s = s_slot_of[ids[static_cast<size_t>(t) * k + lane]];
+      const int dv = s / n_loc;
+      const int r_local = brim0[static_cast<size_t>(dv) * ntok + t] - seg_off[dv];
+      my_row = exp_off[dv * n_loc] + brim1[static_cast<size_t>(s) * ntok + r_local] +
+               OCCULT_EPD_PAD * s;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * 4) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nvec) buf[u] = ld_nc_v4(src + v0 + 32 * u);
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        uint4* dst = reinterpret_cast<uint4*>(x_epd + static_cast<size_t>(row) * D);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v0 + 32 * u < nvec) st_v4(dst + v0 + 32 * u, buf[u]);
+      }
+    }
+  }
+  // padding: (slot, row after its rows) pairs, one warp each
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = warp0; i < Ne * OCCULT_EPD_PAD; i += n_warps) {
+    const int s = i / OCCULT_EPD_PAD, j = i - s * OCCULT_EPD_PAD;
+    const int n = exp_off[s + 1] - exp_off[s];
+    const int padded = (n + OCCULT_EPD_PAD - 1) / OCCULT_EPD_PAD * OCCULT_EPD_PAD;
+    if (n + j >= padded) continue;
+    uint4* dst = reinterpret_cast<uint4*>(
+        x_epd + (static_cast<size_t>(exp_off[s]) + OCCULT_EPD_PAD * s + n + j) * D);
+    for (int v = lane; v < nvec; v += 32) st_v4(dst + v, zero);
   }
 }
 
@@ -240,6 +302,19 @@ int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x
   else
     launch_pdl(dispatch_kernel<float>, g, kWarps * 32, 0, ctx.stream, static_cast<const float*>(x),
                brim0, vmask, ds.T, ds.n_vdev, ds.d, static_cast<float*>(x_sfd), sfd_tok);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_dispatch_epd(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
+                        const int32_t* ids, const int32_t* placement, const int32_t* brim0,
+                        const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
+                        void* x_epd) {
+  if (ds.T == 0) return OCCULT_OK;
+  const int g = grid_for(ctx, ds.T);
+  launch_pdl(dispatch_epd_kernel, g, kWarps * 32, 0, ctx.stream,
+             static_cast<const __nv_bfloat16*>(x), ids, placement, brim0, seg_off, brim1, exp_off,
+             ds.T, ds.top_k, ds.n_experts, ds.n_experts / ds.n_vdev, ds.d,
+             static_cast<__nv_bfloat16*>(x_epd));
   return cuda_status(cudaGetLastError());
 }
 

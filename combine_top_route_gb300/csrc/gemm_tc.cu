@@ -155,9 +155,9 @@ struct Params {
   int64_t g_ld;                // its row length (elements)
   int g_rows;                  // its rows (an MN-major gather names row g_rows for a
                                // row past the segment: outside the map, zero-filled)
-  int a_kpad, b_kpad;          // wgrad, MN-major TMA operand: segment s's K rows start
-                               // at seg_off[s] + kpad * s (a padded EPD copy) instead
-                               // of seg_off[s]
+  int a_pad, b_pad;            // TMA operand rows that are EPD rows of segment s (wgrad:
+                               // the K rows; forward / dgrad: A's rows) are read at
+                               // row + pad * s (a padded EPD copy)
   __nv_bfloat16* a_copy;       // copies_a: padded EPD copy of the gathered A rows
                                // ([rows, K]; segment s's rows from seg_off[s] +
                                // OCCULT_EPD_PAD * s), or NULL
@@ -535,8 +535,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) {
           // K row of an MN-major operand: weight rows (dgrad) or EPD rows (wgrad)
           const int krow = WGRAD ? ti.k0 + kb * BK : static_cast<int>(ti.grp * p.b_group_rows) + kb * BK;
-          const int krow_a = WGRAD ? krow + p.a_kpad * ti.seg : krow;
-          const int krow_b = WGRAD ? krow + p.b_kpad * ti.seg : krow;
+          const int krow_a = WGRAD ? krow + p.a_pad * ti.seg : krow;
+          const int krow_b = WGRAD ? krow + p.b_pad * ti.seg : krow;
+          // K-major A rows (forward / dgrad): EPD rows, padded or not
+          const int arow = ti.m0 + (WGRAD ? 0 : p.a_pad * ti.seg);
           if (SWAP) {
             // this CTA's 128 weight rows of the unit's 256 (SwiGLU: 64 gate rows
             // and the 64 up rows of the same units) and 128 rows of its half of
@@ -553,14 +555,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
               const int wrow = static_cast<int>(ti.grp * p.b_group_rows) + ti.nt * BN + rank * BM;
               tma_load_2d_pair(sa, &tmB, kb * BK, wrow, lbar);
             }
-            if (AM == OP_TMA_K) tma_load_2d_pair(sb, &tmA, kb * BK, ti.m0, lbar);
+            if (AM == OP_TMA_K) tma_load_2d_pair(sb, &tmA, kb * BK, arow, lbar);
           } else if (PAIR) {
             // this CTA's A rows and its half of the B tile (SwiGLU: the gate rows
             // in the even CTA, the up rows in the odd one), all counted on the
             // even CTA's barrier
             if (leader) mbar_arrive_expect_tx(bar, kTmaBytes);
             const uint32_t lbar = full_lead + stage * 8;
-            if (AM == OP_TMA_K) tma_load_2d_pair(sa, &tmA, kb * BK, ti.m0, lbar);
+            if (AM == OP_TMA_K) tma_load_2d_pair(sa, &tmA, kb * BK, arow, lbar);
             if (AM == OP_TMA_MN)
               for (int a = 0; a < BM / 64; ++a)
                 tma_load_2d_pair(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow_a, lbar);
@@ -575,7 +577,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
           } else {
             mbar_arrive_expect_tx(bar, kTmaBytes);
             if (AM == OP_TMA_K) {
-              tma_load_2d(sa, &tmA, kb * BK, ti.m0, bar);
+              tma_load_2d(sa, &tmA, kb * BK, arow, bar);
             } else if (AM == OP_TMA_MN) {
               for (int a = 0; a < BM / 64; ++a) tma_load_2d(sa + a * kMnAtomBytes, &tmA, ti.m0 + 64 * a, krow_a, bar);
             }
@@ -1443,8 +1445,8 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   p.g_ld = a_gathered ? g.a_cols : g.b_cols;
   p.g_rows = static_cast<int>(a_gathered ? g.a_rows : g.b_rows);
   p.b_group_rows = g.b_group_rows;
-  p.a_kpad = g.a_kpad;
-  p.b_kpad = g.b_kpad;
+  p.a_pad = g.a_pad;
+  p.b_pad = g.b_pad;
   p.a_copy = static_cast<__nv_bfloat16*>(g.a_copy);
   p.half_n = g.epi == EPI_SWIGLU ? g.N_out : (g.epi == EPI_SWIGLU_BWD ? g.N_out : 0);
   p.row_gate = g.row_gate;
@@ -1478,6 +1480,7 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32)           // down-projections
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_K, EPI_F32_RED)       // down-projection + merge
     OCCULT_ROWS_GEMM(OP_GATHER_K, OP_TMA_MN, EPI_SWIGLU_BWD)  // dgrad through W_d
+    OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_SWIGLU_BWD)     // the same, dy rows in EPD order
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32)          // dgrad through [W_g; W_u]
     OCCULT_ROWS_GEMM(OP_TMA_K, OP_TMA_MN, EPI_F32_RED)      // the same + merge of dx
 #undef OCCULT_ROWS_GEMM

@@ -23,6 +23,11 @@ size_t brim_ws_bytes(const occult_desc_t& ds);
 
 int launch_dispatch(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
                     const int32_t* brim0, const uint32_t* vmask, void* x_sfd, int32_t* sfd_tok);
+// token rows (bf16) to the padded EPD layout (OCCULT_EPD_PAD), one pass
+int launch_dispatch_epd(const LaunchCtx& ctx, const occult_desc_t& ds, const void* x,
+                        const int32_t* ids, const int32_t* placement, const int32_t* brim0,
+                        const int32_t* seg_off, const int32_t* brim1, const int32_t* exp_off,
+                        void* x_epd);
 
 int launch_combine(const LaunchCtx& ctx, const occult_desc_t& ds, const float* y_epd,
                    const int32_t* brim0, const int32_t* seg_off, const int32_t* brim1,
@@ -89,7 +94,9 @@ struct GroupedGemm {
   const void* B = nullptr;
   int64_t b_rows = 0, b_cols = 0;  // B as stored
   const int32_t* gather = nullptr;
-  int a_kpad = 0, b_kpad = 0;         // wgrad: K rows of segment s at seg_off[s] + kpad * s
+  int a_pad = 0, b_pad = 0;           // operand rows that are EPD rows of segment s (wgrad:
+                                      // its K rows; forward / dgrad: A's rows) are read at
+                                      // row + pad * s (a padded EPD copy)
   void* a_copy = nullptr;             // gathered K-major A (training up-projection, dgrad
                                       // through W_d): padded EPD copy of its rows, or NULL
   int64_t b_group_rows = 0;

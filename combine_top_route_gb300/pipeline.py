@@ -31,7 +31,8 @@ import torch
 from . import (MAX_SOURCES, OCCULT_BF16, OCCULT_F32, ROUTE_DEVICE_LIMITED, ROUTE_EXACT,
                ROUTE_SCORE_PRUNED, ROUTE_SIMILARITY_PRUNED, WS_BUILD_BRIM, WS_EXPERT_BWD,
                occult_all_to_all, occult_build_brim, occult_combine, occult_combine_sfd,
-               occult_desc_t, occult_dispatch, occult_expert_bwd, occult_expert_down,
+               occult_desc_t, occult_dispatch, occult_dispatch_epd, occult_expert_bwd,
+               occult_expert_down,
                occult_expert_down_merge, occult_expert_bwd_merge,
                occult_expert_up, occult_gate_grad, occult_merge_sfd, occult_route,
                occult_route_similarity, occult_router_grad, occult_shard_plan,
@@ -125,7 +126,9 @@ class OccultMoE:
             # padded EPD order, so that the weight gradients read them as tiles
             self.x_epd = e(epd_copy_rows(desc), d, dtype=dt)
             self.dy_epd = e(epd_copy_rows(desc), d, dtype=dt)
-            self.dy_sfd = e(n_sfd_max, d, dtype=dt)
+            # dy's SFD rows only with source shards (one source: dy goes straight
+            # to dy_epd)
+            self.dy_sfd = e(n_sfd_max, d, dtype=dt) if src_off is not None else None
             self.dgu_epd = e(T * k, 2 * I, dtype=dt)
             # fp32 EPD rows of dx only for the ordered merge
             self.dx_epd = e(T * k, d, dtype=f32) if merge == "ordered" else None
@@ -261,18 +264,24 @@ class OccultMoE:
         """Gradients of sum(dy * y) after `forward` (train=True): (dx, dw1, dw2, dgates);
         the gradient of the router logits is left in ``self.dlogits`` [T, Ne].
 
-        dy [T, d] in the layer dtype.  Stage one of scattering sends dy to the SFD
-        rows (BRIM0), the expert backward runs on the EPD rows (BRIM1), and the
-        two-stage merge brings dx back to the tokens; dgates return through
-        BRIM0 -> BRIM1 as well, and on through the softmax of Eq. 2 to the logits
-        the forward was given.
+        dy [T, d] in the layer dtype.  With one source the exchange is the
+        identity, so dy goes in one pass to the padded EPD rows (BRIM0 -> BRIM1)
+        that the backward GEMMs read as tiles; with source shards stage one sends
+        it to the SFD rows and the first exchange moves them.  The expert backward
+        runs on the EPD rows, and the two-stage merge brings dx back to the
+        tokens; dgates return through BRIM0 -> BRIM1 as well, and on through the
+        softmax of Eq. 2 to the logits the forward was given.
         """
         if not self.train:
             raise RuntimeError("OccultMoE was built without train=True")
         ds = self.desc
         if ds.n_shared:
             raise NotImplementedError("backward of shared experts is not provided")
-        self._scatter(dy, self.dy_sfd, None, stream)
+        if self.src_off is None:
+            occult_dispatch_epd(ds, dy, self.ids, self.placement, self.brim0, self.seg_off,
+                                self.brim1, self.exp_off, self.dy_epd, stream)
+        else:
+            self._scatter(dy, self.dy_sfd, None, stream)
         if self.merge == "atomic":
             occult_expert_bwd_merge(ds, self.x_sfd, self.dy_sfd, self.epd_src, self.epd_gate,
                                     self.exp_off, self.placement, self.w["w1"], self.w["w2"],

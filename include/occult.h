@@ -303,6 +303,23 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
                     occult_stream_t stream);
 
 /*
+ * occult_dispatch_epd -- stage one of scattering, the (identity) exchange of a
+ * single source and the device-local expansion in one pass: token t's row goes
+ * to the EPD row of each of its experts (Algorithm 5's numbering: slot s of
+ * expert ids[t, j] on device dv = s / n_loc, row exp_off[dv * n_loc] +
+ * brim1[s][brim0[dv][t] - seg_off[dv]]), in the padded layout (OCCULT_EPD_PAD):
+ *   x_epd[row + OCCULT_EPD_PAD * s] = x[t], and zeros in each slot's padding.
+ * Used for the upstream gradient dy, whose only readers are the backward GEMMs.
+ *   x       [T, d] bf16;  ids int32 [T, k] from occult_route;
+ *   x_epd   out bf16 [T*k + OCCULT_EPD_PAD*Ne, d].
+ * bf16 layers only.
+ */
+int occult_dispatch_epd(const occult_desc_t* desc, const void* x, const int32_t* ids,
+                        const int32_t* placement, const int32_t* brim0, const int32_t* seg_off,
+                        const int32_t* brim1, const int32_t* exp_off, void* x_epd,
+                        occult_stream_t stream);
+
+/*
  * occult_expert_up -- scattering sparse matmul (Algorithm 6, stage two of
  * scattering, SFD -> EPD) fused with the SwiGLU activation and the weight
  * modulation of Algorithm 7:
@@ -475,9 +492,11 @@ int occult_all_to_all(const occult_desc_t* desc, int32_t n_src, const int32_t* c
  *   x_epd   nullable: the padded EPD copy of the x rows that occult_expert_up
  *           wrote; given, dw1 reads it as tiles (x_sfd may then be NULL); NULL:
  *           dw1 gathers x_sfd through epd_src.
- *   dy_epd  nullable scratch, bf16 [T*k + OCCULT_EPD_PAD*Ne, d]: given, the
- *           dh' GEMM writes its gathered dy rows there and dw2 reads them as
- *           tiles; NULL: dw2 gathers dy_sfd again.
+ *   dy_epd  nullable, bf16 [T*k + OCCULT_EPD_PAD*Ne, d]: with dy_sfd given, a
+ *           scratch copy that the dh' GEMM writes its gathered dy rows to and
+ *           dw2 reads as tiles (NULL: dw2 gathers dy_sfd again); with dy_sfd
+ *           NULL, the input: dy in the padded EPD layout (occult_dispatch_epd),
+ *           read as tiles by dh' and dw2.
  *   Both choices give the same bits.
  *   ws  occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
  */
@@ -514,8 +533,10 @@ int occult_expert_bwd_merge(const occult_desc_t* desc, const void* x_sfd, const 
  * occult_expert_dgrad_down -- dh'_r = W_d[e]^T dy_sfd[src_r], then dg_r and
  *   dG | dU as in occult_expert_bwd.
  *   dgu_epd out bf16 [T*k, 2I];  dg_epd out fp32 [T*k];
- *   dy_epd  out bf16, nullable: the gathered dy rows written to their padded EPD
- *           copy (OCCULT_EPD_PAD), for occult_expert_wgrad_down.
+ *   dy_epd  with dy_sfd given: out bf16, nullable, the gathered dy rows written
+ *           to their padded EPD copy (OCCULT_EPD_PAD), for
+ *           occult_expert_wgrad_down; with dy_sfd NULL: the input, dy in the
+ *           padded EPD layout (occult_dispatch_epd), read as tiles.
  *   ws      occult_workspace_size(OCCULT_WS_EXPERT_BWD) bytes.
  */
 int occult_expert_dgrad_down(const occult_desc_t* desc, const void* dy_sfd,

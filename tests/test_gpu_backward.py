@@ -186,11 +186,12 @@ def padded_rows(occ, moe):
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_padded_epd_copies(occ, name):
-    """The training up-projection and the dgrad through W_d write the rows they
-    gather to the padded EPD copies x_epd and dy_epd: EPD row r of slot s at row
-    r + EPD_PAD s, bit for bit the SFD row epd_src[r], and zeros after each slot's
-    rows up to a whole number of EPD_PAD rows (what the weight gradients read
-    past a slot's end)."""
+    """The padded EPD layouts: EPD row r of slot s at row r + EPD_PAD s, zeros
+    after each slot's rows up to a whole number of EPD_PAD rows (what the weight
+    gradients read past a slot's end).  x_epd, written by the training
+    up-projection from the rows it gathers, holds x_sfd[epd_src[r]] bit for bit;
+    dy_epd, written by occult_dispatch_epd straight from dy, holds dy[token of r]
+    (the token of SFD row epd_src[r], as occult_dispatch numbered them)."""
     cfg = CASES[name]
     case = make_case(cfg)
     dy = synth.upstream_grad(cfg, device="cuda")
@@ -198,7 +199,7 @@ def test_padded_epd_copies(occ, name):
     prow, pad = padded_rows(occ, moe)
     src = moe.epd_src.long()
     assert torch.equal(moe.x_epd[prow], moe.x_sfd[src])
-    assert torch.equal(moe.dy_epd[prow], moe.dy_sfd[src])
+    assert torch.equal(moe.dy_epd[prow], dy[moe.sfd_tok.long()[src]])
     assert pad.numel() > 0
     assert not moe.x_epd[pad].any() and not moe.dy_epd[pad].any()
 
@@ -207,28 +208,38 @@ def test_padded_epd_copies(occ, name):
 def test_split_backward_equals_fused(occ, name):
     """The four backward GEMMs called one by one (occult_expert_dgrad_down,
     _dgrad_up, _wgrad_down, _wgrad_up) give the fused call's results: the weight
-    and gate gradients bit for bit, whether the weight gradients gather their
-    rows from the SFD buffers or read the padded EPD copies; dx (fp32 atomic adds
-    in no fixed order) within 2 k 2^-24 sum|rows|; so does the ordered form (EPD
-    rows + combine)."""
+    and gate gradients bit for bit, whether the GEMMs gather dy and x rows from
+    the SFD buffers (dy dispatched with occult_dispatch here) or read the padded
+    EPD layouts as tiles; dx (fp32 atomic adds in no fixed order) within
+    2 k 2^-24 sum|rows|; so does the ordered form (EPD rows + combine)."""
     cfg = CASES[name]
     case = make_case(cfg)
     dy = synth.upstream_grad(cfg, device="cuda")
     moe, (dx, dw1, dw2, dgates) = train_step(occ, case, dy)   # the fused call
     ds = moe.desc
     dg_epd = moe.dg_epd.clone()
+    dgu_fused = moe.dgu_epd.clone()
+    # dy's SFD rows, as the sharded path and the gathering GEMMs take them
+    dy_sfd = torch.empty_like(moe.x_sfd)
+    occ.occult_dispatch(ds, dy, moe.brim0, moe.vmask, dy_sfd)
+    # dh' from dy's padded EPD rows (the fused call's input), once more
+    dgu_t = torch.empty_like(moe.dgu_epd)
+    dg_t = torch.empty_like(moe.dg_epd)
+    occ.occult_expert_dgrad_down(ds, None, moe.epd_src, moe.epd_gate, moe.exp_off, moe.placement,
+                                 moe.w["w2"], moe.gu_epd, dgu_t, dg_t, moe.bwd_ws,
+                                 dy_epd=moe.dy_epd)
     dgu = torch.empty_like(moe.dgu_epd)
     dg2 = torch.empty_like(moe.dg_epd)
     dy_epd = torch.full_like(moe.dy_epd, float("nan"))
     dx2 = torch.full_like(moe.dx, float("nan"))
     dw1_2 = torch.full_like(moe.dw1, float("nan"))
     dw2_2 = torch.full_like(moe.dw2, float("nan"))
-    occ.occult_expert_dgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
+    occ.occult_expert_dgrad_down(ds, dy_sfd, moe.epd_src, moe.epd_gate, moe.exp_off,
                                  moe.placement, moe.w["w2"], moe.gu_epd, dgu, dg2, moe.bwd_ws,
                                  dy_epd=dy_epd)
     occ.occult_expert_dgrad_up(ds, dgu, moe.epd_src, moe.exp_off, moe.placement, moe.w["w1"],
                                dx2, sfd_tok=moe.sfd_tok, zero_dx=True)
-    occ.occult_expert_wgrad_down(ds, moe.dy_sfd, moe.epd_src, moe.exp_off, moe.placement,
+    occ.occult_expert_wgrad_down(ds, dy_sfd, moe.epd_src, moe.exp_off, moe.placement,
                                  moe.h_epd, dw2_2)
     occ.occult_expert_wgrad_up(ds, moe.x_sfd, moe.epd_src, moe.exp_off, moe.placement, dgu,
                                dw1_2)
@@ -247,7 +258,8 @@ def test_split_backward_equals_fused(occ, name):
     occ.occult_combine(ds, dx_epd, moe.brim0, moe.seg_off, moe.brim1, moe.exp_off, dx3)
     torch.cuda.synchronize()
     assert occ.device_error() == 0
-    assert torch.equal(dgu, moe.dgu_epd) and torch.equal(dg2, dg_epd)
+    assert torch.equal(dgu, dgu_fused) and torch.equal(dg2, dg_epd)
+    assert torch.equal(dgu_t, dgu_fused) and torch.equal(dg_t, dg_epd)
     assert (dw1_2.cpu().numpy() == dw1).all() and (dw2_2.cpu().numpy() == dw2).all()
     assert (dw1_3.cpu().numpy() == dw1).all() and (dw2_3.cpu().numpy() == dw2).all()
     prow, _ = padded_rows(occ, moe)
