@@ -258,8 +258,10 @@ __device__ __forceinline__ TileInfo decode_tile(int tau, const Params& p, const 
     }
     int seg = lo, u = mt - mt_off[lo];
     if constexpr (WIN) {
-      seg = lo % p.n_seg;
-      u += win_first(seg_units<PAIR>(p, seg), lo / p.n_seg, p.n_win);
+      if (p.n_win > 1) {
+        seg = lo % p.n_seg;
+        u += win_first(seg_units<PAIR>(p, seg), lo / p.n_seg, p.n_win);
+      }
     }
     ti.seg = seg;
     if (SWAP) {
@@ -475,26 +477,33 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     }
   }
   if (warp == 0) {
-    if (lane == 0) {
-      if (!WGRAD) {
-        // M-tile (pair: two-tile unit) prefix over the windows of the segments,
-        // window-major (at most 256 windows in all)
-        int acc = 0;
-        if constexpr (kWin) {
-          for (int v = 0; v < n_win * p.n_seg; ++v) {
-            tail->mt_off[v] = acc;
-            const int s = v % p.n_seg, w = v / p.n_seg;
-            const int units = seg_units<PAIR>(p, s);
-            acc += win_first(units, w + 1, n_win) - win_first(units, w, n_win);
-          }
-        } else {
-          for (int s = 0; s < p.n_seg; ++s) {
-            tail->mt_off[s] = acc;
-            acc += seg_units<PAIR>(p, s);
-          }
+    if (!WGRAD) {
+      // M-tile (pair: two-tile unit) prefix over the windows of the segments,
+      // window-major (at most 256 windows in all): the lanes load 32 windows'
+      // segment bounds at a time and scan their unit counts
+      const int nv = n_win * p.n_seg;
+      int carry = 0;
+      for (int v0 = 0; v0 < nv; v0 += 32) {
+        const int v = v0 + lane;
+        int c = 0;
+        if (v < nv) {
+          const int sg = kWin ? v % p.n_seg : v;
+          const int units = seg_units<PAIR>(p, sg);
+          c = kWin ? win_first(units, v / p.n_seg + 1, n_win) - win_first(units, v / p.n_seg, n_win)
+                   : units;
         }
-        tail->mt_off[n_win * p.n_seg] = acc;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (v < nv) tail->mt_off[v] = carry + incl - c;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
+      if (lane == 0) tail->mt_off[nv] = carry;
+    }
+    if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (EPI == EPI_SWIGLU_BWD && !SWAP) {
@@ -1354,13 +1363,13 @@ int launch_tc(const LaunchCtx& ctx, const CUtensorMap& ma, const CUtensorMap& mb
 
 }  // namespace
 
-// Largest part of a merged output that one window of units adds into.  On the
-// 32768-token training shape (y: 268 MB fp32) two windows took the swapped
-// down-projection from 970 to 945 us and four to 958 us (each window reads W_d
-// again); the dgrad through [W_g; W_u] re-reads twice the weights and ran
-// slower with windows (1455 us; 1484 with two, 1543 with four): none there.
-constexpr int64_t kMergeWindowBytesSwap = int64_t(160) << 20;
-constexpr int64_t kMergeWindowBytesRows = int64_t(1) << 62;
+// Largest part of the merged down-projection's output that one window of units
+// adds into.  On the 32768-token training shape (y: 268 MB fp32) two windows
+// took the plain units from 947 to 918-930 us (swapped units 1005 -> 988 us, and
+// four windows were slower than two: each window reads W_d again).  The dgrad through [W_g; W_u]
+// re-reads twice the weights and ran slower with windows (1455 us; 1484 with
+// two, 1543 with four): it keeps one.
+constexpr int64_t kMergeWindowBytes = int64_t(160) << 20;
 
 int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   if (g.n_seg > kMaxSeg || g.N_out % 32 != 0) return OCCULT_ERR_UNSUPPORTED;
@@ -1388,9 +1397,14 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // slower there, 164 vs 135 us for the DeepSeek decode up-projection).
   const int epi_eff = g.epi == EPI_F32 && g.out_tok ? EPI_F32_RED
                     : (g.epi == EPI_SWIGLU && g.gu_out ? EPI_SWIGLU_SAVE : g.epi);
+  // The merged down-projection keeps plain units when segments are long (~4096
+  // rows an expert on the 32768-token training shape: 947 us plain against
+  // 1005 us swapped, one window each), where a unit's padding is small and the
+  // merge epilogue needs no transpose.
   const bool swap = pair && !g.wgrad && g.seg_off && g.b_mode == OP_TMA_K &&
                     ((epi_eff == EPI_SWIGLU && g.a_mode == OP_GATHER_K && !g.gu_out) ||
-                     ((epi_eff == EPI_F32 || epi_eff == EPI_F32_RED) && g.a_mode == OP_TMA_K));
+                     ((epi_eff == EPI_F32 || (epi_eff == EPI_F32_RED && avg_rows < 2048)) &&
+                      g.a_mode == OP_TMA_K));
   CUtensorMap ma, mb;
   int rc = operand_map(&ma, am, g.A, g.a_rows, g.a_cols, BM);
   if (rc) return rc;
@@ -1425,11 +1439,11 @@ int launch_grouped_gemm_bf16(const LaunchCtx& ctx, const GroupedGemm& g) {
   // L2: each segment's rows (token order) are split into windows visited
   // window-major, so that the rows being added to at a time span about
   // 1 / n_win of the tokens (at the price of reading the weights n_win times).
+  // Only the down-projection's merge (weights K-major, W_d) takes windows.
   p.n_win = 1;
-  if (epi_eff == EPI_F32_RED && g.seg_off && g.out_rows > 0) {
+  if (epi_eff == EPI_F32_RED && g.seg_off && g.out_rows > 0 && g.b_mode == OP_TMA_K) {
     const int64_t out_bytes = g.out_rows * g.N_out * 4;
-    const int64_t win_bytes = swap ? kMergeWindowBytesSwap : kMergeWindowBytesRows;
-    const int64_t want = (out_bytes + win_bytes - 1) / win_bytes;
+    const int64_t want = (out_bytes + kMergeWindowBytes - 1) / kMergeWindowBytes;
     p.n_win = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, kMaxSeg / g.n_seg)));
   }
   p.single_rows = static_cast<int>(g.max_rows);
