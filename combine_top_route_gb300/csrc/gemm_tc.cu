@@ -21,10 +21,17 @@
 // each SM instead of 48 KB and six stages fit.  The routed forward GEMMs swap the
 // operands (weights on the MMA's M, the segment's rows on its N, a runtime N of
 // the unit's rows rounded up to 16), so a segment's last unit carries at most 15
-// padding rows instead of up to 255.  Short segments (decode) run one 128 x 256
-// tile per CTA with four 48 KB stages.
+// padding rows instead of up to 255 (the merged down-projection on long segments
+// keeps plain units, visited in token windows).  Short segments (decode) run one
+// 128 x 256 tile per CTA with four 48 KB stages.
 //
-// CTA = 10 warps, plus 4 when an operand is gathered; warp-specialised:
+// Operands whose rows are EPD rows may also come from a padded EPD layout (each
+// segment's rows followed by zero rows up to a multiple of 128), read as plain
+// TMA tiles: the weight gradients' x and dy rows, and the dy rows of the dgrad
+// through W_d.
+//
+// CTA = 10 warps, plus 4 when an operand is gathered (and 1 when the gathered A
+// rows are also copied out to a padded EPD layout); warp-specialised:
 //   warp 0       TMA producer for every operand held as a plain 2-D matrix.
 //   warp 1       owns TMEM (512 columns = two 128x256 fp32 accumulators, double-
 //                buffered so one tile's epilogue overlaps the next main loop);
@@ -36,9 +43,13 @@
 //   warps 10..13 producers for a gathered operand (rows picked by the condensed
 //                BRIM1): K-major rows (forward, dgrad) by cp.async, written
 //                straight into the 128-byte swizzle the tensor cores read and
-//                zero-filled past a segment's end (TMA tile::gather4 measured 2.3x
-//                slower there); MN-major rows (weight gradients) by TMA
-//                tile::gather4, four 128-byte rows an instruction.
+//                zero-filled past a unit's rows (TMA tile::gather4 measured 2.3x
+//                slower there); MN-major rows (weight gradients without the
+//                padded layouts) by TMA tile::gather4, four 128-byte rows an
+//                instruction.
+//   warp 14      (the training up-projection, and the dgrad through W_d when it
+//                gathers) copies the gathered A rows of a stage to the padded
+//                EPD copy before the stage is released.
 // Operands are K-major (rows along K) or MN-major (rows along K of a matrix
 // stored K x MN); both use the 128-byte swizzle.  Every wait is bounded (2 s).
 #include <cudaTypedefs.h>

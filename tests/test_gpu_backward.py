@@ -204,6 +204,37 @@ def test_padded_epd_copies(occ, name):
     assert not moe.x_epd[pad].any() and not moe.dy_epd[pad].any()
 
 
+@pytest.mark.parametrize("name,T", [("deepseek_decode_limited", 512), ("olmoe_fwd_score_pruned", 1024),
+                                    ("olmoe_fwd", 3)])
+def test_dispatch_epd_under_other_routings(occ, name, T):
+    """occult_dispatch_epd follows the EPD numbering the BRIM build gives under
+    device-limited and score-pruned routing, and on a 3-token batch where most
+    experts get no row (no padding then): every EPD row holds dy[token of the
+    row] bit for bit, every padding row zero; T = 0 is accepted and writes
+    nothing."""
+    cfg = synth.CONFIGS[name].with_(T=T)
+    case = make_case(cfg)
+    ds = occ.desc_for(cfg)
+    moe = occ.OccultMoE(ds, case.weights, torch.as_tensor(case.placement))
+    moe.forward(case.logits.cuda(), case.x)
+    dy = synth.upstream_grad(cfg, device="cuda")
+    dy_epd = torch.full((occ.epd_copy_rows(ds), cfg.d), float("nan"), dtype=torch.bfloat16,
+                        device="cuda")
+    occ.occult_dispatch_epd(ds, dy, moe.ids, moe.placement, moe.brim0, moe.seg_off, moe.brim1,
+                            moe.exp_off, dy_epd)
+    torch.cuda.synchronize()
+    assert occ.device_error() == 0
+    prow, pad = padded_rows(occ, moe)
+    assert torch.equal(dy_epd[prow], dy[moe.sfd_tok.long()[moe.epd_src.long()]])
+    assert not dy_epd[pad].any()
+    before = dy_epd.clone()
+    empty = occ.desc_for(cfg.with_(T=0))
+    occ.occult_dispatch_epd(empty, dy[:0], moe.ids[:0], moe.placement, moe.brim0, moe.seg_off,
+                            moe.brim1, moe.exp_off, dy_epd)
+    torch.cuda.synchronize()
+    assert torch.equal(dy_epd.view(torch.int16), before.view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["train_slice_1024", "pair_ragged"])
 def test_split_backward_equals_fused(occ, name):
     """The four backward GEMMs called one by one (occult_expert_dgrad_down,
