@@ -222,6 +222,9 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
   int rc = check(desc);
   if (rc) return rc;
   OCCULT_REQUIRE(desc->T == 0 || (x && brim0 && vmask && x_sfd));
+  // rows move as 16-byte vectors
+  OCCULT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(x_sfd) % 16 == 0);
   OCCULT_CTX(stream);
   return launch_dispatch(ctx, *desc, x, brim0, vmask, x_sfd, sfd_tok);
 }
@@ -235,6 +238,8 @@ int occult_dispatch_epd(const occult_desc_t* desc, const void* x, const int32_t*
   if (desc->dtype != OCCULT_BF16) return OCCULT_ERR_UNSUPPORTED;
   OCCULT_REQUIRE(placement && exp_off);
   OCCULT_REQUIRE(desc->T == 0 || (x && ids && brim0 && seg_off && brim1 && x_epd));
+  OCCULT_REQUIRE(reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(x_epd) % 16 == 0);
   OCCULT_CTX(stream);
   return launch_dispatch_epd(ctx, *desc, x, ids, placement, brim0, seg_off, brim1, exp_off, x_epd);
 }

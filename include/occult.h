@@ -294,8 +294,9 @@ int occult_build_brim_noalloc(const occult_desc_t* desc, const int32_t* ids, con
  * occult_dispatch -- Algorithm 4: x_sfd[brim0[d, t]] = x[t] for every
  * non-negative entry (stage one of scattering, ORI -> SFD).  The result is the
  * first all-to-all's send buffer, segment d going to virtual device d.
- *   x        [T, d] layer dtype.
- *   x_sfd    out [T*min(k,Nd), d] layer dtype; rows >= N_sfd untouched.
+ *   x        [T, d] layer dtype, 16-byte aligned.
+ *   x_sfd    out [T*min(k,Nd), d] layer dtype, 16-byte aligned; rows >= N_sfd
+ *            untouched.
  *   sfd_tok  out int32 [T*min(k,Nd)] ORI token of each SFD row (nullable).
  */
 int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* brim0,
@@ -310,8 +311,8 @@ int occult_dispatch(const occult_desc_t* desc, const void* x, const int32_t* bri
  * brim1[s][brim0[dv][t] - seg_off[dv]]), in the padded layout (OCCULT_EPD_PAD):
  *   x_epd[row + OCCULT_EPD_PAD * s] = x[t], and zeros in each slot's padding.
  * Used for the upstream gradient dy, whose only readers are the backward GEMMs.
- *   x       [T, d] bf16;  ids int32 [T, k] from occult_route;
- *   x_epd   out bf16 [T*k + OCCULT_EPD_PAD*Ne, d].
+ *   x       [T, d] bf16, 16-byte aligned;  ids int32 [T, k] from occult_route;
+ *   x_epd   out bf16 [T*k + OCCULT_EPD_PAD*Ne, d], 16-byte aligned.
  * bf16 layers only.
  */
 int occult_dispatch_epd(const occult_desc_t* desc, const void* x, const int32_t* ids,

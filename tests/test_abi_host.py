@@ -126,6 +126,12 @@ def test_calls_reject_bad_arguments_before_launching(occ):
     assert L.occult_similarity_accumulate(ctypes.byref(good), v, -1, v, null) == -1
     assert L.occult_similarity_finish(ctypes.byref(good), null, v, null) == -1
     assert L.occult_router_grad(ctypes.byref(good), v, null, v, v, null) == -1
+    # the row-moving dispatches refuse rows that are not 16-byte aligned
+    odd = ctypes.c_void_p(16 + 2)
+    assert L.occult_dispatch(ctypes.byref(good), odd, v, v, v, null, null) == -1
+    assert L.occult_dispatch(ctypes.byref(good), v, v, v, odd, null, null) == -1
+    assert L.occult_dispatch_epd(ctypes.byref(good), odd, v, v, v, v, v, v, v, null) == -1
+    assert L.occult_dispatch_epd(ctypes.byref(good), v, v, v, v, v, v, v, odd, null) == -1
     # stage-split merge and the sharded-source plan and exchange
     assert L.occult_merge_sfd(ctypes.byref(good), v, v, v, v, v, null, null) == -1
     assert L.occult_combine_sfd(ctypes.byref(good), v, null, null, v, null) == -1
