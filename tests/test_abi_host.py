@@ -51,6 +51,29 @@ def declared_arity():
     return out
 
 
+def test_binding_constants_match_the_header(occ):
+    """Every numeric #define of occult.h that the binding mirrors (as OCCULT_X or
+    X) has the same value there; the ones the binding needs are all mirrored."""
+    with open(os.path.join(ROOT, "include", "occult.h")) as f:
+        text = f.read()
+    defines = {m.group(1): int(m.group(2))
+               for m in re.finditer(r"^#define OCCULT_(\w+)\s+(-?\d+)", text, re.M)}
+    mirrored = {}
+    for name, value in defines.items():
+        for attr in ("OCCULT_" + name, name):
+            if hasattr(occ, attr):
+                mirrored[name] = getattr(occ, attr)
+                break
+    for name, value in mirrored.items():
+        assert value == defines[name], f"OCCULT_{name}: header {defines[name]}, binding {value}"
+    needed = {"F32", "BF16", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_WORKSPACE", "ERR_CUDA",
+              "ERR_DEVICE_TIMEOUT", "ROUTE_EXACT", "ROUTE_DEVICE_LIMITED", "ROUTE_SCORE_PRUNED",
+              "ROUTE_SIMILARITY_PRUNED", "MAX_EXPERTS", "MAX_VDEV", "MAX_TOPK", "MAX_SOURCES",
+              "EPD_PAD", "WS_BUILD_BRIM", "WS_PROFILE_COACT", "WS_EXPERT_BWD",
+              "STATIC_SCRATCH_BYTES"}
+    assert needed <= set(mirrored), sorted(needed - set(mirrored))
+
+
 def test_binding_signatures_match_the_header(occ):
     """Every ctypes prototype has as many arguments as its C declaration."""
     arity = declared_arity()
