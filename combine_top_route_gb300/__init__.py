@@ -368,6 +368,8 @@ def occult_expert_bwd_merge(desc, x_sfd, dy_sfd, epd_src, epd_gate, exp_off, pla
 
 def occult_expert_dgrad_down(desc, dy_sfd, epd_src, epd_gate, exp_off, placement, w2, gu_epd,
                              dgu_epd, dg_epd, ws, dy_epd=None, stream=None):
+    """dh', dG|dU and dg; dy rows gathered from dy_sfd (then copied to dy_epd when
+    given), or, with dy_sfd None, read from dy's padded EPD rows dy_epd."""
     T, d, Ne, k, I = desc.T, desc.d, desc.n_experts, desc.top_k, desc.inter
     dt, f32, i32 = desc.torch_dtype, torch.float32, torch.int32
     need = workspace_size(desc, WS_EXPERT_BWD)

@@ -253,7 +253,8 @@ class OccultMoE:
     @property
     def launches_per_backward(self) -> int:
         """Kernels one backward call launches."""
-        # dispatch dy, 2 dgrad GEMMs, dg reduce, 2 wgrad GEMMs, combine, gate grad,
+        # dispatch of dy (one source: to its padded EPD rows), 2 dgrad GEMMs, dg
+        # reduce, 2 wgrad GEMMs, combine, gate grad,
         # router grad (+ 2 exchanges and the split merge when sharded)
         # (atomic merge: the dgrad through [W_g; W_u] merges dx, and the zeroing of
         # dx takes the combine's place)
